@@ -1,0 +1,250 @@
+/*
+ * pst.h -- C ABI of libpst: decode-phase attention over a prefix-shared,
+ * tree-structured, paged KV cache on one GPU (sm_103a).
+ *
+ * Method: CoDec: Prefix-Shared Decoding Kernel for LLMs (papercache.org,
+ * 2026-06): the KV cache is a forest of nodes (a virtual root joins unrelated
+ * prefixes, "KV cache management"); each node's K/V is read from HBM once for
+ * all the queries that share it (KV-guided grouping, DEFT section 3.3); a
+ * partial attention computation (PAC) per node chunk emits a partial output
+ * with its log-sum-exp, and the partial output reduction (POR) merges them per
+ * query ("intra-block primitives", "inter-block launch and tree reduction");
+ * a cost-model partitioner splits long nodes along the KV axis ("workload
+ * balancing").
+ *
+ * Conventions for every call:
+ *   - Return value 0 (PST_OK) on success, a negative PST_E* code on failure.
+ *     No exception crosses the ABI. pst_last_error() gives a message for the
+ *     last failure on the calling thread.
+ *   - Host arrays passed in are read during the call only (copied); the caller
+ *     keeps ownership.
+ *   - Device buffers (Q, pools, O, LSE, workspace) are owned by the caller.
+ *   - A `stream` argument is a cudaStream_t passed as void* (NULL = legacy
+ *     default stream). Device work is asynchronous on that stream; no call
+ *     synchronises the host unless it says so.
+ */
+#ifndef PST_H
+#define PST_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- errors */
+#define PST_OK            0
+#define PST_EINVAL       -1   /* malformed argument (null, negative size, query sees no token) */
+#define PST_ECYCLE       -2   /* parent array has a cycle */
+#define PST_ERANGE       -3   /* parent / page id / offset out of range */
+#define PST_EUNSUPPORTED -4   /* shape the kernels do not cover (d, page size, Hq % Hkv) */
+#define PST_EWORKSPACE   -5   /* workspace missing, too small or misaligned */
+#define PST_ECUDA        -6   /* a CUDA runtime call failed (message has the CUDA error) */
+#define PST_EDEVICE      -7   /* a kernel reported a fault in the device status word */
+#define PST_ENOMEM       -8   /* host allocation failed */
+
+typedef struct pst_tree pst_tree;
+typedef struct pst_plan pst_plan;
+typedef struct pst_timer pst_timer;
+
+typedef enum { PST_BF16 = 0, PST_F32 = 1 } pst_dtype;
+
+/* Split policies of the partitioner (CoDec "workload balancing"). */
+typedef enum {
+    PST_SPLIT_COST_MODEL = 0, /* binary search on the max-block cost + greedy b_k  */
+    PST_SPLIT_NONE       = 1, /* b_k = 1: one chunk per node (DEFT-Node)            */
+    PST_SPLIT_UNIFORM    = 2  /* every node cut into chunks of `fixed_chunk` tokens */
+} pst_split_policy;
+
+typedef struct {
+    int32_t split_policy;   /* pst_split_policy; default PST_SPLIT_COST_MODEL          */
+    int32_t fixed_chunk;    /* tokens per chunk for PST_SPLIT_UNIFORM (multiple of 64)  */
+    int32_t tc_min_rows;    /* rows (queries x GQA group) from which a node runs on the
+                               tensor-core PAC; default 16; fp32 inputs never do      */
+    int32_t pack_masks;     /* 1 (default): pack a page-contiguous subtree of <= 64
+                               tokens into one chunk with a 64-bit causal mask per
+                               query (DEFT bit causal mask); 0: one chunk per node  */
+    int32_t num_sms;        /* 0: ask the current device                              */
+    int32_t slots_per_sm;   /* concurrent PAC thread blocks per SM assumed by the
+                               list schedule; 0: default (1)                         */
+} pst_plan_opts;
+
+/* Fill `o` with the defaults above. */
+void pst_plan_opts_default(pst_plan_opts* o);
+
+/* --------------------------------------------------------------- tree_build
+ * Set up the KV forest (CoDec "KV cache management"; block tables as in the
+ * shared-prefix techniques blog, section 4.3).
+ *
+ *   n_nodes        number of KV nodes N (>= 1)
+ *   node_len[N]    tokens held by each node (>= 0; 0-length nodes are skipped)
+ *   parent[N]      parent node id, or -1 for a child of the virtual root; the
+ *                  edge p -> c means "p is a prefix of c"
+ *   page_ptr[N+1]  CSR offsets into page_ids (page_ptr[0] == 0, non-decreasing)
+ *   page_ids[..]   physical page ids, each in [0, num_pages)
+ *   first_offset   nullable (= all 0): row of the node's first token inside its
+ *                  first listed page; token t of node n lives in page
+ *                  page_ids[page_ptr[n] + (first_offset[n]+t)/page_size], row
+ *                  (first_offset[n]+t) % page_size
+ *   page_size      tokens per page: 16 or 32
+ *   num_pages      pages in the pool
+ *   out            receives the tree handle (free with pst_tree_destroy)
+ *
+ * Errors: PST_EINVAL (null/negative), PST_ECYCLE, PST_ERANGE (parent, page id,
+ * first_offset >= page_size, or a node's tokens overrun its listed pages),
+ * PST_EUNSUPPORTED (page_size).
+ */
+int pst_tree_build(int32_t n_nodes, const int32_t* node_len, const int32_t* parent,
+                   const int64_t* page_ptr, const int32_t* page_ids,
+                   const int32_t* first_offset, int32_t page_size, int64_t num_pages,
+                   pst_tree** out);
+void pst_tree_destroy(pst_tree* t);
+
+/* ---------------------------------------------------------------- plan
+ * KV-guided grouping + partition plan (CoDec "workload balancing"; DEFT
+ * Algorithm 1).
+ *
+ *   tree           from pst_tree_build (not retained: the plan copies what it needs)
+ *   n_queries      decode queries B (>= 1)
+ *   query_node[B]  node each query sits on; it attends every token on the path
+ *                  from the top of its tree down to that node, inclusive
+ *   n_q_heads, n_kv_heads   Hq, Hkv with Hq % Hkv == 0; q-head h reads kv head
+ *                  h / (Hq/Hkv)
+ *   d              head dimension: 64 or 128
+ *   dtype          element type of Q, K_pool and V_pool
+ *   opts           nullable: defaults
+ *   out            receives the plan (free with pst_plan_destroy)
+ *
+ * The plan is immutable and reusable for any number of pst_decode_attn calls
+ * while the tree topology, node lengths and page tables stay unchanged.
+ * Errors: PST_EINVAL (query out of range, a query that sees no token),
+ * PST_EUNSUPPORTED (d, Hq % Hkv), PST_ECUDA (device query when num_sms == 0).
+ */
+int pst_plan_create(const pst_tree* tree, int32_t n_queries, const int32_t* query_node,
+                    int32_t n_q_heads, int32_t n_kv_heads, int32_t d, pst_dtype dtype,
+                    const pst_plan_opts* opts, pst_plan** out);
+void pst_plan_destroy(pst_plan* p);
+
+/* Bytes of device workspace the plan needs: its metadata plus the partial
+ * output scratch (fp32 partial outputs and log-sum-exps). */
+int64_t pst_plan_workspace_bytes(const pst_plan* p);
+
+/* Copy the plan's metadata into the caller-owned device workspace (one
+ * host-to-device copy on `stream`) and bind the workspace to the plan. The
+ * workspace must stay allocated and unused by anything else while the plan
+ * is used. d_workspace must be 256-byte aligned.
+ * Errors: PST_EWORKSPACE (null, too small, misaligned), PST_ECUDA. */
+int pst_plan_upload(pst_plan* p, void* d_workspace, int64_t bytes, void* stream);
+
+/* ---------------------------------------------------------------- decode_attn
+ * Tree decode attention on `stream` (asynchronous):
+ *   O[b][h][:] = softmax(q_{b,h} K_b^T / sqrt(d)) V_b,
+ *   LSE[b][h]  = ln sum_j exp(q_{b,h} . k_j / sqrt(d)),
+ * where K_b, V_b are the tokens on query b's path (CoDec "background"; DEFT
+ * section 3.2 for the LSE).
+ *
+ *   Q       device [B][Hq][d], dtype of the plan
+ *   K_pool  device [num_pages][Hkv][page_size][d], dtype of the plan, 16-byte aligned
+ *   V_pool  same layout as K_pool
+ *   O       device fp32 [B][Hq][d]
+ *   LSE     device fp32 [B][Hq], natural log
+ *
+ * Page rows not covered by any node may hold any finite or non-finite values;
+ * they are never read into the result. Requires a prior pst_plan_upload.
+ * Errors: PST_EWORKSPACE (no upload), PST_EINVAL (null pointer), PST_ECUDA
+ * (launch failure). Device-side faults detected by the kernels' own checks
+ * are reported by pst_plan_check_status().
+ */
+int pst_decode_attn(const pst_plan* p, const void* Q, const void* K_pool, const void* V_pool,
+                    float* O, float* LSE, void* stream);
+
+/* Read and clear the device status word written by the kernels' bounds and
+ * wait-limit checks (synchronises `stream`). 0 = clean, PST_EDEVICE = a
+ * kernel gave up; *code (nullable) receives the raw word. */
+int pst_plan_check_status(const pst_plan* p, void* stream, int32_t* code);
+
+/* ---------------------------------------------------------------- timing
+ * Per-kernel device times of pst_decode_attn, for roofline accounting. A timer
+ * holds CUDA events for up to `max_calls` calls; pst_decode_attn_timed records
+ * an event before the first kernel and after each kernel on `stream`.
+ * pst_timer_read synchronises on the last event, writes the summed
+ * milliseconds per kernel slot into ms[0..n-1], the number of timed calls into
+ * *calls, and resets the timer. Kernel slot names: pst_timer_kernel_name(). */
+int pst_timer_create(int32_t max_calls, pst_timer** out);
+void pst_timer_destroy(pst_timer* t);
+int pst_decode_attn_timed(const pst_plan* p, const void* Q, const void* K_pool,
+                          const void* V_pool, float* O, float* LSE, void* stream,
+                          pst_timer* timer);
+int pst_timer_read(pst_timer* t, float* ms, int32_t n, int32_t* calls);
+const char* pst_timer_kernel_name(int32_t slot);
+
+/* ---------------------------------------------------------------- introspection */
+typedef struct {
+    double  plan_us;              /* host time of pst_plan_create                    */
+    double  predicted_makespan_us;/* list-schedule makespan under the cost model     */
+    double  cost_lower_bound_us;  /* binary-searched lower bound cost_l              */
+    int64_t n_chunks;             /* KV chunks (a node part or a packed subtree)     */
+    int64_t n_items;              /* PAC thread blocks: chunk x kv head x row block  */
+    int64_t n_tc_items;           /* ... on the tensor-core PAC                      */
+    int64_t n_cc_items;           /* ... on the CUDA-core PAC                        */
+    int64_t n_partial_rows;       /* partial outputs written per call                */
+    int64_t unique_kv_tokens;     /* sum of node lengths                             */
+    int64_t kv_tokens_read;       /* tokens loaded per kv head (chunks' page span)   */
+    int64_t workspace_bytes;
+    int32_t num_slots;            /* m: concurrent PAC blocks the schedule assumes    */
+    int32_t n_launches;           /* kernels per pst_decode_attn                      */
+} pst_plan_stats;
+int pst_plan_stats_get(const pst_plan* p, pst_plan_stats* s);
+
+/* Plan export for exact (integer) checks. pst_plan_export_sizes fills the
+ * array lengths; pst_plan_export fills every non-null pointer of `e`, each of
+ * the length given by the sizes.
+ *   qpath:  per query, its nodes root first (QMapKV)
+ *   nodeq:  per node, ascending ids of queries sharing it (KVMapQ)
+ *   chunk_q / chunk_q_mask: per chunk, its queries and, per query, a 64-bit
+ *           visibility mask over the chunk's first 64 tokens (all ones when
+ *           the chunk has no mask)
+ *   chunk_tok_node / chunk_tok_t: per chunk, the (node, token) it covers in
+ *           chunk order
+ *   chunk_kind: 0 CUDA-core PAC, 1 tensor-core PAC
+ *   merge: per query, the partial-row bases merged by POR */
+typedef struct {
+    int64_t n_queries, n_nodes, n_chunks;
+    int64_t n_qpath, n_nodeq, n_chunk_q, n_chunk_tok, n_merge;
+} pst_export_sizes;
+
+typedef struct {
+    int32_t*  qpath_ptr;      /* n_queries + 1 */
+    int32_t*  qpath_node;     /* n_qpath       */
+    int32_t*  nodeq_ptr;      /* n_nodes + 1   */
+    int32_t*  nodeq;          /* n_nodeq       */
+    int32_t*  chunk_q_ptr;    /* n_chunks + 1  */
+    int32_t*  chunk_q;        /* n_chunk_q     */
+    uint64_t* chunk_q_mask;   /* n_chunk_q     */
+    int32_t*  chunk_tok_ptr;  /* n_chunks + 1  */
+    int32_t*  chunk_tok_node; /* n_chunk_tok   */
+    int32_t*  chunk_tok_t;    /* n_chunk_tok   */
+    int32_t*  chunk_kind;     /* n_chunks      */
+    int32_t*  merge_ptr;      /* n_queries + 1 */
+    int32_t*  merge_row;      /* n_merge       */
+} pst_export;
+
+int pst_plan_export_sizes(const pst_plan* p, pst_export_sizes* s);
+int pst_plan_export(const pst_plan* p, pst_export* e);
+
+/* Cost model C_est(rows, tokens) in microseconds for one PAC thread block
+ * (CoDec "profile-based cost estimation"). pst_cost_set_table installs a
+ * table measured on the device: n_r row grid points x n_n token grid points,
+ * values row-major [n_r][n_n], kind 0 = CUDA-core PAC, 1 = tensor-core PAC;
+ * between grid points the estimate is bilinear in (log rows, log tokens).
+ * Process-wide; plans created afterwards use it. */
+int pst_cost_set_table(int32_t kind, int32_t n_r, const float* rows, int32_t n_n,
+                       const float* tokens, const float* us);
+double pst_cost_estimate(int32_t kind, double rows, double tokens);
+
+const char* pst_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PST_H */

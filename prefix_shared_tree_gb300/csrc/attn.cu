@@ -1,0 +1,312 @@
+// Partial output reduction (POR) and the host side of pst_decode_attn:
+// workspace binding, TMA descriptors, launches, timing and status.
+//
+// CoDec, "intra-block primitives", POR: two partial outputs O1, O2 of the same
+// query with maxima m1, m2 and sums s1, s2 merge to m = max(m1, m2),
+// s = s1 e^{m1-m} + s2 e^{m2-m}, O = (O1 s1 e^{m1-m} + O2 s2 e^{m2-m}) / s.
+// CoDec, "inter-block launch and tree reduction": the merge is associative and
+// commutative and the reductions of different queries are independent, so the
+// tree reduction becomes one independent chain per query. Here each partial
+// carries its log-sum-exp (base 2) lse_i = m_i + log2 s_i, which folds the
+// two statistics into one: weights w_i = 2^{lse_i - max lse}; one warp per
+// (query, q-head) merges all of the query's partials at once.
+#include <cudaTypedefs.h>
+
+#include <chrono>
+#include <cmath>
+#include <mutex>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "dev_common.cuh"
+
+namespace pst {
+
+cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const void* tv, const void* Q,
+                          int r_tile, int n_items, int item_off, cudaStream_t st);
+cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
+                          int item_off, cudaStream_t st);
+
+namespace dev {
+
+constexpr int kPorWarps = 8;
+
+template <int D>
+__global__ void __launch_bounds__(kPorWarps * 32) por_kernel(DevPlan P, float* __restrict__ O, float* __restrict__ LSE) {
+    constexpr int EPL = D / 32;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int64_t w = (int64_t)blockIdx.x * kPorWarps + warp;
+    const int Hq = P.n_q_heads;
+    if (w >= (int64_t)P.n_queries * Hq) return;
+    const int q = (int)(w / Hq), h = (int)(w % Hq);
+    const int e0 = P.merge_ptr[q], e1 = P.merge_ptr[q + 1];
+    float M = -INFINITY;
+    for (int e = e0 + lane; e < e1; e += 32) M = fmaxf(M, P.part_lse[P.merge_row[e] + h]);
+#pragma unroll
+    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float acc[EPL];
+#pragma unroll
+    for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
+    float W = 0.f;
+    for (int e = e0; e < e1; ++e) {
+        const int64_t row = (int64_t)P.merge_row[e] + h;
+        const float wt = fast_exp2(P.part_lse[row] - Mu);
+        W += wt;
+        const float* src = P.part_o + row * D + lane * EPL;
+        if constexpr (EPL == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            acc[0] = fmaf(wt, v.x, acc[0]);
+            acc[1] = fmaf(wt, v.y, acc[1]);
+            acc[2] = fmaf(wt, v.z, acc[2]);
+            acc[3] = fmaf(wt, v.w, acc[3]);
+        } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            acc[0] = fmaf(wt, v.x, acc[0]);
+            acc[1] = fmaf(wt, v.y, acc[1]);
+        }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    float* dst = O + w * D + lane * EPL;
+    if constexpr (EPL == 4) {
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    } else {
+        *reinterpret_cast<float2*>(dst) = make_float2(acc[0] * inv, acc[1] * inv);
+    }
+    if (lane == 0) LSE[w] = (M + __log2f(W)) * 0.69314718055994530942f;
+}
+
+}  // namespace dev
+
+int device_sm_count(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(out, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return 0;
+}
+
+static int cuda_fail(const char* what, cudaError_t e) {
+    return fail(PST_ECUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// TMA descriptor over a pool [num_pages][Hkv][page_size][d] viewed as 3-D
+// (d, page row, page*Hkv + head); boxes of one 128-byte slab x 16 rows with the
+// 128B swizzle.
+static int make_pool_map(const pst_plan* p, const void* pool, unsigned char* out) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PST_ECUDA, "decode_attn: cuTensorMapEncodeTiled is unavailable");
+    const int eb = p->dtype == PST_BF16 ? 2 : 4;
+    cuuint64_t dims[3] = {(cuuint64_t)p->d, (cuuint64_t)p->page_size, (cuuint64_t)p->num_pages * p->hkv};
+    cuuint64_t strides[2] = {(cuuint64_t)p->d * eb, (cuuint64_t)p->page_size * p->d * eb};
+    cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)kBoxRows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(reinterpret_cast<CUtensorMap*>(out),
+                    p->dtype == PST_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                    const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PST_ECUDA, "decode_attn: cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return PST_OK;
+}
+
+static DevPlan dev_plan(const pst_plan* p) {
+    uint8_t* b = static_cast<uint8_t*>(p->d_ws);
+    DevPlan d;
+    d.items = reinterpret_cast<const DevItem*>(b + p->ws.items);
+    d.chunks = reinterpret_cast<const DevChunk*>(b + p->ws.chunks);
+    d.pages = reinterpret_cast<const int32_t*>(b + p->ws.pages);
+    d.chunk_q = reinterpret_cast<const int32_t*>(b + p->ws.chunk_q);
+    d.masks = reinterpret_cast<const uint64_t*>(b + p->ws.masks);
+    d.merge_ptr = reinterpret_cast<const int32_t*>(b + p->ws.merge_ptr);
+    d.merge_row = reinterpret_cast<const int32_t*>(b + p->ws.merge_row);
+    d.part_o = reinterpret_cast<float*>(b + p->ws.part_o);
+    d.part_lse = reinterpret_cast<float*>(b + p->ws.part_lse);
+    d.status = reinterpret_cast<int32_t*>(b + p->ws.status);
+    d.n_queries = p->n_queries;
+    d.n_q_heads = p->hq;
+    d.n_kv_heads = p->hkv;
+    d.group = p->group;
+    d.d = p->d;
+    d.page_size = p->page_size;
+    d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->d));
+    return d;
+}
+
+}  // namespace pst
+
+struct pst_timer {
+    int32_t max_calls = 0;
+    int32_t calls = 0;
+    int32_t n_slots = 0;                 // kernels per call in the recorded calls
+    std::vector<cudaEvent_t> ev;         // max_calls x (1 + kMaxKernels)
+    static constexpr int kMaxKernels = 4;
+};
+
+using namespace pst;
+
+extern "C" int pst_plan_upload(pst_plan* p, void* d_ws, int64_t bytes, void* stream) {
+    if (!p) return fail(PST_EINVAL, "plan_upload: plan is null");
+    if (!d_ws) return fail(PST_EWORKSPACE, "plan_upload: workspace is null");
+    if (reinterpret_cast<uintptr_t>(d_ws) % 256) return fail(PST_EWORKSPACE, "plan_upload: workspace must be 256-byte aligned");
+    if (bytes < p->ws.total) return fail(PST_EWORKSPACE, "plan_upload: workspace too small (need " + std::to_string(p->ws.total) + " bytes)");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(d_ws, p->meta_blob.data(), p->meta_blob.size(), cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) return cuda_fail("plan_upload: cudaMemcpyAsync", e);
+    // the host image stays alive with the plan; make the copy complete before returning so the
+    // caller may free nothing early
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail("plan_upload: cudaStreamSynchronize", e);
+    p->d_ws = d_ws;
+    p->tmap_k_ptr = p->tmap_v_ptr = nullptr;
+    return PST_OK;
+}
+
+static int decode_impl(const pst_plan* p, const void* Q, const void* K, const void* V, float* O, float* LSE,
+                       void* stream, pst_timer* timer) {
+    if (!p) return fail(PST_EINVAL, "decode_attn: plan is null");
+    if (!p->d_ws) return fail(PST_EWORKSPACE, "decode_attn: plan has no uploaded workspace");
+    if (!Q || !K || !V || !O || !LSE) return fail(PST_EINVAL, "decode_attn: null tensor pointer");
+    if ((reinterpret_cast<uintptr_t>(K) | reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(Q) |
+         reinterpret_cast<uintptr_t>(O)) % 16)
+        return fail(PST_EINVAL, "decode_attn: Q, K_pool, V_pool and O must be 16-byte aligned");
+    if (p->tmap_k_ptr != K) {
+        int rc = make_pool_map(p, K, p->tmap_k);
+        if (rc) return rc;
+        p->tmap_k_ptr = K;
+    }
+    if (p->tmap_v_ptr != V) {
+        int rc = make_pool_map(p, V, p->tmap_v);
+        if (rc) return rc;
+        p->tmap_v_ptr = V;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const DevPlan dp = dev_plan(p);
+    cudaEvent_t* ev = nullptr;
+    if (timer) {
+        if (timer->calls >= timer->max_calls) return fail(PST_EINVAL, "decode_attn_timed: timer is full");
+        ev = timer->ev.data() + (size_t)timer->calls * (1 + pst_timer::kMaxKernels);
+        cudaEventRecord(ev[0], st);
+    }
+    int slot = 0;
+    cudaError_t e;
+    // slot 0: tensor-core PAC, slot 1: CUDA-core PAC, slot 2: POR
+    if (p->n_tc_items > 0) {
+        e = launch_pac_tc(dp, p->tmap_k, p->tmap_v, Q, (int)p->n_tc_items, 0, st);
+        if (e != cudaSuccess) return cuda_fail("decode_attn: PAC (tensor core) launch", e);
+    }
+    if (ev) cudaEventRecord(ev[++slot], st);
+    for (int k = 0; k < 4; ++k) {
+        if (p->cc_class_cnt[k] == 0) continue;
+        e = launch_pac_cc(dp, p->dtype, p->tmap_k, p->tmap_v, Q, 8 >> k, (int)p->cc_class_cnt[k],
+                          (int)p->cc_class_off[k], st);
+        if (e != cudaSuccess) return cuda_fail("decode_attn: PAC (CUDA core) launch", e);
+    }
+    if (ev) cudaEventRecord(ev[++slot], st);
+    {
+        const int64_t warps = (int64_t)p->n_queries * p->hq;
+        const int blocks = (int)((warps + dev::kPorWarps - 1) / dev::kPorWarps);
+        if (p->d == 128) dev::por_kernel<128><<<blocks, dev::kPorWarps * 32, 0, st>>>(dp, O, LSE);
+        else dev::por_kernel<64><<<blocks, dev::kPorWarps * 32, 0, st>>>(dp, O, LSE);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail("decode_attn: POR launch", e);
+    }
+    if (ev) {
+        cudaEventRecord(ev[++slot], st);
+        timer->n_slots = slot;
+        timer->calls++;
+    }
+    return PST_OK;
+}
+
+extern "C" int pst_decode_attn(const pst_plan* p, const void* Q, const void* K, const void* V, float* O, float* LSE,
+                               void* stream) {
+    return decode_impl(p, Q, K, V, O, LSE, stream, nullptr);
+}
+
+extern "C" int pst_decode_attn_timed(const pst_plan* p, const void* Q, const void* K, const void* V, float* O,
+                                     float* LSE, void* stream, pst_timer* timer) {
+    if (!timer) return fail(PST_EINVAL, "decode_attn_timed: timer is null");
+    return decode_impl(p, Q, K, V, O, LSE, stream, timer);
+}
+
+extern "C" int pst_plan_check_status(const pst_plan* p, void* stream, int32_t* code) {
+    if (!p || !p->d_ws) return fail(PST_EWORKSPACE, "check_status: plan has no workspace");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t word = 0;
+    int32_t* dstatus = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(p->d_ws) + p->ws.status);
+    cudaError_t e = cudaMemcpyAsync(&word, dstatus, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dstatus, 0, 4, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail("check_status", e);
+    if (code) *code = word;
+    if (word) return fail(PST_EDEVICE, "check_status: device status word " + std::to_string(word));
+    return PST_OK;
+}
+
+extern "C" int pst_timer_create(int32_t max_calls, pst_timer** out) {
+    if (!out || max_calls <= 0) return fail(PST_EINVAL, "timer_create: bad argument");
+    pst_timer* t = new (std::nothrow) pst_timer();
+    if (!t) return fail(PST_ENOMEM, "timer_create: out of memory");
+    t->max_calls = max_calls;
+    t->ev.resize((size_t)max_calls * (1 + pst_timer::kMaxKernels), nullptr);
+    for (auto& e : t->ev) {
+        cudaError_t r = cudaEventCreate(&e);
+        if (r != cudaSuccess) {
+            for (auto& x : t->ev) if (x) cudaEventDestroy(x);
+            delete t;
+            return cuda_fail("timer_create: cudaEventCreate", r);
+        }
+    }
+    *out = t;
+    return PST_OK;
+}
+
+extern "C" void pst_timer_destroy(pst_timer* t) {
+    if (!t) return;
+    for (auto& e : t->ev) if (e) cudaEventDestroy(e);
+    delete t;
+}
+
+extern "C" int pst_timer_read(pst_timer* t, float* ms, int32_t n, int32_t* calls) {
+    if (!t) return fail(PST_EINVAL, "timer_read: timer is null");
+    for (int k = 0; k < n; ++k) ms[k] = 0.f;
+    const int stride = 1 + pst_timer::kMaxKernels;
+    if (t->calls > 0) {
+        cudaError_t e = cudaEventSynchronize(t->ev[(size_t)(t->calls - 1) * stride + t->n_slots]);
+        if (e != cudaSuccess) return cuda_fail("timer_read: cudaEventSynchronize", e);
+    }
+    for (int c = 0; c < t->calls; ++c) {
+        for (int k = 0; k < t->n_slots && k < n; ++k) {
+            float x = 0.f;
+            cudaError_t e = cudaEventElapsedTime(&x, t->ev[(size_t)c * stride + k], t->ev[(size_t)c * stride + k + 1]);
+            if (e != cudaSuccess) return cuda_fail("timer_read: cudaEventElapsedTime", e);
+            ms[k] += x;
+        }
+    }
+    if (calls) *calls = t->calls;
+    t->calls = 0;
+    return PST_OK;
+}
+
+extern "C" const char* pst_timer_kernel_name(int32_t slot) {
+    switch (slot) {
+        case 0: return "pac_tc";
+        case 1: return "pac_cc";
+        case 2: return "por";
+        default: return "";
+    }
+}

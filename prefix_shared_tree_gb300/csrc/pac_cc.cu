@@ -1,0 +1,383 @@
+// CUDA-core partial attention computation (PAC) for thin chunks: fewer than
+// 16 query rows (aggregated queries x GQA group) per kv head.
+//
+// CoDec, "intra-block primitives": a PAC computes attention between the
+// queries aggregated on a KV node and that node's K/V, loading each K/V tile
+// into shared memory once for all of them, and emits a partial output with
+// its softmax statistics. CoDec, "KV cache management": node-local
+// stabilisation -- per row a running max m and sum of e^{s-m}, rescaled to
+// the larger max when a new block is folded in.
+//
+// Layout of the work: one thread block per (chunk, kv head, row block of up
+// to 8 rows). A producer warp streams the chunk's pages with TMA into a
+// 2-stage ring (128B-swizzled 16-row boxes). Each of 4 compute warps owns 16
+// rows of every 64-token tile; inside a warp, groups of LPT lanes each take
+// one token at a time with the channels split across the group's lanes
+// (16-byte vector reads of the staged rows). Dot products are reduced across
+// the group with a transposing butterfly, so each lane ends up holding the
+// score of one row; every group keeps its own running (m, l, O) and the
+// groups, then the warps, are merged with the same rescaling rule at the end.
+#include "dev_common.cuh"
+
+namespace pst {
+namespace dev {
+
+constexpr int kCcWarps = 4;
+constexpr int kCcStages = 2;
+
+template <typename T>
+struct ElemTraits;
+template <>
+struct ElemTraits<__nv_bfloat16> {
+    static constexpr int kBytes = 2;
+    // 16-byte chunk -> 8 floats
+    __device__ __forceinline__ static void unpack(const uint4& v, float* out) {
+        out[0] = bf16lo(v.x); out[1] = bf16hi(v.x);
+        out[2] = bf16lo(v.y); out[3] = bf16hi(v.y);
+        out[4] = bf16lo(v.z); out[5] = bf16hi(v.z);
+        out[6] = bf16lo(v.w); out[7] = bf16hi(v.w);
+    }
+};
+template <>
+struct ElemTraits<float> {
+    static constexpr int kBytes = 4;
+    __device__ __forceinline__ static void unpack(const uint4& v, float* out) {
+        out[0] = __uint_as_float(v.x); out[1] = __uint_as_float(v.y);
+        out[2] = __uint_as_float(v.z); out[3] = __uint_as_float(v.w);
+    }
+};
+
+// Sum RT per-lane values over the LPT lanes of a group; afterwards lane j of
+// the group holds the total of value index j >> (log2 LPT - log2 RT). Each
+// butterfly stage with N > 1 live values sends half of them to the partner
+// lane and keeps the other half (transposing as it reduces); once one value
+// is left the remaining stages are plain sums.
+template <int OFF, int N>
+struct ReduceStep {
+    template <int RT>
+    __device__ __forceinline__ static void run(float (&a)[RT], int j) {
+        if constexpr (OFF >= 1) {
+            if constexpr (N > 1) {
+                constexpr int H = N / 2;
+                const bool up = (j & OFF) != 0;
+#pragma unroll
+                for (int i = 0; i < H; ++i) {
+                    const float send = up ? a[i] : a[i + H];
+                    const float keep = up ? a[i + H] : a[i];
+                    a[i] = keep + __shfl_xor_sync(0xffffffffu, send, OFF);
+                }
+                ReduceStep<OFF / 2, H>::run(a, j);
+            } else {
+                a[0] += __shfl_xor_sync(0xffffffffu, a[0], OFF);
+                ReduceStep<OFF / 2, 1>::run(a, j);
+            }
+        }
+    }
+};
+
+template <int LPT, int RT>
+__device__ __forceinline__ float reduce_transpose(float (&a)[RT], int j) {
+    ReduceStep<LPT / 2, RT>::run(a, j);
+    return a[0];
+}
+
+template <int LPT, int RT>
+__device__ __forceinline__ constexpr int owner_shift() {
+    return (LPT == 8 ? 3 : LPT == 16 ? 4 : 5) - (RT == 1 ? 0 : RT == 2 ? 1 : RT == 4 ? 2 : 3);
+}
+static_assert(owner_shift<8, 8>() == 0, "owner shift");
+
+// One chunk x kv head x row block on the compute warps.
+template <typename T, int D, int LPT, int RT>
+__device__ __forceinline__ void cc_consume(const DevPlan& P, const DevChunk& C, int head, int rb, const T* __restrict__ Q,
+                           uint32_t ring, const uint8_t* ring_ptr, uint32_t bar_full, uint32_t bar_empty,
+                           float* scratch) {
+    constexpr int EB = ElemTraits<T>::kBytes;
+    constexpr int ROWB = D * EB;            // bytes per K/V row
+    constexpr int NSLAB = ROWB / 128;
+    constexpr int CHUNKS = ROWB / 16;
+    constexpr int CPL = CHUNKS / LPT;       // 16-byte chunks per lane
+    constexpr int EPC = 16 / EB;            // elements per chunk
+    constexpr int EPL = CPL * EPC;          // elements per lane
+    constexpr int TPI = 32 / LPT;           // tokens per warp step
+    constexpr int BT = 16 / TPI;            // tokens per group per tile
+    constexpr int SH = owner_shift<LPT, RT>();
+    constexpr uint32_t kSlabBytes = kTileTokens * 128;
+    constexpr uint32_t kHalf = NSLAB * kSlabBytes;
+    static_assert(CPL >= 1, "lane mapping");
+
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int grp = lane / LPT, j = lane % LPT;
+    const int G = P.group, Hq = P.n_q_heads;
+    const int rows_total = C.n_q * G;
+    const int own = j >> SH;                // row whose score this lane holds
+
+    // ---- queries of this row block, channels of this lane, pre-scaled to log2 units
+    float q[RT][EPL];
+    uint64_t own_mask = ~0ull;
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+        const int row = rb * RT + r;
+        if (row < rows_total) {
+            const int qi = row / G, gh = row % G;
+            const int qid = P.chunk_q[C.q_base + qi];
+            const T* qrow = Q + ((int64_t)qid * Hq + head * G + gh) * D;
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+                const int gc = j + k * LPT;
+                const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(qrow) + gc * 16);
+                float f[EPC];
+                ElemTraits<T>::unpack(v, f);
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) q[r][k * EPC + e] = f[e] * P.scale_log2;
+            }
+            if (r == own && C.mask_base >= 0) own_mask = P.masks[C.mask_base + qi];
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) q[r][e] = 0.f;
+        }
+    }
+
+    float o[RT][EPL];
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) o[r][e] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;
+
+    const ChunkGeo g = chunk_geo(C);
+    const int owner_base = grp * LPT;
+    bool ok = true;
+    for (int i = 0; i < g.n_tiles; ++i) {
+        const int s = i % kCcStages;
+        if (!mbar_wait(bar_full + 8 * s, (i / kCcStages) & 1, P.status)) { ok = false; break; }
+        const uint8_t* kb = ring_ptr + s * 2 * kHalf;
+        const uint8_t* vb = kb + kHalf;
+        const int tpos = g.tile0 + i * kTileTokens;
+
+        float sc[BT];
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            const int row = warp * 16 + grp + TPI * b;
+            float kf[EPL];
+#pragma unroll
+            for (int k = 0; k < CPL; ++k) {
+                const int gc = j + k * LPT;
+                const uint4 v = *reinterpret_cast<const uint4*>(kb + (gc / 8) * kSlabBytes + swz(row, gc % 8));
+                ElemTraits<T>::unpack(v, kf + k * EPC);
+            }
+            float pd[RT];
+#pragma unroll
+            for (int r = 0; r < RT; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc = fmaf(q[r][e], kf[e], acc);
+                pd[r] = acc;
+            }
+            const float sv = reduce_transpose<LPT, RT>(pd, j);
+            const int pos = tpos + row;
+            const int t = pos - g.pos_begin;
+            bool valid = pos >= g.pos_begin && pos < g.pos_end;
+            if (valid && t < 64) valid = (own_mask >> t) & 1ull;
+            sc[b] = valid ? sv : -INFINITY;
+        }
+        float mb = sc[0];
+#pragma unroll
+        for (int b = 1; b < BT; ++b) mb = fmaxf(mb, sc[b]);
+        const float m_new = fmaxf(m_run, mb);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = fast_exp2(m_run - m_use);
+        float p[BT];
+        float ps = 0.f;
+#pragma unroll
+        for (int b = 0; b < BT; ++b) { p[b] = fast_exp2(sc[b] - m_use); ps += p[b]; }
+        l_run = l_run * alpha + ps;
+        m_run = m_new;
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+            const float ar = __shfl_sync(0xffffffffu, alpha, owner_base + (r << SH));
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[r][e] *= ar;
+        }
+#pragma unroll
+        for (int b = 0; b < BT; ++b) {
+            const int row = warp * 16 + grp + TPI * b;
+            const int pos = tpos + row;
+            const bool tok_ok = pos >= g.pos_begin && pos < g.pos_end;
+            float pr[RT];
+#pragma unroll
+            for (int r = 0; r < RT; ++r) pr[r] = __shfl_sync(0xffffffffu, p[b], owner_base + (r << SH));
+            if (tok_ok) {
+                float vf[EPL];
+#pragma unroll
+                for (int k = 0; k < CPL; ++k) {
+                    const int gc = j + k * LPT;
+                    const uint4 v = *reinterpret_cast<const uint4*>(vb + (gc / 8) * kSlabBytes + swz(row, gc % 8));
+                    ElemTraits<T>::unpack(v, vf + k * EPC);
+                }
+#pragma unroll
+                for (int r = 0; r < RT; ++r)
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) o[r][e] = fmaf(pr[r], vf[e], o[r][e]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar_empty + 8 * s);
+    }
+
+    // ---- merge the groups of this warp (butterfly over the group bits)
+    float mr[RT], lr[RT];
+#pragma unroll
+    for (int r = 0; r < RT; ++r) {
+        mr[r] = __shfl_sync(0xffffffffu, m_run, owner_base + (r << SH));
+        lr[r] = __shfl_sync(0xffffffffu, l_run, owner_base + (r << SH));
+    }
+#pragma unroll
+    for (int off = LPT; off < 32; off <<= 1) {
+#pragma unroll
+        for (int r = 0; r < RT; ++r) {
+            const float m2 = __shfl_xor_sync(0xffffffffu, mr[r], off);
+            const float l2 = __shfl_xor_sync(0xffffffffu, lr[r], off);
+            const float M = fmaxf(mr[r], m2);
+            const float Mu = M == -INFINITY ? 0.f : M;
+            const float a1 = fast_exp2(mr[r] - Mu), a2 = fast_exp2(m2 - Mu);
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const float o2 = __shfl_xor_sync(0xffffffffu, o[r][e], off);
+                o[r][e] = o[r][e] * a1 + o2 * a2;
+            }
+            lr[r] = lr[r] * a1 + l2 * a2;
+            mr[r] = M;
+        }
+    }
+    // ---- across warps through shared memory: per warp [RT][D] O, [RT] m, [RT] l
+    float* so = scratch + warp * RT * (D + 2);
+    if (grp == 0) {
+#pragma unroll
+        for (int r = 0; r < RT; ++r)
+#pragma unroll
+            for (int k = 0; k < CPL; ++k)
+#pragma unroll
+                for (int e = 0; e < EPC; ++e) so[r * D + (j + k * LPT) * EPC + e] = o[r][k * EPC + e];
+    }
+    if (lane < RT) {
+        so[RT * D + lane] = mr[lane];
+        so[RT * D + RT + lane] = lr[lane];
+    }
+    asm volatile("bar.sync 1, %0;" ::"r"(kCcWarps * 32) : "memory");
+    if (!ok) return;
+    for (int r = warp; r < RT; r += kCcWarps) {
+        const int row = rb * RT + r;
+        if (row >= rows_total) continue;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kCcWarps; ++w) M = fmaxf(M, scratch[w * RT * (D + 2) + RT * D + r]);
+        const float Mu = M == -INFINITY ? 0.f : M;
+        float wts[kCcWarps], L = 0.f;
+#pragma unroll
+        for (int w = 0; w < kCcWarps; ++w) {
+            const float* sw = scratch + w * RT * (D + 2);
+            wts[w] = fast_exp2(sw[RT * D + r] - Mu);
+            L += sw[RT * D + RT + r] * wts[w];
+        }
+        const int qi = row / G, gh = row % G;
+        const int64_t prow = (int64_t)C.part_base + (int64_t)qi * Hq + head * G + gh;
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        for (int dd = lane; dd < D; dd += 32) {
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kCcWarps; ++w) acc += scratch[w * RT * (D + 2) + r * D + dd] * wts[w];
+            P.part_o[prow * D + dd] = acc * inv;
+        }
+        if (lane == 0) P.part_lse[prow] = L > 0.f ? M + __log2f(L) : -INFINITY;
+    }
+}
+
+template <typename T, int D, int RT>
+__global__ void __launch_bounds__((kCcWarps + 1) * 32)
+pac_cc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+              const T* __restrict__ Q, int item_off) {
+    constexpr int EB = ElemTraits<T>::kBytes;
+    constexpr int NSLAB = D * EB / 128;
+    constexpr uint32_t kStage = 2 * NSLAB * kTileTokens * 128;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t ring = smem_u32(base);
+    float* scratch = reinterpret_cast<float*>(base + kCcStages * kStage);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + kCcStages * kStage + kCcWarps * 8 * (D + 2) * 4);
+    const uint32_t bar_full = smem_u32(bars), bar_empty = smem_u32(bars + kCcStages);
+
+    const DevItem it = P.items[item_off + blockIdx.x];
+    const DevChunk C = P.chunks[it.chunk];
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kCcStages; ++s) {
+            mbar_init(bar_full + 8 * s, 1);
+            mbar_init(bar_empty + 8 * s, kCcWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    const int warp = threadIdx.x / 32;
+    if (warp == kCcWarps) {
+        if ((threadIdx.x & 31) == 0) {
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+            produce_chunk<NSLAB, kCcStages, 128 / EB>(P, C, it.kv_head, ring, bar_full, bar_empty, &tk, &tv);
+        }
+        return;
+    }
+    // lanes per token: 8 for one row, 16 for 2-4 rows, up to 32 for 8 rows,
+    // never more than the 16-byte chunks of a row
+    constexpr int CH = D * EB / 16;
+    constexpr int LW = RT == 1 ? 8 : RT <= 4 ? 16 : 32;
+    constexpr int LPT = CH < LW ? CH : LW;
+    cc_consume<T, D, LPT, RT>(P, C, it.kv_head, it.row_block, Q, ring, base, bar_full, bar_empty, scratch);
+}
+
+template <typename T, int D>
+size_t cc_smem_bytes() {
+    constexpr int EB = ElemTraits<T>::kBytes;
+    constexpr int NSLAB = D * EB / 128;
+    return 1024 + kCcStages * 2 * NSLAB * kTileTokens * 128 + kCcWarps * 8 * (D + 2) * 4 + 2 * kCcStages * 8;
+}
+
+template <typename T, int D, int RT>
+cudaError_t launch_cc_rt(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q,
+                         int n_items, int item_off, cudaStream_t st) {
+    const size_t smem = cc_smem_bytes<T, D>();
+    static bool attr_set = false;  // once per process (single device per process)
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(pac_cc_kernel<T, D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    pac_cc_kernel<T, D, RT><<<n_items, (kCcWarps + 1) * 32, smem, st>>>(P, *tk, *tv, static_cast<const T*>(Q), item_off);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t launch_cc_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int r_tile,
+                        int n_items, int item_off, cudaStream_t st) {
+    switch (r_tile) {
+        case 1: return launch_cc_rt<T, D, 1>(P, tk, tv, Q, n_items, item_off, st);
+        case 2: return launch_cc_rt<T, D, 2>(P, tk, tv, Q, n_items, item_off, st);
+        case 4: return launch_cc_rt<T, D, 4>(P, tk, tv, Q, n_items, item_off, st);
+        default: return launch_cc_rt<T, D, 8>(P, tk, tv, Q, n_items, item_off, st);
+    }
+}
+
+}  // namespace dev
+
+cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const void* tv, const void* Q,
+                          int r_tile, int n_items, int item_off, cudaStream_t st) {
+    const CUtensorMap* k = static_cast<const CUtensorMap*>(tk);
+    const CUtensorMap* v = static_cast<const CUtensorMap*>(tv);
+    if (dt == PST_BF16) {
+        if (P.d == 128) return dev::launch_cc_t<__nv_bfloat16, 128>(P, k, v, Q, r_tile, n_items, item_off, st);
+        return dev::launch_cc_t<__nv_bfloat16, 64>(P, k, v, Q, r_tile, n_items, item_off, st);
+    }
+    if (P.d == 128) return dev::launch_cc_t<float, 128>(P, k, v, Q, r_tile, n_items, item_off, st);
+    return dev::launch_cc_t<float, 64>(P, k, v, Q, r_tile, n_items, item_off, st);
+}
+
+}  // namespace pst

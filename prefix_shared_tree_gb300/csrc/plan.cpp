@@ -1,0 +1,775 @@
+// pst_plan_create: KV-guided grouping, mask packing, cost model and the
+// partitioner that chooses the KV-axis split b_k of every node.
+//
+// CoDec, "workload balancing": each node is a task T[i] = (n_q[i], n[i]); the
+// query axis is never split (b_q = 1) and the KV axis is split b_k[i] ways; the
+// objective is the smallest maximum per-block cost over assignments A of the
+// sub-tasks to m blocks. A binary search finds the lower bound cost_l on the
+// block cost (the average block cost rises monotonically as splits get finer),
+// b_k[i] is bounded by ceil(C_est(n_q[i], n[i]) / cost_l), and a search over
+// the b_k picks the split with the best list schedule (Graham 1966).
+//
+// DEFT, Algorithm 1 (QKV preparation): QMapKV (per query its prefix nodes) and
+// KVMapQ (per node the queries sharing it). DEFT's bit causal mask: one 64-bit
+// word per query records which tokens of a chunk it may see.
+#include <algorithm>
+#include <chrono>
+#include <memory>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <numeric>
+#include <queue>
+#include <string>
+
+#include "pst_internal.h"
+
+namespace pst {
+
+int device_sm_count(int* out);  // attn.cu
+
+// ------------------------------------------------------------------ cost model
+// Profile-based estimator C_est(rows, tokens) (CoDec "profile-based cost
+// estimation"): a measured table per PAC kind, bilinear in (log rows, log
+// tokens); an analytic model stands in until a table is installed.
+namespace {
+struct CostTable {
+    bool set = false;
+    std::vector<double> lr, ln, us;  // log rows, log tokens, values [n_r][n_n]
+};
+std::mutex g_cost_mu;
+CostTable g_cost[2];
+
+double interp(const std::vector<double>& g, double x, int* i0) {
+    // returns the fractional position of x between g[i0] and g[i0+1], clamped
+    int n = (int)g.size();
+    if (n == 1 || x <= g[0]) { *i0 = 0; return 0.0; }
+    if (x >= g[n - 1]) { *i0 = std::max(0, n - 2); return n == 1 ? 0.0 : 1.0; }
+    int i = (int)(std::upper_bound(g.begin(), g.end(), x) - g.begin()) - 1;
+    *i0 = i;
+    return (x - g[i]) / (g[i + 1] - g[i]);
+}
+}  // namespace
+
+// Analytic stand-in, per PAC thread block with every SM busy: a fixed block
+// cost plus the larger of its HBM time and its arithmetic time, plus the
+// partial output it writes and POR reads back.
+static double analytic_cost(int kind, double rows, double tokens, double bytes_per_tok, int d,
+                            int num_sms) {
+    const double bw_sm = 6.0e6 / std::max(1, num_sms);        // bytes per us per SM
+    const double t0 = 1.5;                                     // us per block
+    const double mem = tokens * bytes_per_tok / bw_sm;
+    double cmp;
+    if (kind == 1) {
+        const double rpad = std::ceil(rows / 16.0) * 16.0;
+        cmp = tokens * rpad * 4.0 * d / (3.0e6);               // flop per us per SM (mma.sync)
+    } else {
+        const double instr = 8.0 + 11.0 * rows;                // warp instructions per token
+        cmp = tokens * instr * (d / 128.0) / (4.0 * 1800.0);   // 4 issue/clk at 1.8 GHz
+    }
+    const double part = rows * (4.0 * d + 4.0) * 2.0 / bw_sm;
+    return t0 + std::max(mem, cmp) + part;
+}
+
+double cost_estimate(int kind, double rows, double tokens) {
+    return analytic_cost(kind, rows, tokens, 512.0, 128, 152);
+}
+
+static double cost_us(int kind, double rows, double tokens, double bytes_per_tok, int d,
+                      int num_sms) {
+    {
+        std::lock_guard<std::mutex> lk(g_cost_mu);
+        const CostTable& T = g_cost[kind ? 1 : 0];
+        if (T.set && d == 128 && bytes_per_tok == 512.0) {
+            int i, j;
+            double fr = interp(T.lr, std::log(std::max(1.0, rows)), &i);
+            double ft = interp(T.ln, std::log(std::max(1.0, tokens)), &j);
+            const int nn = (int)T.ln.size();
+            auto at = [&](int a, int b) {
+                a = std::min(a, (int)T.lr.size() - 1);
+                b = std::min(b, nn - 1);
+                return T.us[(size_t)a * nn + b];
+            };
+            double v0 = at(i, j) * (1 - ft) + at(i, j + 1) * ft;
+            double v1 = at(i + 1, j) * (1 - ft) + at(i + 1, j + 1) * ft;
+            return v0 * (1 - fr) + v1 * fr;
+        }
+    }
+    return analytic_cost(kind, rows, tokens, bytes_per_tok, d, num_sms);
+}
+
+}  // namespace pst
+
+using namespace pst;
+
+extern "C" int pst_cost_set_table(int32_t kind, int32_t n_r, const float* rows, int32_t n_n,
+                                  const float* tokens, const float* us) {
+    if (kind != 0 && kind != 1) return fail(PST_EINVAL, "cost_set_table: kind must be 0 or 1");
+    std::lock_guard<std::mutex> lk(g_cost_mu);
+    CostTable& T = g_cost[kind];
+    if (n_r <= 0 || n_n <= 0 || !rows || !tokens || !us) {
+        T = CostTable();  // clearing reverts to the analytic model
+        return PST_OK;
+    }
+    CostTable nt;
+    for (int i = 0; i < n_r; ++i) {
+        if (rows[i] <= 0 || (i && rows[i] <= rows[i - 1]))
+            return fail(PST_EINVAL, "cost_set_table: rows must be positive and increasing");
+        nt.lr.push_back(std::log((double)rows[i]));
+    }
+    for (int j = 0; j < n_n; ++j) {
+        if (tokens[j] <= 0 || (j && tokens[j] <= tokens[j - 1]))
+            return fail(PST_EINVAL, "cost_set_table: tokens must be positive and increasing");
+        nt.ln.push_back(std::log((double)tokens[j]));
+    }
+    nt.us.assign(us, us + (size_t)n_r * n_n);
+    nt.set = true;
+    T = std::move(nt);
+    return PST_OK;
+}
+
+extern "C" double pst_cost_estimate(int32_t kind, double rows, double tokens) {
+    return cost_us(kind ? 1 : 0, rows, tokens, 512.0, 128, 152);
+}
+
+extern "C" void pst_plan_opts_default(pst_plan_opts* o) {
+    if (!o) return;
+    o->split_policy = PST_SPLIT_COST_MODEL;
+    o->fixed_chunk = 1024;
+    o->tc_min_rows = 16;
+    o->pack_masks = 1;
+    o->num_sms = 0;
+    o->slots_per_sm = 1;
+}
+
+namespace {
+
+int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+// Chunk boundaries of a node: the node's page-space span [fo, fo+len) is cut
+// at multiples of the tile size so that every chunk starts on a TMA tile.
+struct Span {
+    int32_t fo, len, first_block, n_blocks;
+};
+Span node_span(int32_t fo, int32_t len) {
+    Span s{fo, len, fo / kTileTokens, 0};
+    const int32_t end_block = (fo + len + kTileTokens - 1) / kTileTokens;
+    s.n_blocks = std::max(1, end_block - s.first_block);
+    return s;
+}
+// token range [b, e) of chunk k of b_k
+void chunk_range(const Span& s, int32_t bk, int32_t k, int32_t* b, int32_t* e) {
+    const int64_t blk0 = s.first_block + (int64_t)s.n_blocks * k / bk;
+    const int64_t blk1 = s.first_block + (int64_t)s.n_blocks * (k + 1) / bk;
+    int64_t p0 = std::max<int64_t>(blk0 * kTileTokens, s.fo);
+    int64_t p1 = std::min<int64_t>(blk1 * kTileTokens, (int64_t)s.fo + s.len);
+    *b = (int32_t)(p0 - s.fo);
+    *e = (int32_t)std::max<int64_t>(p1 - s.fo, p0 - s.fo);
+}
+
+int32_t cc_row_tile(int32_t rows) {
+    if (rows <= 1) return 1;
+    if (rows <= 2) return 2;
+    if (rows <= 4) return 4;
+    return 8;
+}
+
+struct ItemCost {
+    double cost;
+    int32_t chunk;
+    int16_t head, rb;
+};
+
+// Graham list scheduling (largest first) of item costs onto m slots: returns
+// the makespan.
+double list_schedule(std::vector<ItemCost>& v, int m) {
+    std::sort(v.begin(), v.end(), [](const ItemCost& a, const ItemCost& b) {
+        if (a.cost != b.cost) return a.cost > b.cost;
+        if (a.chunk != b.chunk) return a.chunk < b.chunk;
+        if (a.head != b.head) return a.head < b.head;
+        return a.rb < b.rb;
+    });
+    using Slot = std::pair<double, int>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> pq;
+    for (int i = 0; i < m; ++i) pq.push({0.0, i});
+    double mk = 0;
+    for (const auto& it : v) {
+        Slot s = pq.top();
+        pq.pop();
+        s.first += it.cost;
+        mk = std::max(mk, s.first);
+        pq.push(s);
+    }
+    return mk;
+}
+
+}  // namespace
+
+struct Planner {
+    const Tree& T;
+    pst_plan& P;
+    int num_sms = 152;
+    double bytes_per_tok = 0;
+
+    Planner(const Tree& t, pst_plan& p) : T(t), P(p) {}
+
+    double item_cost(int kind, int rows_blk, int tokens) const {
+        return cost_us(kind, rows_blk, std::max(1, tokens), bytes_per_tok, P.d, num_sms);
+    }
+
+    int rows_per_block(const Task& t) const {
+        return t.kind == 1 ? kTcRowsPerBlock : cc_row_tile(t.rows);
+    }
+
+    // per-item cost and item count of task t split b ways
+    void task_items(const Task& t, int b, std::vector<ItemCost>* out, double* total,
+                    int chunk_id_base) const {
+        const int rpb = rows_per_block(t);
+        const int n_rb = (t.rows + rpb - 1) / rpb;
+        Span s = t.node >= 0 ? node_span(T.first_offset[t.node], t.n_tok) : Span{0, t.n_tok, 0, 1};
+        for (int k = 0; k < b; ++k) {
+            int32_t tb = 0, te = t.n_tok;
+            if (t.node >= 0) chunk_range(s, b, k, &tb, &te);
+            for (int rb = 0; rb < n_rb; ++rb) {
+                const int rows_blk = std::min(rpb, t.rows - rb * rpb);
+                const double c = item_cost(t.kind, rows_blk, te - tb);
+                if (total) *total += c * P.hkv;
+                if (out)
+                    for (int h = 0; h < P.hkv; ++h)
+                        out->push_back({c, chunk_id_base + k, (int16_t)h, (int16_t)rb});
+            }
+        }
+    }
+
+    double makespan(const std::vector<int>& b, int m) const {
+        std::vector<ItemCost> v;
+        int cid = 0;
+        for (size_t i = 0; i < P.tasks.size(); ++i) {
+            task_items(P.tasks[i], b[i], &v, nullptr, cid);
+            cid += b[i];
+        }
+        return list_schedule(v, m);
+    }
+
+    // CoDec's heuristic solver: binary search for cost_l, bound b_k, then a
+    // search over the bounded b_k vectors scored by the list schedule.
+    void partition(int m) {
+        auto& tasks = P.tasks;
+        const size_t nt = tasks.size();
+        std::vector<double> c_full(nt);
+        for (size_t i = 0; i < nt; ++i) c_full[i] = item_cost(tasks[i].kind, rows_per_block(tasks[i]), tasks[i].n_tok);
+        auto b_of = [&](size_t i, double Tc, int cap) {
+            if (Tc <= 0) return cap;
+            int b = (int)std::ceil(c_full[i] / Tc - 1e-9);
+            return std::max(1, std::min(b, cap));
+        };
+        auto avg_at = [&](double Tc) {
+            double total = 0;
+            for (size_t i = 0; i < nt; ++i)
+                task_items(tasks[i], b_of(i, Tc, tasks[i].max_splits), nullptr, &total, 0);
+            return total / m;
+        };
+        double hi = 0, lo = 1e30;
+        for (size_t i = 0; i < nt; ++i) {
+            hi = std::max(hi, c_full[i]);
+            lo = std::min(lo, item_cost(tasks[i].kind, rows_per_block(tasks[i]), std::min(tasks[i].n_tok, kTileTokens)));
+        }
+        double cost_l;
+        const double avg_hi = avg_at(hi);
+        if (avg_hi >= hi) {
+            cost_l = avg_hi;  // coarsest split already averages above the largest task
+        } else {
+            lo = std::min(lo, hi);
+            for (int it = 0; it < 60 && hi - lo > 1e-4 * hi; ++it) {
+                const double mid = 0.5 * (lo + hi);
+                if (avg_at(mid) <= mid) hi = mid; else lo = mid;
+            }
+            cost_l = hi;
+        }
+        P.cost_l_us = cost_l;
+        std::vector<int> ub(nt);
+        for (size_t i = 0; i < nt; ++i) ub[i] = b_of(i, cost_l, tasks[i].max_splits);
+
+        std::vector<int> best(nt, 1);
+        double best_mk = 1e300;
+        const double factors[] = {0.6, 0.7, 0.8, 0.9, 1.0, 1.15, 1.3, 1.5, 2.0, 3.0};
+        auto consider = [&](const std::vector<int>& b) {
+            const double mk = makespan(b, m);
+            if (mk < best_mk * (1 - 1e-9)) { best_mk = mk; best = b; }
+        };
+        for (double f : factors) {
+            std::vector<int> b(nt);
+            for (size_t i = 0; i < nt; ++i) b[i] = b_of(i, cost_l * f, ub[i]);
+            consider(b);
+        }
+        // the plan is never worse (under C_est) than no split or a uniform split
+        consider(std::vector<int>(nt, 1));
+        for (int chunk = kTileTokens; chunk <= 8192; chunk *= 2) {
+            std::vector<int> b(nt);
+            for (size_t i = 0; i < nt; ++i)
+                b[i] = tasks[i].node < 0 ? 1 : std::max(1, std::min(tasks[i].max_splits, (tasks[i].n_tok + chunk - 1) / chunk));
+            consider(b);
+        }
+        // greedy +-1 refinement of single tasks, largest per-item cost first
+        for (int iter = 0; iter < 24; ++iter) {
+            std::vector<size_t> order(nt);
+            std::iota(order.begin(), order.end(), 0);
+            std::sort(order.begin(), order.end(), [&](size_t a, size_t b2) {
+                double ca = c_full[a] / best[a], cb = c_full[b2] / best[b2];
+                return ca != cb ? ca > cb : a < b2;
+            });
+            bool improved = false;
+            for (size_t k = 0; k < std::min<size_t>(order.size(), 4) && !improved; ++k) {
+                const size_t i = order[k];
+                for (int delta : {+1, -1}) {
+                    const int nb = best[i] + delta;
+                    if (nb < 1 || nb > tasks[i].max_splits) continue;
+                    std::vector<int> b = best;
+                    b[i] = nb;
+                    const double mk = makespan(b, m);
+                    if (mk < best_mk * (1 - 1e-6)) { best_mk = mk; best = b; improved = true; break; }
+                }
+            }
+            if (!improved) break;
+        }
+        for (size_t i = 0; i < nt; ++i) tasks[i].b_k = best[i];
+        P.makespan_us = best_mk;
+    }
+};
+
+static bool build_packed_group(const Tree& T, int32_t root, const std::vector<int32_t>& desc,
+                               PackedGroup* g) {
+    // Try chunk orders: ascending node id (allocation order), then preorder.
+    std::vector<std::vector<int32_t>> orders;
+    std::vector<int32_t> by_id = desc;
+    std::sort(by_id.begin(), by_id.end());
+    orders.push_back(by_id);
+    orders.push_back(desc);  // desc is in preorder
+    const int32_t ps = T.page_size;
+    for (const auto& ord : orders) {
+        std::vector<int32_t> plist, tn, tt;
+        int32_t pos_begin = -1, cur_page = -1, cur_row = -1;
+        bool ok = true;
+        for (int32_t n : ord) {
+            for (int32_t t = 0; t < T.len[n] && ok; ++t) {
+                const int64_t pos = (int64_t)T.first_offset[n] + t;
+                const int32_t page = T.page_ids[T.page_ptr[n] + pos / ps];
+                const int32_t row = (int32_t)(pos % ps);
+                if (cur_page < 0) {
+                    plist.push_back(page);
+                    pos_begin = row;
+                } else if (page == cur_page && row == cur_row + 1) {
+                    // continues in the same page
+                } else if (cur_row == ps - 1 && row == 0) {
+                    plist.push_back(page);
+                } else {
+                    ok = false;
+                }
+                cur_page = page;
+                cur_row = row;
+                tn.push_back(n);
+                tt.push_back(t);
+            }
+            if (!ok) break;
+        }
+        if (!ok || tn.empty()) continue;
+        g->root = root;
+        g->nodes = ord;
+        g->tok_node = std::move(tn);
+        g->tok_t = std::move(tt);
+        g->page_list = std::move(plist);
+        g->pos_begin = pos_begin;
+        return true;
+    }
+    return false;
+}
+
+extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const int32_t* query_node,
+                               int32_t n_q_heads, int32_t n_kv_heads, int32_t d, pst_dtype dtype,
+                               const pst_plan_opts* opts, pst_plan** out) {
+    const auto t_start = std::chrono::steady_clock::now();
+    if (!out) return fail(PST_EINVAL, "plan_create: out is null");
+    *out = nullptr;
+    if (!tree) return fail(PST_EINVAL, "plan_create: tree is null");
+    if (n_queries < 1 || !query_node) return fail(PST_EINVAL, "plan_create: need >= 1 query");
+    if (n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads)
+        return fail(PST_EUNSUPPORTED, "plan_create: n_q_heads must be a positive multiple of n_kv_heads");
+    if (n_q_heads > 32767 || n_kv_heads > 32767) return fail(PST_EUNSUPPORTED, "plan_create: too many heads");
+    if (d != 64 && d != 128) return fail(PST_EUNSUPPORTED, "plan_create: d must be 64 or 128");
+    if (dtype != PST_BF16 && dtype != PST_F32) return fail(PST_EUNSUPPORTED, "plan_create: dtype");
+    const Tree& T = tree->t;
+    pst_plan_opts o;
+    pst_plan_opts_default(&o);
+    if (opts) o = *opts;
+    if (o.tc_min_rows <= 0) o.tc_min_rows = 16;
+    if (o.slots_per_sm <= 0) o.slots_per_sm = 1;
+    if (o.split_policy == PST_SPLIT_UNIFORM && (o.fixed_chunk <= 0 || o.fixed_chunk % kTileTokens))
+        return fail(PST_EINVAL, "plan_create: fixed_chunk must be a positive multiple of 64");
+
+    pst_plan* P = new (std::nothrow) pst_plan();
+    if (!P) return fail(PST_ENOMEM, "plan_create: out of memory");
+    std::unique_ptr<pst_plan> guard(P);
+    P->n_queries = n_queries;
+    P->hq = n_q_heads;
+    P->hkv = n_kv_heads;
+    P->group = n_q_heads / n_kv_heads;
+    P->d = d;
+    P->dtype = dtype;
+    P->page_size = T.page_size;
+    P->num_pages = T.num_pages;
+    P->n_nodes = T.n_nodes;
+    P->opts = o;
+    const int32_t N = T.n_nodes, G = P->group;
+
+    // ---- QMapKV: per query, its path from the top of its tree (DEFT Alg. 1 step 1)
+    P->qpath_ptr.assign(n_queries + 1, 0);
+    for (int32_t q = 0; q < n_queries; ++q) {
+        const int32_t v = query_node[q];
+        if (v < 0 || v >= N) return fail(PST_EINVAL, "plan_create: query " + std::to_string(q) + " node out of range");
+        P->qpath_ptr[q + 1] = P->qpath_ptr[q] + T.depth[v] + 1;
+    }
+    P->qpath_node.resize(P->qpath_ptr[n_queries]);
+    for (int32_t q = 0; q < n_queries; ++q) {
+        int32_t k = P->qpath_ptr[q + 1];
+        int64_t seen = 0;
+        for (int32_t n = query_node[q]; n >= 0; n = T.parent[n]) {
+            P->qpath_node[--k] = n;
+            seen += T.len[n];
+        }
+        if (seen == 0) return fail(PST_EINVAL, "plan_create: query " + std::to_string(q) + " sees no token");
+    }
+    // ---- KVMapQ: per node, ascending queries sharing it (DEFT Alg. 1 step 2)
+    P->nodeq_ptr.assign(N + 1, 0);
+    for (int32_t n : P->qpath_node) P->nodeq_ptr[n + 1]++;
+    for (int32_t n = 0; n < N; ++n) P->nodeq_ptr[n + 1] += P->nodeq_ptr[n];
+    P->nodeq.resize(P->nodeq_ptr[N]);
+    {
+        std::vector<int32_t> fill(P->nodeq_ptr.begin(), P->nodeq_ptr.end() - 1);
+        for (int32_t q = 0; q < n_queries; ++q)
+            for (int32_t k = P->qpath_ptr[q]; k < P->qpath_ptr[q + 1]; ++k)
+                P->nodeq[fill[P->qpath_node[k]]++] = q;
+    }
+    auto nq_of = [&](int32_t n) { return P->nodeq_ptr[n + 1] - P->nodeq_ptr[n]; };
+
+    // ---- packing: a page-contiguous set of descendants of <= 64 tokens
+    std::vector<int32_t> packed_in(N, -1);
+    if (o.pack_masks) {
+        // subtree token totals (excluding the node itself) via reverse preorder
+        std::vector<int64_t> sub_tok(N, 0), sub_cnt(N, 0);
+        for (int i = N - 1; i >= 0; --i) {
+            const int32_t n = T.preorder[i];
+            for (int32_t c : T.children[n]) {
+                sub_tok[n] += sub_tok[c] + T.len[c];
+                sub_cnt[n] += sub_cnt[c] + 1;
+            }
+        }
+        for (int i = 0; i < N; ++i) {
+            const int32_t p = T.preorder[i];
+            if (packed_in[p] >= 0) continue;
+            if (sub_cnt[p] < 2 || sub_tok[p] < 2 || sub_tok[p] > kMaskTokens) continue;
+            // descendants in preorder
+            std::vector<int32_t> desc, st(T.children[p].rbegin(), T.children[p].rend());
+            while (!st.empty()) {
+                int32_t n = st.back();
+                st.pop_back();
+                desc.push_back(n);
+                for (auto it = T.children[n].rbegin(); it != T.children[n].rend(); ++it) st.push_back(*it);
+            }
+            PackedGroup g;
+            if (!build_packed_group(T, p, desc, &g)) continue;
+            // queries: union of the packed nodes' query lists
+            std::vector<int32_t> qs;
+            for (int32_t n : desc)
+                qs.insert(qs.end(), P->nodeq.begin() + P->nodeq_ptr[n], P->nodeq.begin() + P->nodeq_ptr[n + 1]);
+            std::sort(qs.begin(), qs.end());
+            qs.erase(std::unique(qs.begin(), qs.end()), qs.end());
+            if (qs.empty()) continue;
+            std::vector<int32_t> pos_of_node(0);
+            g.queries = qs;
+            g.mask.assign(qs.size(), 0);
+            for (size_t qi = 0; qi < qs.size(); ++qi) {
+                const int32_t q = qs[qi];
+                uint64_t m = 0;
+                for (size_t j = 0; j < g.tok_node.size(); ++j) {
+                    const int32_t n = g.tok_node[j];
+                    // visible iff n is on the query's path
+                    bool on = false;
+                    for (int32_t k = P->qpath_ptr[q]; k < P->qpath_ptr[q + 1]; ++k)
+                        if (P->qpath_node[k] == n) { on = true; break; }
+                    if (on) m |= (uint64_t)1 << j;
+                }
+                g.mask[qi] = m;
+            }
+            const int32_t gid = (int32_t)P->groups.size();
+            for (int32_t n : desc) packed_in[n] = gid;
+            P->groups.push_back(std::move(g));
+        }
+    }
+
+    // ---- tasks T[i] = (n_q[i], n[i])
+    const bool tc_ok = dtype == PST_BF16;
+    for (int i = 0; i < N; ++i) {
+        const int32_t n = T.preorder[i];
+        if (packed_in[n] >= 0 || T.len[n] == 0 || nq_of(n) == 0) continue;
+        Task t;
+        t.node = n;
+        t.group = -1;
+        t.n_q = nq_of(n);
+        t.rows = t.n_q * G;
+        t.n_tok = T.len[n];
+        t.kind = (tc_ok && t.rows >= o.tc_min_rows) ? 1 : 0;
+        t.max_splits = node_span(T.first_offset[n], T.len[n]).n_blocks;
+        P->tasks.push_back(t);
+    }
+    for (size_t gi = 0; gi < P->groups.size(); ++gi) {
+        const auto& g = P->groups[gi];
+        Task t;
+        t.node = -1;
+        t.group = (int32_t)gi;
+        t.n_q = (int32_t)g.queries.size();
+        t.rows = t.n_q * G;
+        t.n_tok = (int32_t)g.tok_node.size();
+        t.kind = (tc_ok && t.rows >= o.tc_min_rows) ? 1 : 0;
+        t.max_splits = 1;
+        P->tasks.push_back(t);
+    }
+
+    // ---- partition (b_k)
+    Planner pl(T, *P);
+    if (o.num_sms > 0) pl.num_sms = o.num_sms;
+    else {
+        int sms = 0;
+        if (device_sm_count(&sms) != 0 || sms <= 0) return fail(PST_ECUDA, "plan_create: cannot query the SM count (set opts.num_sms)");
+        pl.num_sms = sms;
+    }
+    pl.bytes_per_tok = 2.0 * d * (dtype == PST_BF16 ? 2 : 4);
+    const int m = pl.num_sms * o.slots_per_sm;
+    P->num_slots = m;
+    if (o.split_policy == PST_SPLIT_NONE) {
+        for (auto& t : P->tasks) t.b_k = 1;
+    } else if (o.split_policy == PST_SPLIT_UNIFORM) {
+        for (auto& t : P->tasks)
+            t.b_k = t.node < 0 ? 1 : std::max(1, std::min(t.max_splits, (t.n_tok + o.fixed_chunk - 1) / o.fixed_chunk));
+    } else {
+        pl.partition(m);
+    }
+    {
+        std::vector<int> b(P->tasks.size());
+        for (size_t i = 0; i < b.size(); ++i) b[i] = P->tasks[i].b_k;
+        P->makespan_us = pl.makespan(b, m);
+    }
+
+    // ---- chunks, pages, chunk queries, masks, partial rows
+    P->pages = T.page_ids;
+    int64_t part_rows = 0;
+    for (size_t ti = 0; ti < P->tasks.size(); ++ti) {
+        const Task& t = P->tasks[ti];
+        if (t.node >= 0) {
+            Span s = node_span(T.first_offset[t.node], t.n_tok);
+            for (int k = 0; k < t.b_k; ++k) {
+                int32_t tb, te;
+                chunk_range(s, t.b_k, k, &tb, &te);
+                if (te <= tb) continue;
+                HostChunk c;
+                c.task = (int32_t)ti;
+                c.node = t.node;
+                c.tok_begin = tb;
+                c.tok_end = te;
+                c.kind = t.kind;
+                c.dev.page_base = (int32_t)T.page_ptr[t.node];
+                c.dev.pos_begin = T.first_offset[t.node] + tb;
+                c.dev.n_tok = te - tb;
+                c.dev.q_base = (int32_t)P->chunk_q.size();
+                c.dev.n_q = t.n_q;
+                c.dev.mask_base = -1;
+                c.dev.r_tile = t.kind == 1 ? kTcRowsPerBlock : cc_row_tile(t.rows);
+                P->chunk_q.insert(P->chunk_q.end(), P->nodeq.begin() + P->nodeq_ptr[t.node],
+                                  P->nodeq.begin() + P->nodeq_ptr[t.node + 1]);
+                P->chunks.push_back(c);
+            }
+        } else {
+            const PackedGroup& g = P->groups[t.group];
+            HostChunk c;
+            c.task = (int32_t)ti;
+            c.node = -1;
+            c.tok_begin = 0;
+            c.tok_end = t.n_tok;
+            c.kind = t.kind;
+            c.dev.page_base = (int32_t)P->pages.size();
+            P->pages.insert(P->pages.end(), g.page_list.begin(), g.page_list.end());
+            c.dev.pos_begin = g.pos_begin;
+            c.dev.n_tok = t.n_tok;
+            c.dev.q_base = (int32_t)P->chunk_q.size();
+            c.dev.n_q = t.n_q;
+            c.dev.mask_base = (int32_t)P->masks.size();
+            c.dev.r_tile = t.kind == 1 ? kTcRowsPerBlock : cc_row_tile(t.rows);
+            P->chunk_q.insert(P->chunk_q.end(), g.queries.begin(), g.queries.end());
+            P->masks.insert(P->masks.end(), g.mask.begin(), g.mask.end());
+            P->chunks.push_back(c);
+        }
+    }
+    for (auto& c : P->chunks) {
+        c.dev.part_base = (int32_t)part_rows;
+        part_rows += (int64_t)c.dev.n_q * n_q_heads;
+        // tokens the kernel loads (whole 16-row boxes)
+        const int32_t b0 = c.dev.pos_begin / kBoxRows, b1 = (c.dev.pos_begin + c.dev.n_tok + kBoxRows - 1) / kBoxRows;
+        P->kv_tokens_read += (int64_t)(b1 - b0) * kBoxRows;
+    }
+    if (part_rows > INT32_MAX) return fail(PST_EUNSUPPORTED, "plan_create: too many partial rows");
+    P->n_part_rows = part_rows;
+    for (int32_t n = 0; n < N; ++n) P->unique_tokens += T.len[n];
+
+    // ---- merge lists: per query, the partial rows POR combines
+    P->merge_ptr.assign(n_queries + 1, 0);
+    for (const auto& c : P->chunks)
+        for (int32_t k = 0; k < c.dev.n_q; ++k) P->merge_ptr[P->chunk_q[c.dev.q_base + k] + 1]++;
+    for (int32_t q = 0; q < n_queries; ++q) P->merge_ptr[q + 1] += P->merge_ptr[q];
+    P->merge_row.resize(P->merge_ptr[n_queries]);
+    {
+        std::vector<int32_t> fill(P->merge_ptr.begin(), P->merge_ptr.end() - 1);
+        for (const auto& c : P->chunks)
+            for (int32_t k = 0; k < c.dev.n_q; ++k)
+                P->merge_row[fill[P->chunk_q[c.dev.q_base + k]]++] = c.dev.part_base + k * n_q_heads;
+    }
+
+    // ---- items in largest-first order (the hardware block dispatcher then
+    // realises a list schedule of them), tensor-core items first
+    std::vector<ItemCost> tc, cc;
+    for (size_t ci = 0; ci < P->chunks.size(); ++ci) {
+        const auto& c = P->chunks[ci];
+        const Task& t = P->tasks[c.task];
+        const int rpb = pl.rows_per_block(t);
+        const int n_rb = (t.rows + rpb - 1) / rpb;
+        for (int rb = 0; rb < n_rb; ++rb) {
+            const int rows_blk = std::min(rpb, t.rows - rb * rpb);
+            const double cst = pl.item_cost(t.kind, rows_blk, c.dev.n_tok);
+            for (int h = 0; h < n_kv_heads; ++h)
+                (t.kind == 1 ? tc : cc).push_back({cst, (int32_t)ci, (int16_t)h, (int16_t)rb});
+        }
+    }
+    list_schedule(tc, m);
+    list_schedule(cc, m);
+    for (const auto& it : tc) P->items.push_back({it.chunk, it.head, it.rb});
+    P->n_tc_items = (int64_t)tc.size();
+    P->n_cc_items = (int64_t)cc.size();
+    // one CUDA-core launch per row tile (8, 4, 2, 1), each in largest-first order
+    for (int k = 0; k < 4; ++k) {
+        P->cc_class_off[k] = (int64_t)P->items.size();
+        for (const auto& it : cc)
+            if (P->chunks[it.chunk].dev.r_tile == (8 >> k)) P->items.push_back({it.chunk, it.head, it.rb});
+        P->cc_class_cnt[k] = (int64_t)P->items.size() - P->cc_class_off[k];
+    }
+
+    // ---- workspace layout and the metadata image
+    WsLayout& W = P->ws;
+    int64_t off = 0;
+    W.status = off; off = align256(off + 64);
+    W.items = off; off = align256(off + (int64_t)P->items.size() * sizeof(DevItem));
+    W.chunks = off; off = align256(off + (int64_t)P->chunks.size() * sizeof(DevChunk));
+    W.pages = off; off = align256(off + (int64_t)P->pages.size() * 4);
+    W.chunk_q = off; off = align256(off + (int64_t)P->chunk_q.size() * 4);
+    W.masks = off; off = align256(off + (int64_t)P->masks.size() * 8);
+    W.merge_ptr = off; off = align256(off + (int64_t)P->merge_ptr.size() * 4);
+    W.merge_row = off; off = align256(off + (int64_t)P->merge_row.size() * 4);
+    W.meta_end = off;
+    W.part_o = off; off = align256(off + part_rows * d * 4);
+    W.part_lse = off; off = align256(off + part_rows * 4);
+    W.total = off;
+    P->meta_blob.assign(W.meta_end, 0);
+    auto put = [&](int64_t at, const void* src, size_t n) { if (n) std::memcpy(P->meta_blob.data() + at, src, n); };
+    put(W.items, P->items.data(), P->items.size() * sizeof(DevItem));
+    {
+        std::vector<DevChunk> dc(P->chunks.size());
+        for (size_t i = 0; i < dc.size(); ++i) dc[i] = P->chunks[i].dev;
+        put(W.chunks, dc.data(), dc.size() * sizeof(DevChunk));
+    }
+    put(W.pages, P->pages.data(), P->pages.size() * 4);
+    put(W.chunk_q, P->chunk_q.data(), P->chunk_q.size() * 4);
+    put(W.masks, P->masks.data(), P->masks.size() * 8);
+    put(W.merge_ptr, P->merge_ptr.data(), P->merge_ptr.size() * 4);
+    put(W.merge_row, P->merge_row.data(), P->merge_row.size() * 4);
+
+    P->plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t_start).count();
+    *out = guard.release();
+    return PST_OK;
+}
+
+extern "C" void pst_plan_destroy(pst_plan* p) { delete p; }
+
+extern "C" int64_t pst_plan_workspace_bytes(const pst_plan* p) { return p ? p->ws.total : -1; }
+
+extern "C" int pst_plan_stats_get(const pst_plan* p, pst_plan_stats* s) {
+    if (!p || !s) return fail(PST_EINVAL, "plan_stats: null argument");
+    s->plan_us = p->plan_us;
+    s->predicted_makespan_us = p->makespan_us;
+    s->cost_lower_bound_us = p->cost_l_us;
+    s->n_chunks = (int64_t)p->chunks.size();
+    s->n_items = (int64_t)p->items.size();
+    s->n_tc_items = p->n_tc_items;
+    s->n_cc_items = p->n_cc_items;
+    s->n_partial_rows = p->n_part_rows;
+    s->unique_kv_tokens = p->unique_tokens;
+    s->kv_tokens_read = p->kv_tokens_read;
+    s->workspace_bytes = p->ws.total;
+    s->num_slots = p->num_slots;
+    s->n_launches = (p->n_tc_items > 0) + 1;
+    for (int k = 0; k < 4; ++k) s->n_launches += p->cc_class_cnt[k] > 0;
+    return PST_OK;
+}
+
+extern "C" int pst_plan_export_sizes(const pst_plan* p, pst_export_sizes* s) {
+    if (!p || !s) return fail(PST_EINVAL, "plan_export_sizes: null argument");
+    s->n_queries = p->n_queries;
+    s->n_nodes = p->n_nodes;
+    s->n_chunks = (int64_t)p->chunks.size();
+    s->n_qpath = (int64_t)p->qpath_node.size();
+    s->n_nodeq = (int64_t)p->nodeq.size();
+    s->n_chunk_q = (int64_t)p->chunk_q.size();
+    int64_t nt = 0;
+    for (const auto& c : p->chunks) nt += c.dev.n_tok;
+    s->n_chunk_tok = nt;
+    s->n_merge = (int64_t)p->merge_row.size();
+    return PST_OK;
+}
+
+extern "C" int pst_plan_export(const pst_plan* p, pst_export* e) {
+    if (!p || !e) return fail(PST_EINVAL, "plan_export: null argument");
+    auto cp = [](int32_t* dst, const std::vector<int32_t>& v) { if (dst && !v.empty()) std::memcpy(dst, v.data(), v.size() * 4); };
+    cp(e->qpath_ptr, p->qpath_ptr);
+    cp(e->qpath_node, p->qpath_node);
+    cp(e->nodeq_ptr, p->nodeq_ptr);
+    cp(e->nodeq, p->nodeq);
+    cp(e->chunk_q, p->chunk_q);
+    cp(e->merge_ptr, p->merge_ptr);
+    cp(e->merge_row, p->merge_row);
+    int32_t qacc = 0, tacc = 0;
+    int64_t tk = 0, qk = 0;
+    const size_t nc = p->chunks.size();
+    for (size_t i = 0; i < nc; ++i) {
+        const auto& c = p->chunks[i];
+        if (e->chunk_q_ptr) e->chunk_q_ptr[i] = qacc;
+        if (e->chunk_tok_ptr) e->chunk_tok_ptr[i] = tacc;
+        if (e->chunk_kind) e->chunk_kind[i] = c.kind;
+        for (int32_t k = 0; k < c.dev.n_q; ++k, ++qk)
+            if (e->chunk_q_mask)
+                e->chunk_q_mask[qk] = c.dev.mask_base < 0 ? ~uint64_t(0) : p->masks[c.dev.mask_base + k];
+        if (c.node >= 0) {
+            for (int32_t t = c.tok_begin; t < c.tok_end; ++t, ++tk) {
+                if (e->chunk_tok_node) e->chunk_tok_node[tk] = c.node;
+                if (e->chunk_tok_t) e->chunk_tok_t[tk] = t;
+            }
+        } else {
+            const auto& g = p->groups[p->tasks[c.task].group];
+            for (size_t j = 0; j < g.tok_node.size(); ++j, ++tk) {
+                if (e->chunk_tok_node) e->chunk_tok_node[tk] = g.tok_node[j];
+                if (e->chunk_tok_t) e->chunk_tok_t[tk] = g.tok_t[j];
+            }
+        }
+        qacc += c.dev.n_q;
+        tacc += c.dev.n_tok;
+    }
+    if (e->chunk_q_ptr) e->chunk_q_ptr[nc] = qacc;
+    if (e->chunk_tok_ptr) e->chunk_tok_ptr[nc] = tacc;
+    return PST_OK;
+}

@@ -1,0 +1,173 @@
+// Internal data structures of libpst shared by the host planner and the
+// device kernels. Not part of the public ABI (see include/pst.h).
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "../../include/pst.h"
+
+namespace pst {
+
+// Rows of the tensor-core PAC per thread block (8 warps x 16 rows).
+constexpr int kTcRowsPerBlock = 128;
+// Rows of the CUDA-core PAC per thread block (largest row tile).
+constexpr int kCcRowsPerBlock = 8;
+// KV tokens per pipeline stage of both PAC kernels (4 boxes of 16 rows).
+constexpr int kTileTokens = 64;
+// Rows of one TMA box (page_size must be a multiple).
+constexpr int kBoxRows = 16;
+// Maximum tokens of a chunk that carries a per-query 64-bit mask.
+constexpr int kMaskTokens = 64;
+
+// One KV chunk: a token range of a node, or a packed page-contiguous subtree
+// whose visibility is given by one 64-bit mask per query.
+struct DevChunk {
+    int32_t page_base;  // index into pages[] of the chunk's page list entry 0
+    int32_t pos_begin;  // page-space position of chunk token 0 (row in entry 0 + 16*k)
+    int32_t n_tok;      // tokens in the chunk
+    int32_t q_base;     // index into chunk_q[] of the chunk's first query
+    int32_t n_q;        // queries grouped with this chunk
+    int32_t part_base;  // partial row of (chunk query 0, q-head 0); row = base + qi*Hq + h
+    int32_t mask_base;  // -1: every query sees every token; else index into masks[]
+    int32_t r_tile;     // CUDA-core PAC: rows per block (1, 2, 4 or 8); tensor-core: 128
+};
+static_assert(sizeof(DevChunk) == 32, "DevChunk layout");
+
+// One PAC thread block: a chunk, a kv head and a block of rows.
+struct DevItem {
+    int32_t chunk;
+    int16_t kv_head;
+    int16_t row_block;
+};
+static_assert(sizeof(DevItem) == 8, "DevItem layout");
+
+// Byte offsets of the workspace sections (all 256-aligned).
+struct WsLayout {
+    int64_t status = 0;      // int32 device status word (+ padding)
+    int64_t items = 0;
+    int64_t chunks = 0;
+    int64_t pages = 0;
+    int64_t chunk_q = 0;
+    int64_t masks = 0;
+    int64_t merge_ptr = 0;
+    int64_t merge_row = 0;
+    int64_t meta_end = 0;    // metadata [status, meta_end) is uploaded once
+    int64_t part_o = 0;      // fp32 [n_part_rows][d]
+    int64_t part_lse = 0;    // fp32 [n_part_rows] (log2 domain)
+    int64_t total = 0;
+};
+
+// Device-side view of a bound plan, passed by value to the kernels.
+struct DevPlan {
+    const DevItem* items;
+    const DevChunk* chunks;
+    const int32_t* pages;
+    const int32_t* chunk_q;
+    const uint64_t* masks;
+    const int32_t* merge_ptr;
+    const int32_t* merge_row;
+    float* part_o;
+    float* part_lse;
+    int32_t* status;
+    int32_t n_queries, n_q_heads, n_kv_heads, group, d, page_size;
+    float scale_log2;  // log2(e) / sqrt(d)
+};
+
+// Device status word codes (bit flags).
+enum : int32_t {
+    kStatusWaitTimeout = 1,  // a bounded mbarrier wait gave up
+    kStatusBadIndex = 2,     // a page or row index failed its range check
+};
+
+struct Tree {
+    int32_t n_nodes = 0;
+    int32_t page_size = 16;
+    int64_t num_pages = 0;
+    std::vector<int32_t> len, parent, first_offset, depth, preorder;
+    std::vector<int64_t> page_ptr;
+    std::vector<int32_t> page_ids;
+    std::vector<std::vector<int32_t>> children;
+};
+
+struct HostChunk {
+    int32_t task;          // index into tasks
+    int32_t node;          // node id, or -1 for a packed subtree
+    int32_t tok_begin;     // token range inside the node (node chunks)
+    int32_t tok_end;
+    int32_t kind;          // 0 CUDA-core, 1 tensor-core
+    DevChunk dev;
+};
+
+struct Task {              // CoDec T[i] = (n_q[i], n[i]) per kv head
+    int32_t node;          // -1 for a packed subtree
+    int32_t group;         // packed group index or -1
+    int32_t n_q;           // queries sharing it
+    int32_t rows;          // n_q * G
+    int32_t n_tok;
+    int32_t kind;
+    int32_t b_k = 1;       // KV-axis splits
+    int32_t max_splits = 1;
+};
+
+struct PackedGroup {
+    int32_t root;                      // the node whose descendants are packed
+    std::vector<int32_t> nodes;        // packed nodes in chunk order
+    std::vector<int32_t> tok_node;     // per chunk token: node
+    std::vector<int32_t> tok_t;        // per chunk token: token index in node
+    std::vector<int32_t> page_list;    // virtual page list
+    int32_t pos_begin = 0;
+    std::vector<int32_t> queries;      // ascending
+    std::vector<uint64_t> mask;        // per query
+};
+
+void set_error(const std::string& msg);
+int fail(int code, const std::string& msg);
+
+// cost model (plan.cpp)
+double cost_estimate(int kind, double rows, double tokens);
+
+}  // namespace pst
+
+struct pst_tree {
+    pst::Tree t;
+};
+
+struct pst_plan {
+    // inputs
+    int32_t n_queries = 0, hq = 0, hkv = 0, group = 0, d = 0;
+    pst_dtype dtype = PST_BF16;
+    int32_t page_size = 16;
+    int64_t num_pages = 0;
+    int32_t n_nodes = 0;
+    pst_plan_opts opts{};
+    // index (CSR)
+    std::vector<int32_t> qpath_ptr, qpath_node, nodeq_ptr, nodeq;
+    // partition
+    std::vector<pst::Task> tasks;
+    std::vector<pst::PackedGroup> groups;
+    std::vector<pst::HostChunk> chunks;
+    std::vector<int32_t> pages;        // tree pages + packed virtual page lists
+    std::vector<int32_t> chunk_q;
+    std::vector<uint64_t> masks;
+    std::vector<int32_t> merge_ptr, merge_row;
+    std::vector<pst::DevItem> items;   // tensor-core items first, then CUDA-core
+    int64_t n_tc_items = 0, n_cc_items = 0;
+    // CUDA-core items grouped by row tile 8, 4, 2, 1: offsets into items[] and counts
+    int64_t cc_class_off[4] = {0, 0, 0, 0}, cc_class_cnt[4] = {0, 0, 0, 0};
+    int64_t n_part_rows = 0;
+    // stats
+    double plan_us = 0, makespan_us = 0, cost_l_us = 0;
+    int32_t num_slots = 0;
+    int64_t kv_tokens_read = 0, unique_tokens = 0;
+    // device binding
+    pst::WsLayout ws;
+    std::vector<uint8_t> meta_blob;    // staged metadata image [0, meta_end)
+    void* d_ws = nullptr;
+    // cached TMA descriptors (built on first decode for a pool pointer)
+    mutable const void* tmap_k_ptr = nullptr;
+    mutable const void* tmap_v_ptr = nullptr;
+    alignas(64) mutable unsigned char tmap_k[128];
+    alignas(64) mutable unsigned char tmap_v[128];
+};

@@ -1,0 +1,78 @@
+"""torch glue for libpst: device memory and streams from torch, nothing else.
+
+``TreeDecodeAttention`` builds the tree and the plan once, allocates the plan's
+device workspace as a torch uint8 tensor, uploads the plan, and then runs
+``pst_decode_attn`` on torch tensors on the current (or given) stream.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import pst
+
+_TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def to_device(x: np.ndarray, dtype: str, device="cuda") -> torch.Tensor:
+    """Host array (uint16 bf16 bit patterns or float32) -> device tensor."""
+    if dtype == "bf16":
+        t = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).view(torch.bfloat16)
+    else:
+        t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(device)
+
+
+class TreeDecodeAttention:
+    def __init__(self, node_len, parent, page_ptr, page_ids, first_offset, page_size, num_pages,
+                 query_node, n_q_heads, n_kv_heads, d, dtype="bf16", device="cuda", **plan_opts):
+        self.device = torch.device(device)
+        self.dtype = dtype
+        self.n_q_heads, self.n_kv_heads, self.d = n_q_heads, n_kv_heads, d
+        self.n_queries = len(query_node)
+        self.num_pages, self.page_size = int(num_pages), int(page_size)
+        self.tree = pst.tree_build(node_len, parent, page_ptr, page_ids, first_offset, page_size, num_pages)
+        with torch.cuda.device(self.device):
+            if "num_sms" not in plan_opts:
+                plan_opts["num_sms"] = torch.cuda.get_device_properties(self.device).multi_processor_count
+            self.plan = pst.plan_create(self.tree, query_node, n_q_heads, n_kv_heads, d, dtype, **plan_opts)
+            self.workspace = torch.empty(max(256, self.plan.workspace_bytes), dtype=torch.uint8, device=self.device)
+            stream = torch.cuda.current_stream(self.device)
+            self.plan.upload(self.workspace.data_ptr(), self.workspace.numel(), stream.cuda_stream,
+                             keepalive=self.workspace)
+
+    @classmethod
+    def from_workload(cls, wl, device="cuda", **plan_opts):
+        return cls(wl.node_len, wl.parent, wl.page_ptr, wl.page_ids, wl.first_offset, wl.page_size,
+                   wl.num_pages, wl.query_node, wl.n_q_heads, wl.n_kv_heads, wl.d, wl.dtype, device,
+                   **plan_opts)
+
+    def _check(self, Q, K, V):
+        td = _TORCH_DTYPE[self.dtype]
+        for name, t in (("Q", Q), ("K_pool", K), ("V_pool", V)):
+            if t.dtype != td or t.device != self.device or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous {td} tensor on {self.device}")
+        if tuple(Q.shape) != (self.n_queries, self.n_q_heads, self.d):
+            raise ValueError(f"Q shape {tuple(Q.shape)}")
+        want = (self.num_pages, self.n_kv_heads, self.page_size, self.d)
+        if tuple(K.shape) != want or tuple(V.shape) != want:
+            raise ValueError(f"pool shape must be {want}")
+
+    def __call__(self, Q, K_pool, V_pool, O=None, LSE=None, stream=None, timer=None):
+        self._check(Q, K_pool, V_pool)
+        if O is None:
+            O = torch.empty((self.n_queries, self.n_q_heads, self.d), dtype=torch.float32, device=self.device)
+        if LSE is None:
+            LSE = torch.empty((self.n_queries, self.n_q_heads), dtype=torch.float32, device=self.device)
+        st = (stream or torch.cuda.current_stream(self.device)).cuda_stream
+        if timer is None:
+            pst.decode_attn(self.plan, Q.data_ptr(), K_pool.data_ptr(), V_pool.data_ptr(), O.data_ptr(),
+                            LSE.data_ptr(), st)
+        else:
+            pst.decode_attn_timed(self.plan, Q.data_ptr(), K_pool.data_ptr(), V_pool.data_ptr(),
+                                  O.data_ptr(), LSE.data_ptr(), st, timer)
+        return O, LSE
+
+    def check_status(self, stream=None) -> int:
+        st = (stream or torch.cuda.current_stream(self.device)).cuda_stream
+        return self.plan.check_status(st)

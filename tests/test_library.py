@@ -1,0 +1,196 @@
+"""Host-side checks of libpst (no GPU needed): the library loads and exports
+every function the header declares, tree_build rejects malformed trees, the
+KV-guided index matches the oracle bit for bit, and every plan covers each
+(query, KV token) pair exactly once."""
+import ctypes
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import tree as ot
+
+
+def test_exports_every_header_symbol(lib):
+    names = lib.header_functions()
+    assert len(names) >= 18
+    L = lib.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        assert ctypes.cast(getattr(L, n), ctypes.c_void_p).value
+
+
+def _tree(lib, wl, **kw):
+    return lib.tree_build(wl.node_len, wl.parent, wl.page_ptr, wl.page_ids, wl.first_offset,
+                          wl.page_size, wl.num_pages, **kw)
+
+
+def _plan(lib, wl, **kw):
+    t = _tree(lib, wl)
+    kw.setdefault("num_sms", 152)
+    return lib.plan_create(t, wl.query_node, wl.n_q_heads, wl.n_kv_heads, wl.d, wl.dtype, **kw)
+
+
+# ------------------------------------------------------------ validation
+
+def test_tree_build_rejects_bad_input(lib):
+    ok = dict(node_len=[20, 5], parent=[-1, 0], page_ptr=[0, 2, 3], page_ids=[0, 1, 2], num_pages=3)
+    lib.tree_build(**ok)
+
+    def code(**kw):
+        args = dict(ok)
+        args.update(kw)
+        with pytest.raises(lib.PstError) as e:
+            lib.tree_build(**args)
+        return e.value.code
+
+    assert code(parent=[1, 0]) == -2                        # cycle
+    assert code(parent=[-1, 5]) == -3                       # parent out of range
+    assert code(page_ids=[0, 1, 7]) == -3                   # page id >= num_pages
+    assert code(node_len=[40, 5]) == -3                     # overruns its 2 pages
+    assert code(first_offset=[0, 16]) == -3                 # offset >= page size
+    assert code(first_offset=[0, 12]) == -3                 # 12 + 5 > 16
+    assert code(page_size=24) == -4
+    assert code(node_len=[-1, 5]) == -1
+    assert code(page_ptr=[0, 3, 2]) == -1
+
+
+def test_plan_rejects_bad_input(lib):
+    wl = synth.random_tree(5)
+    t = _tree(lib, wl)
+    with pytest.raises(lib.PstError) as e:
+        lib.plan_create(t, wl.query_node, 6, 4, 64, "bf16", num_sms=8)
+    assert e.value.code == -4
+    with pytest.raises(lib.PstError) as e:
+        lib.plan_create(t, wl.query_node, 4, 2, 96, "bf16", num_sms=8)
+    assert e.value.code == -4
+    with pytest.raises(lib.PstError) as e:
+        lib.plan_create(t, [wl.n_nodes], 4, 2, 64, "bf16", num_sms=8)
+    assert e.value.code == -1
+    # a query whose whole path is empty sees no token
+    t2 = lib.tree_build([0, 3], [-1, -1], [0, 0, 1], [0], num_pages=1)
+    with pytest.raises(lib.PstError) as e:
+        lib.plan_create(t2, [0], 1, 1, 64, "f32", num_sms=8)
+    assert e.value.code == -1
+
+
+# ------------------------------------------------------------ index (bit-exact)
+
+def _workloads():
+    out = [synth.tiny_two_level(), synth.few_shot(), synth.document_qa(), synth.speculative(),
+           synth.tree_of_thought("gqa"), synth.trees.paged_example(), synth.trees.cascade_example()]
+    out += [synth.random_tree(1000 + s) for s in range(40)]
+    return out
+
+
+@pytest.mark.parametrize("wl", _workloads(), ids=lambda w: w.name)
+def test_index_matches_oracle(lib, wl):
+    e = _plan(lib, wl).export()
+    paths = ot.query_paths(wl.parent, wl.query_node)
+    want_ptr = np.cumsum([0] + [len(p) for p in paths])
+    assert np.array_equal(e["qpath_ptr"], want_ptr)
+    assert np.array_equal(e["qpath_node"], np.concatenate([np.array(p, np.int32) for p in paths]))
+    nq = ot.node_queries(wl.parent, wl.query_node, wl.n_nodes)
+    assert np.array_equal(e["nodeq_ptr"], np.cumsum([0] + [len(x) for x in nq]))
+    assert np.array_equal(e["nodeq"], np.array([q for x in nq for q in x], np.int32))
+
+
+def _covered_pairs(wl, e):
+    """Multiset of (query, node, token) the plan's chunks cover, as int64 codes."""
+    codes = []
+    tok_base = np.zeros(wl.n_nodes + 1, np.int64)
+    tok_base[1:] = np.cumsum(wl.node_len.astype(np.int64))
+    total = int(tok_base[-1])
+    for c in range(len(e["chunk_q_ptr"]) - 1):
+        qs = e["chunk_q"][e["chunk_q_ptr"][c]:e["chunk_q_ptr"][c + 1]].astype(np.int64)
+        masks = e["chunk_q_mask"][e["chunk_q_ptr"][c]:e["chunk_q_ptr"][c + 1]]
+        nodes = e["chunk_tok_node"][e["chunk_tok_ptr"][c]:e["chunk_tok_ptr"][c + 1]]
+        ts = e["chunk_tok_t"][e["chunk_tok_ptr"][c]:e["chunk_tok_ptr"][c + 1]]
+        gid = tok_base[nodes] + ts
+        j = np.arange(len(gid))
+        for q, m in zip(qs, masks):
+            if m == np.uint64(0xFFFFFFFFFFFFFFFF):
+                vis = np.ones(len(gid), bool)
+            else:
+                vis = ((np.uint64(m) >> j.astype(np.uint64)) & np.uint64(1)).astype(bool) if len(j) <= 64 else None
+                assert vis is not None, "masked chunk longer than 64 tokens"
+            codes.append(q * total + gid[vis])
+    return np.sort(np.concatenate(codes)) if codes else np.zeros(0, np.int64)
+
+
+def _visible_pairs(wl):
+    tok_base = np.zeros(wl.n_nodes + 1, np.int64)
+    tok_base[1:] = np.cumsum(wl.node_len.astype(np.int64))
+    total = int(tok_base[-1])
+    codes = []
+    for q, path in enumerate(ot.query_paths(wl.parent, wl.query_node)):
+        for n in path:
+            codes.append(q * total + tok_base[n] + np.arange(int(wl.node_len[n]), dtype=np.int64))
+    return np.sort(np.concatenate(codes))
+
+
+@pytest.mark.parametrize("policy", ["cost_model", "none", "uniform"])
+@pytest.mark.parametrize("wl", _workloads(), ids=lambda w: w.name)
+def test_plan_covers_each_pair_exactly_once(lib, wl, policy):
+    kw = {"split_policy": policy}
+    if policy == "uniform":
+        kw["fixed_chunk"] = 128
+    e = _plan(lib, wl, **kw).export()
+    got = _covered_pairs(wl, e)
+    want = _visible_pairs(wl)
+    assert got.shape == want.shape
+    assert np.array_equal(got, want)            # same multiset: nothing missing, nothing twice
+    # the merge list of each query names one partial row per chunk that contains it
+    for q in range(wl.n_queries):
+        rows = e["merge_row"][e["merge_ptr"][q]:e["merge_ptr"][q + 1]]
+        assert len(rows) == len(set(rows.tolist()))
+        n_chunks_with_q = sum(q in set(e["chunk_q"][e["chunk_q_ptr"][c]:e["chunk_q_ptr"][c + 1]].tolist())
+                              for c in range(len(e["chunk_q_ptr"]) - 1))
+        assert len(rows) == n_chunks_with_q
+
+
+def test_speculative_drafts_are_packed_with_masks(lib):
+    wl = synth.speculative()
+    e = _plan(lib, wl).export()
+    n_chunks = len(e["chunk_q_ptr"]) - 1
+    masked = [c for c in range(n_chunks)
+              if np.any(e["chunk_q_mask"][e["chunk_q_ptr"][c]:e["chunk_q_ptr"][c + 1]] != np.uint64(2**64 - 1))]
+    assert len(masked) == 8                     # one 64-token draft chunk per tree
+    for c in masked:
+        assert e["chunk_tok_ptr"][c + 1] - e["chunk_tok_ptr"][c] == 64
+        assert e["chunk_q_ptr"][c + 1] - e["chunk_q_ptr"][c] == 64
+        assert e["chunk_kind"][c] == 1          # 64 queries x 4 = 256 rows: tensor cores
+
+
+def test_kernel_choice_by_rows(lib):
+    wl = synth.document_qa()
+    e = _plan(lib, wl).export()
+    for c in range(len(e["chunk_q_ptr"]) - 1):
+        nq = e["chunk_q_ptr"][c + 1] - e["chunk_q_ptr"][c]
+        assert e["chunk_kind"][c] == (1 if nq * 4 >= 16 else 0)
+    e1 = _plan(lib, synth.tiny_two_level()).export()
+    assert not np.any(e1["chunk_kind"])         # fp32 never runs on tensor cores
+
+
+def test_planner_never_worse_than_fixed_splits(lib):
+    for wl in (synth.document_qa(), synth.few_shot(), synth.tree_of_thought("gqa"), synth.speculative()):
+        best = _plan(lib, wl).stats()["predicted_makespan_us"]
+        others = [_plan(lib, wl, split_policy="none").stats()["predicted_makespan_us"]]
+        for ch in (256, 1024, 4096):
+            others.append(_plan(lib, wl, split_policy="uniform", fixed_chunk=ch).stats()["predicted_makespan_us"])
+        assert best <= min(others) * (1 + 1e-9)
+
+
+def test_cost_table_interpolation(lib):
+    rows = [1, 4, 16, 256]
+    toks = [64, 1024, 16384]
+    us = np.array([[1, 2, 20], [1.5, 3, 30], [2, 4, 40], [4, 8, 80]], np.float32)
+    lib.cost_set_table(1, rows, toks, us)
+    try:
+        assert abs(lib.cost_estimate(1, 16, 1024) - 4.0) < 1e-5
+        assert abs(lib.cost_estimate(1, 4, 1024) - 3.0) < 1e-5
+        mid = lib.cost_estimate(1, 8, 1024)       # halfway in log rows
+        assert abs(mid - 3.5) < 1e-4
+        assert abs(lib.cost_estimate(1, 1000, 1e6) - 80) < 1e-4   # clamped
+    finally:
+        lib.cost_set_table(1, None, None, None)

@@ -1,0 +1,134 @@
+"""GPU parity: libpst's CUDA path against the fp64 oracle, element by element.
+
+Tolerances (fp32 output, bf16 or fp32 inputs): every |O - O_ref| <= 2e-3,
+per (query, head) row max|O - O_ref| / max(max|O_ref|, 1e-6) <= 1e-2, and
+|LSE - LSE_ref| <= 1e-3 (natural log)."""
+import numpy as np
+import pytest
+
+import synth
+from oracle import attention as oa
+
+pytestmark = pytest.mark.gpu
+
+ABS_TOL, REL_TOL, LSE_TOL = 2e-3, 1e-2, 1e-3
+
+
+def run_gpu(lib, wl, pools=None, Q=None, **opts):
+    import torch
+    from prefix_shared_tree_gb300.torch_api import TreeDecodeAttention, to_device
+    K, V = wl.kv_pools() if pools is None else pools
+    Q = wl.q() if Q is None else Q
+    att = TreeDecodeAttention.from_workload(wl, **opts)
+    Qd, Kd, Vd = to_device(Q, wl.dtype), to_device(K, wl.dtype), to_device(V, wl.dtype)
+    O, L = att(Qd, Kd, Vd)
+    torch.cuda.synchronize()
+    assert att.check_status() == 0
+    O2, L2 = att(Qd, Kd, Vd)
+    torch.cuda.synchronize()
+    assert torch.equal(O, O2) and torch.equal(L, L2), "repeated calls differ"
+    return O.cpu().numpy(), L.cpu().numpy(), (K, V, Q), att
+
+
+def assert_matches(wl, O, L, K, V, Q, queries=None):
+    qs = list(range(wl.n_queries)) if queries is None else list(queries)
+    Oref, Lref = oa.decode_attention(wl, K, V, Q, qs)
+    for q in qs:
+        o = O[q].astype(np.float64)
+        r = Oref[q]
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(L[q]))
+        err = np.abs(o - r)
+        assert err.max() <= ABS_TOL, f"query {q}: max abs {err.max():.3e}"
+        rel = err.max(axis=1) / np.maximum(np.abs(r).max(axis=1), 1e-6)
+        assert rel.max() <= REL_TOL, f"query {q}: row rel {rel.max():.3e}"
+        le = np.abs(L[q].astype(np.float64) - Lref[q])
+        assert le.max() <= LSE_TOL, f"query {q}: lse {le.max():.3e}"
+
+
+def test_tiny_two_level_fp32(lib):
+    wl = synth.tiny_two_level()
+    O, L, (K, V, Q), _ = run_gpu(lib, wl)
+    assert_matches(wl, O, L, K, V, Q)
+
+
+RANDOM_CASES = []
+for s in range(48):
+    heads = [(4, 2), (8, 1), (32, 8), (4, 4), (2, 1), (16, 16)][s % 6]
+    d = (64, 128)[(s // 6) % 2]
+    dtype = ("bf16", "bf16", "f32")[(s // 12) % 3]
+    RANDOM_CASES.append((s, heads, d, dtype))
+
+
+@pytest.mark.parametrize("seed,heads,d,dtype", RANDOM_CASES)
+def test_random_trees(lib, seed, heads, d, dtype):
+    wl = synth.random_tree(7000 + seed, max_nodes=14, max_len=150, heads=heads, d=d, dtype=dtype,
+                           n_queries=None)
+    O, L, (K, V, Q), _ = run_gpu(lib, wl)
+    assert_matches(wl, O, L, K, V, Q)
+
+
+@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("opts", [dict(tc_min_rows=1), dict(split_policy="uniform", fixed_chunk=64),
+                                  dict(split_policy="none"), dict(pack_masks=False)],
+                         ids=["all_tensor_core", "uniform64", "no_split", "no_masks"])
+def test_random_trees_plan_variants(lib, seed, opts):
+    wl = synth.random_tree(8000 + seed, max_nodes=12, max_len=300, heads=(8, 2), d=128, dtype="bf16",
+                           n_queries=24)
+    O, L, (K, V, Q), _ = run_gpu(lib, wl, **opts)
+    assert_matches(wl, O, L, K, V, Q)
+
+
+def test_non_finite_junk_in_unused_page_rows(lib):
+    """Rows of a page that no node covers may hold NaN; they never reach O."""
+    for seed in range(6):
+        wl = synth.random_tree(9100 + seed, max_nodes=10, max_len=90, heads=(8, 2), d=128, dtype="bf16",
+                               n_queries=20)
+        K, V = wl.kv_pools()
+        unused = (wl.row_lids() < 0).reshape(wl.num_pages, wl.page_size)
+        K[np.broadcast_to(unused[:, None, :, None], K.shape)] = 0x7FC0
+        V[np.broadcast_to(unused[:, None, :, None], V.shape)] = 0x7FC0
+        for opts in ({}, {"tc_min_rows": 1}):
+            O, L, _, _ = run_gpu(lib, wl, pools=(K, V), **opts)
+            assert_matches(wl, O, L, K, V, wl.q())
+
+
+def test_few_shot_full(lib):
+    wl = synth.few_shot()
+    O, L, (K, V, Q), att = run_gpu(lib, wl)
+    assert_matches(wl, O, L, K, V, Q)
+    st = att.plan.stats()
+    assert st["n_tc_items"] > 0 and st["n_cc_items"] > 0
+
+
+def test_document_qa_full_size_sampled(lib):
+    wl = synth.document_qa()
+    O, L, (K, V, Q), _ = run_gpu(lib, wl)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+    assert_matches(wl, O, L, K, V, Q, queries=[0, 17, 38, 63])
+
+
+def test_speculative_full_size_sampled(lib):
+    wl = synth.speculative()
+    O, L, (K, V, Q), _ = run_gpu(lib, wl)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+    # queries at every draft depth of tree 0 and a few of other trees
+    assert_matches(wl, O, L, K, V, Q, queries=[0, 9, 20, 40, 63, 64 * 3 + 11, 64 * 7 + 63])
+
+
+@pytest.mark.parametrize("variant", ["gqa", "mqa", "mha"])
+def test_tree_of_thought_full_size_sampled(lib, variant):
+    wl = synth.tree_of_thought(variant)
+    O, L, (K, V, Q), _ = run_gpu(lib, wl)
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+    assert_matches(wl, O, L, K, V, Q, queries=[0, 101, 255])
+
+
+def test_flat_control_matches_shared(lib):
+    """The no-sharing flat control (copied pages) computes the same outputs."""
+    wl = synth.few_shot()
+    O, L, (K, V, Q), _ = run_gpu(lib, wl)
+    fl = synth.flat_control(wl)
+    Of, Lf, (Kf, Vf, Qf), att = run_gpu(lib, fl)
+    assert np.array_equal(Qf, Q)
+    assert np.abs(Of - O).max() <= 2 * ABS_TOL and np.abs(Lf - L).max() <= 2 * LSE_TOL
+    assert_matches(fl, Of, Lf, Kf, Vf, Qf, queries=[0, 31, 63])
