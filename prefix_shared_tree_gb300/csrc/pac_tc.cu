@@ -49,6 +49,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// (a, b) -> bf16 pairs hi = rn(a, b) and lo = rn(a - hi_a, b - hi_b)
+__device__ __forceinline__ void split_bf16(float a, float b, uint32_t& hi, uint32_t& lo) {
+    hi = pack_bf16(a, b);
+    const float ha = __uint_as_float(hi << 16), hb = __uint_as_float(hi & 0xffff0000u);
+    lo = pack_bf16(a - ha, b - hb);
+}
+
 template <int D>
 __global__ void __launch_bounds__((kTcWarps + 1) * 32, 1)
 pac_tc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -188,7 +195,9 @@ pac_tc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
             mA = nA;
             mB = nB;
             float sumA = 0.f, sumB = 0.f;
-            uint32_t pa[4][4];
+            // P enters the PV product as bf16 hi + lo parts (p = hi + lo to about
+            // 2^-16 relative), so rounding P to bf16 costs no accuracy.
+            uint32_t pa[4][4], pl[4][4];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const float p0 = fast_exp2(sacc[j][0] - uA), p1 = fast_exp2(sacc[j][1] - uA);
@@ -196,8 +205,8 @@ pac_tc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
                 sumA += p0 + p1;
                 sumB += p2 + p3;
                 const int kk = j / 2, hi = j % 2;
-                pa[kk][hi * 2 + 0] = pack_bf16(p0, p1);
-                pa[kk][hi * 2 + 1] = pack_bf16(p2, p3);
+                split_bf16(p0, p1, pa[kk][hi * 2 + 0], pl[kk][hi * 2 + 0]);
+                split_bf16(p2, p3, pa[kk][hi * 2 + 1], pl[kk][hi * 2 + 1]);
             }
             lA = lA * aA + sumA;
             lB = lB * aB + sumB;
@@ -227,8 +236,14 @@ pac_tc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
                     const int ch = 2 * dp + idx / 2;
                     uint32_t b0, b1, b2, b3;
                     ldsm_x4_t(vb + (ch / 8) * kSlabBytes + swz(tok, ch % 8), b0, b1, b2, b3);
-                    mma_bf16(oacc[2 * dp], pa[kk], b0 & mlo, b1 & mhi);
-                    mma_bf16(oacc[2 * dp + 1], pa[kk], b2 & mlo, b3 & mhi);
+                    b0 &= mlo;
+                    b1 &= mhi;
+                    b2 &= mlo;
+                    b3 &= mhi;
+                    mma_bf16(oacc[2 * dp], pa[kk], b0, b1);
+                    mma_bf16(oacc[2 * dp + 1], pa[kk], b2, b3);
+                    mma_bf16(oacc[2 * dp], pl[kk], b0, b1);
+                    mma_bf16(oacc[2 * dp + 1], pl[kk], b2, b3);
                 }
             }
         }

@@ -27,6 +27,8 @@ class TreeDecodeAttention:
     def __init__(self, node_len, parent, page_ptr, page_ids, first_offset, page_size, num_pages,
                  query_node, n_q_heads, n_kv_heads, d, dtype="bf16", device="cuda", **plan_opts):
         self.device = torch.device(device)
+        if self.device.index is None:
+            self.device = torch.device(self.device.type, torch.cuda.current_device())
         self.dtype = dtype
         self.n_q_heads, self.n_kv_heads, self.d = n_q_heads, n_kv_heads, d
         self.n_queries = len(query_node)
