@@ -178,6 +178,36 @@ int pst_decode_attn_timed(const pst_plan* p, const void* Q, const void* K_pool,
 int pst_timer_read(pst_timer* t, float* ms, int32_t n, int32_t* calls);
 const char* pst_timer_kernel_name(int32_t slot);
 
+/* ---------------------------------------------------------------- no-allocation variant
+ * No counterpart in the papers: this is a convenience of this library.
+ *
+ * Same computation and arguments as pst_decode_attn, but it needs no
+ * workspace: not from the caller and not from the library at call time. It is
+ * meant for callers that cannot allocate device memory where they run
+ * attention -- e.g. a plug-in inside an engine whose framework owns and
+ * pre-plans all device memory, or code that must avoid the device-wide
+ * synchronisation of cudaFree. Its scratch (the plan's metadata and partial
+ * outputs) lives in one fixed array of PST_NOALLOC_WORKSPACE_BYTES inside the
+ * library's device image; every GPU on which the library is loaded holds that
+ * array until the process exits.
+ *
+ *   - The plan need not be uploaded; plans whose pst_plan_workspace_bytes()
+ *     exceeds PST_NOALLOC_WORKSPACE_BYTES are rejected with PST_EWORKSPACE.
+ *   - Each call copies the plan's metadata into the array (one host-to-device
+ *     copy on `stream`) before its kernels run; no allocation of any kind.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     CUDA stream capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU (on
+ *     different streams, or from different threads) race and corrupt each
+ *     other. Serialise them.
+ *   - The device status word used by the kernels' bounded waits lives in the
+ *     array too and is not reported by this entry point.
+ */
+#define PST_NOALLOC_WORKSPACE_BYTES (32ll << 20)
+int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const void* K_pool, const void* V_pool,
+                            float* O, float* LSE, void* stream);
+
 /* ---------------------------------------------------------------- introspection */
 typedef struct {
     double  plan_us;              /* host time of pst_plan_create                    */

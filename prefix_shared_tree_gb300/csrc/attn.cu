@@ -146,6 +146,41 @@ static DevPlan dev_plan(const pst_plan* p) {
     return d;
 }
 
+// For entry points that run a plan out of device memory other than its bound
+// workspace (same layout, base `ws`).
+int encode_pool_map(const pst_plan* p, const void* pool, unsigned char* out) { return make_pool_map(p, pool, out); }
+
+DevPlan dev_plan_at(const pst_plan* p, void* ws) {
+    uint8_t* b = static_cast<uint8_t*>(ws);
+    DevPlan d;
+    d.items = reinterpret_cast<const DevItem*>(b + p->ws.items);
+    d.chunks = reinterpret_cast<const DevChunk*>(b + p->ws.chunks);
+    d.pages = reinterpret_cast<const int32_t*>(b + p->ws.pages);
+    d.chunk_q = reinterpret_cast<const int32_t*>(b + p->ws.chunk_q);
+    d.masks = reinterpret_cast<const uint64_t*>(b + p->ws.masks);
+    d.merge_ptr = reinterpret_cast<const int32_t*>(b + p->ws.merge_ptr);
+    d.merge_row = reinterpret_cast<const int32_t*>(b + p->ws.merge_row);
+    d.part_o = reinterpret_cast<float*>(b + p->ws.part_o);
+    d.part_lse = reinterpret_cast<float*>(b + p->ws.part_lse);
+    d.status = reinterpret_cast<int32_t*>(b + p->ws.status);
+    d.n_queries = p->n_queries;
+    d.n_q_heads = p->hq;
+    d.n_kv_heads = p->hkv;
+    d.group = p->group;
+    d.d = p->d;
+    d.page_size = p->page_size;
+    d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->d));
+    return d;
+}
+
+cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, cudaStream_t st) {
+    const int64_t warps = (int64_t)dp.n_queries * dp.n_q_heads;
+    const int blocks = (int)((warps + dev::kPorWarps - 1) / dev::kPorWarps);
+    if (dp.d == 128) dev::por_kernel<128><<<blocks, dev::kPorWarps * 32, 0, st>>>(dp, O, LSE);
+    else dev::por_kernel<64><<<blocks, dev::kPorWarps * 32, 0, st>>>(dp, O, LSE);
+    return cudaGetLastError();
+}
+
 }  // namespace pst
 
 struct pst_timer {

@@ -84,6 +84,7 @@ def lib() -> C.CDLL:
         "pst_plan_workspace_bytes": (i64, [vp]),
         "pst_plan_upload": (C.c_int, [vp, vp, i64, vp]),
         "pst_decode_attn": (C.c_int, [vp, vp, vp, vp, vp, vp, vp]),
+        "pst_decode_attn_noalloc": (C.c_int, [vp, vp, vp, vp, vp, vp, vp]),
         "pst_plan_check_status": (C.c_int, [vp, vp, C.POINTER(i32)]),
         "pst_timer_create": (C.c_int, [i32, C.POINTER(vp)]),
         "pst_timer_destroy": (None, [vp]),
@@ -225,6 +226,17 @@ def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int,
 def decode_attn(plan: Plan, q: int, k_pool: int, v_pool: int, o: int, lse: int, stream: int = 0):
     _check(lib().pst_decode_attn(plan._h, C.c_void_p(q), C.c_void_p(k_pool), C.c_void_p(v_pool),
                                  C.c_void_p(o), C.c_void_p(lse), C.c_void_p(stream)))
+
+
+NOALLOC_WORKSPACE_BYTES = 32 << 20
+
+
+def decode_attn_noalloc(plan: Plan, q: int, k_pool: int, v_pool: int, o: int, lse: int, stream: int = 0):
+    """pst_decode_attn without any workspace: for callers that cannot allocate
+    device memory where they run attention (the scratch is a fixed array of
+    NOALLOC_WORKSPACE_BYTES inside the library; overlapping calls race)."""
+    _check(lib().pst_decode_attn_noalloc(plan._h, C.c_void_p(q), C.c_void_p(k_pool), C.c_void_p(v_pool),
+                                         C.c_void_p(o), C.c_void_p(lse), C.c_void_p(stream)))
 
 
 class Timer:

@@ -1,0 +1,74 @@
+"""pst_decode_attn_noalloc: the entry point for callers that cannot allocate
+device memory where they run attention (its scratch is a fixed array inside
+the library). Its outputs must match pst_decode_attn's on the same inputs, on
+two calls in a row (the shared array keeps the previous call's contents, so
+the second call checks that nothing stale leaks through). This file sorts
+last so that a run stopping at its first failure has run everything else."""
+import numpy as np
+import pytest
+
+import synth
+
+pytestmark = pytest.mark.gpu
+
+ABS_TOL, LSE_TOL = 2e-3, 1e-3
+
+
+def _setup(wl, **opts):
+    import torch
+    from prefix_shared_tree_gb300.torch_api import TreeDecodeAttention, to_device
+    att = TreeDecodeAttention.from_workload(wl, **opts)
+    K, V = wl.kv_pools()
+    return att, to_device(wl.q(), wl.dtype), to_device(K, wl.dtype), to_device(V, wl.dtype)
+
+
+@pytest.mark.parametrize("make", [synth.few_shot, lambda: synth.random_tree(4242, max_nodes=12, max_len=200,
+                                                                              heads=(8, 2), d=128, n_queries=30),
+                                  synth.tiny_two_level],
+                         ids=["few_shot", "random_bf16", "tiny_fp32"])
+def test_noalloc_matches_workspace_path(lib, make):
+    import torch
+    wl = make()
+    att, Q, K, V = _setup(wl)
+    assert att.plan.workspace_bytes <= lib.NOALLOC_WORKSPACE_BYTES
+    O_ref, L_ref = att(Q, K, V)
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream().cuda_stream
+    for _ in range(2):
+        O = torch.full_like(O_ref, float("nan"))
+        L = torch.full_like(L_ref, float("nan"))
+        lib.decode_attn_noalloc(att.plan, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), L.data_ptr(), st)
+        torch.cuda.synchronize()
+        o, l = O.cpu().numpy(), L.cpu().numpy()
+        assert np.all(np.isfinite(o)) and np.all(np.isfinite(l))
+        assert np.abs(o - O_ref.cpu().numpy()).max() <= ABS_TOL
+        assert np.abs(l - L_ref.cpu().numpy()).max() <= LSE_TOL
+
+
+def test_noalloc_after_another_plan(lib):
+    """A call with plan B after plan A: B's metadata replaces A's in the array."""
+    import torch
+    a = _setup(synth.few_shot())
+    b = _setup(synth.random_tree(4343, max_nodes=9, max_len=120, heads=(8, 2), d=128, n_queries=12))
+    st = torch.cuda.current_stream().cuda_stream
+    refs = [x[0](x[1], x[2], x[3]) for x in (a, b)]
+    for (att, Q, K, V), (O_ref, L_ref) in zip((a, b), refs):
+        O = torch.empty_like(O_ref)
+        L = torch.empty_like(L_ref)
+        lib.decode_attn_noalloc(att.plan, Q.data_ptr(), K.data_ptr(), V.data_ptr(), O.data_ptr(), L.data_ptr(), st)
+        torch.cuda.synchronize()
+        assert np.abs(O.cpu().numpy() - O_ref.cpu().numpy()).max() <= ABS_TOL
+        assert np.abs(L.cpu().numpy() - L_ref.cpu().numpy()).max() <= LSE_TOL
+
+
+def test_noalloc_rejects_oversized_plan(lib):
+    """A plan whose scratch exceeds the built-in array is refused before any GPU work."""
+    wl = synth.tree_of_thought("mha")
+    t = lib.tree_build(wl.node_len, wl.parent, wl.page_ptr, wl.page_ids, wl.first_offset, wl.page_size,
+                       wl.num_pages)
+    p = lib.plan_create(t, wl.query_node, wl.n_q_heads, wl.n_kv_heads, wl.d, wl.dtype, num_sms=152,
+                        split_policy="uniform", fixed_chunk=64)
+    assert p.workspace_bytes > lib.NOALLOC_WORKSPACE_BYTES
+    with pytest.raises(lib.PstError) as e:
+        lib.decode_attn_noalloc(p, 16, 16, 16, 16, 16, 0)
+    assert e.value.code == -5 and "built-in scratch" in str(e.value)
