@@ -67,6 +67,8 @@ typedef struct {
     int32_t num_sms;        /* 0: ask the current device                              */
     int32_t slots_per_sm;   /* concurrent PAC thread blocks per SM assumed by the
                                list schedule; 0: default (1)                         */
+    int32_t tc_engine;      /* tensor-core PAC: 0 (default) tcgen05 + tensor memory,
+                               1 legacy mma.sync (kept for comparison)               */
 } pst_plan_opts;
 
 /* Fill `o` with the defaults above. */

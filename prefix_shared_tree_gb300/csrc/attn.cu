@@ -27,6 +27,8 @@ cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const 
                           int r_tile, int n_items, int item_off, cudaStream_t st);
 cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
                           int item_off, cudaStream_t st);
+cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
+                            int item_off, cudaStream_t st);
 
 namespace dev {
 
@@ -240,7 +242,8 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
     cudaError_t e;
     // slot 0: tensor-core PAC, slot 1: CUDA-core PAC, slot 2: POR
     if (p->n_tc_items > 0) {
-        e = launch_pac_tc(dp, p->tmap_k, p->tmap_v, Q, (int)p->n_tc_items, 0, st);
+        e = p->opts.tc_engine == 1 ? launch_pac_tc(dp, p->tmap_k, p->tmap_v, Q, (int)p->n_tc_items, 0, st)
+                                   : launch_pac_umma(dp, p->tmap_k, p->tmap_v, Q, (int)p->n_tc_items, 0, st);
         if (e != cudaSuccess) return cuda_fail("decode_attn: PAC (tensor core) launch", e);
     }
     if (ev) cudaEventRecord(ev[++slot], st);

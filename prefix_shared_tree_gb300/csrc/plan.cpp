@@ -141,6 +141,7 @@ extern "C" void pst_plan_opts_default(pst_plan_opts* o) {
     o->pack_masks = 1;
     o->num_sms = 0;
     o->slots_per_sm = 1;
+    o->tc_engine = 0;
 }
 
 namespace {

@@ -22,6 +22,8 @@ cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const 
                           int r_tile, int n_items, int item_off, cudaStream_t st);
 cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
                           int item_off, cudaStream_t st);
+cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
+                            int item_off, cudaStream_t st);
 cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, cudaStream_t st);
 int encode_pool_map(const pst_plan* p, const void* pool, unsigned char* out);
 DevPlan dev_plan_at(const pst_plan* p, void* ws);
@@ -89,7 +91,8 @@ extern "C" int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const v
     if (rc) return rc;
     const DevPlan dp = dev_plan_at(p, ws);
     if (p->n_tc_items > 0) {
-        e = launch_pac_tc(dp, tk, tv, Q, (int)p->n_tc_items, 0, st);
+        e = p->opts.tc_engine == 1 ? launch_pac_tc(dp, tk, tv, Q, (int)p->n_tc_items, 0, st)
+                                   : launch_pac_umma(dp, tk, tv, Q, (int)p->n_tc_items, 0, st);
         if (e != cudaSuccess) return fail(PST_ECUDA, std::string("decode_attn_noalloc: PAC launch: ") + cudaGetErrorString(e));
     }
     for (int k = 0; k < 4; ++k) {

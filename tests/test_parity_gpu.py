@@ -69,8 +69,9 @@ def test_random_trees(lib, seed, heads, d, dtype):
 
 @pytest.mark.parametrize("seed", range(12))
 @pytest.mark.parametrize("opts", [dict(tc_min_rows=1), dict(split_policy="uniform", fixed_chunk=64),
-                                  dict(split_policy="none"), dict(pack_masks=False)],
-                         ids=["all_tensor_core", "uniform64", "no_split", "no_masks"])
+                                  dict(split_policy="none"), dict(pack_masks=False),
+                                  dict(tc_min_rows=1, tc_engine="mma_sync")],
+                         ids=["all_tensor_core", "uniform64", "no_split", "no_masks", "mma_sync"])
 def test_random_trees_plan_variants(lib, seed, opts):
     wl = synth.random_tree(8000 + seed, max_nodes=12, max_len=300, heads=(8, 2), d=128, dtype="bf16",
                            n_queries=24)
