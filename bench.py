@@ -70,6 +70,8 @@ def parse():
     ap.add_argument("--cpu-sample-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=90.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--plan-opt", action="append", default=[],
+                    help="planner option key=value (split_policy, fixed_chunk, tc_min_rows, tc_engine, ...)")
     return ap.parse_args()
 
 
@@ -233,7 +235,11 @@ def run_ours(args, rank, world):
     del K_np, V_np
 
     t0 = time.perf_counter()
-    att = TreeDecodeAttention.from_workload(wl, device=dev)
+    plan_opts = {}
+    for kv in args.plan_opt:
+        k, v = kv.split("=", 1)
+        plan_opts[k] = int(v) if v.lstrip("-").isdigit() else v
+    att = TreeDecodeAttention.from_workload(wl, device=dev, **plan_opts)
     plan_wall_us = (time.perf_counter() - t0) * 1e6
     st = att.plan.stats()
     ex = att.plan.export()

@@ -43,6 +43,7 @@ __global__ void __launch_bounds__(kPorWarps * 32) por_kernel(DevPlan P, float* _
     if (w >= (int64_t)P.n_queries * Hq) return;
     const int q = (int)(w / Hq), h = (int)(w % Hq);
     const int e0 = P.merge_ptr[q], e1 = P.merge_ptr[q + 1];
+    // the query's partials, 32 at a time: lane i holds entry i's row and weight
     float M = -INFINITY;
     for (int e = e0 + lane; e < e1; e += 32) M = fmaxf(M, P.part_lse[P.merge_row[e] + h]);
 #pragma unroll
@@ -52,21 +53,40 @@ __global__ void __launch_bounds__(kPorWarps * 32) por_kernel(DevPlan P, float* _
 #pragma unroll
     for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
     float W = 0.f;
-    for (int e = e0; e < e1; ++e) {
-        const int64_t row = (int64_t)P.merge_row[e] + h;
-        const float wt = fast_exp2(P.part_lse[row] - Mu);
-        W += wt;
-        const float* src = P.part_o + row * D + lane * EPL;
-        if constexpr (EPL == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            acc[0] = fmaf(wt, v.x, acc[0]);
-            acc[1] = fmaf(wt, v.y, acc[1]);
-            acc[2] = fmaf(wt, v.z, acc[2]);
-            acc[3] = fmaf(wt, v.w, acc[3]);
-        } else {
-            const float2 v = *reinterpret_cast<const float2*>(src);
-            acc[0] = fmaf(wt, v.x, acc[0]);
-            acc[1] = fmaf(wt, v.y, acc[1]);
+    for (int b = e0; b < e1; b += 32) {
+        const int cnt = min(32, e1 - b);
+        int64_t my_row = 0;
+        float my_w = 0.f;
+        if (lane < cnt) {
+            my_row = (int64_t)P.merge_row[b + lane] + h;
+            my_w = fast_exp2(P.part_lse[my_row] - Mu);
+        }
+        float ws = my_w;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+        W += ws;
+        // four partial rows in flight at a time
+        for (int i = 0; i < cnt; i += 4) {
+            float v[4][EPL];
+            float wt[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int src_lane = min(i + u, cnt - 1);
+                const int64_t row = __shfl_sync(0xffffffffu, my_row, src_lane);
+                wt[u] = i + u < cnt ? __shfl_sync(0xffffffffu, my_w, src_lane) : 0.f;
+                const float* src = P.part_o + row * D + lane * EPL;
+                if constexpr (EPL == 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(src);
+                    v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2*>(src);
+                    v[u][0] = x.x; v[u][1] = x.y;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int k = 0; k < EPL; ++k) acc[k] = fmaf(wt[u], v[u][k], acc[k]);
         }
     }
     const float inv = W > 0.f ? 1.f / W : 0.f;
@@ -189,6 +209,7 @@ struct pst_timer {
     int32_t max_calls = 0;
     int32_t calls = 0;
     int32_t n_slots = 0;                 // kernels per call in the recorded calls
+    int32_t forked = 0;                  // the CUDA-core PAC ran beside the tensor-core PAC
     std::vector<cudaEvent_t> ev;         // max_calls x (1 + kMaxKernels)
     static constexpr int kMaxKernels = 4;
 };
@@ -238,22 +259,49 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
         ev = timer->ev.data() + (size_t)timer->calls * (1 + pst_timer::kMaxKernels);
         cudaEventRecord(ev[0], st);
     }
-    int slot = 0;
     cudaError_t e;
-    // slot 0: tensor-core PAC, slot 1: CUDA-core PAC, slot 2: POR
+    // Both PAC kernels write disjoint partial rows; when a plan has both
+    // kinds, the CUDA-core PAC runs on a side stream forked from `st` so its
+    // blocks fill the SMs the tensor-core blocks leave idle, and POR waits on
+    // the join. Timer events: [0] start, [1] after the tensor-core PAC (st),
+    // [2] after the CUDA-core PAC (its stream), [3] after POR (st).
+    const bool fork = p->n_tc_items > 0 && p->n_cc_items > 0;
+    cudaStream_t cc_st = st;
+    if (fork) {
+        if (!p->side_stream) {
+            cudaStream_t s2;
+            cudaEvent_t a, b;
+            if ((e = cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking)) != cudaSuccess)
+                return cuda_fail("decode_attn: side stream", e);
+            if ((e = cudaEventCreateWithFlags(&a, cudaEventDisableTiming)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&b, cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail("decode_attn: fork/join events", e);
+            p->side_stream = s2;
+            p->ev_fork = a;
+            p->ev_join = b;
+        }
+        cc_st = static_cast<cudaStream_t>(p->side_stream);
+        cudaEventRecord(static_cast<cudaEvent_t>(p->ev_fork), st);
+        cudaStreamWaitEvent(cc_st, static_cast<cudaEvent_t>(p->ev_fork), 0);
+    }
     if (p->n_tc_items > 0) {
         e = p->opts.tc_engine == 1 ? launch_pac_tc(dp, p->tmap_k, p->tmap_v, Q, (int)p->n_tc_items, 0, st)
                                    : launch_pac_umma(dp, p->tmap_k, p->tmap_v, Q, (int)p->n_tc_items, 0, st);
         if (e != cudaSuccess) return cuda_fail("decode_attn: PAC (tensor core) launch", e);
     }
-    if (ev) cudaEventRecord(ev[++slot], st);
+    if (ev) cudaEventRecord(ev[1], st);
     for (int k = 0; k < 4; ++k) {
         if (p->cc_class_cnt[k] == 0) continue;
         e = launch_pac_cc(dp, p->dtype, p->tmap_k, p->tmap_v, Q, 8 >> k, (int)p->cc_class_cnt[k],
-                          (int)p->cc_class_off[k], st);
+                          (int)p->cc_class_off[k], cc_st);
         if (e != cudaSuccess) return cuda_fail("decode_attn: PAC (CUDA core) launch", e);
     }
-    if (ev) cudaEventRecord(ev[++slot], st);
+    if (ev) cudaEventRecord(ev[2], cc_st);
+    if (fork) {
+        cudaEventRecord(static_cast<cudaEvent_t>(p->ev_join), cc_st);
+        cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(p->ev_join), 0);
+    }
+    int slot = 2;
     {
         const int64_t warps = (int64_t)p->n_queries * p->hq;
         const int blocks = (int)((warps + dev::kPorWarps - 1) / dev::kPorWarps);
@@ -265,10 +313,20 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
     if (ev) {
         cudaEventRecord(ev[++slot], st);
         timer->n_slots = slot;
+        timer->forked = fork ? 1 : 0;
         timer->calls++;
     }
     return PST_OK;
 }
+
+namespace pst {
+void release_plan_streams(pst_plan* p) {
+    if (p->side_stream) cudaStreamDestroy(static_cast<cudaStream_t>(p->side_stream));
+    if (p->ev_fork) cudaEventDestroy(static_cast<cudaEvent_t>(p->ev_fork));
+    if (p->ev_join) cudaEventDestroy(static_cast<cudaEvent_t>(p->ev_join));
+    p->side_stream = p->ev_fork = p->ev_join = nullptr;
+}
+}  // namespace pst
 
 extern "C" int pst_decode_attn(const pst_plan* p, const void* Q, const void* K, const void* V, float* O, float* LSE,
                                void* stream) {
@@ -330,7 +388,9 @@ extern "C" int pst_timer_read(pst_timer* t, float* ms, int32_t n, int32_t* calls
     for (int c = 0; c < t->calls; ++c) {
         for (int k = 0; k < t->n_slots && k < n; ++k) {
             float x = 0.f;
-            cudaError_t e = cudaEventElapsedTime(&x, t->ev[(size_t)c * stride + k], t->ev[(size_t)c * stride + k + 1]);
+            // a forked CUDA-core PAC starts with the call, not after the tensor-core PAC
+            const int from = (k == 1 && t->forked) ? 0 : k;
+            cudaError_t e = cudaEventElapsedTime(&x, t->ev[(size_t)c * stride + from], t->ev[(size_t)c * stride + k + 1]);
             if (e != cudaSuccess) return cuda_fail("timer_read: cudaEventElapsedTime", e);
             ms[k] += x;
         }

@@ -9,29 +9,34 @@
 // statistics for the POR merge. DEFT's bit causal mask gives per-row
 // visibility inside packed draft-token chunks.
 //
-// One thread block per (chunk, kv head, block of 128 rows), warp-specialised:
+// One thread block per (chunk, kv head, block of up to 256 rows), warp-
+// specialised (10 warps):
 //   warp 0      TMA producer: 64-token K/V tiles (16-row page boxes, 128B
-//               swizzle) into a 4-stage ring;
-//   warp 1      allocates tensor memory and issues the MMAs from one thread:
-//               S_j = Q K_j^T (M=128, N=64, fp32 in tensor memory, double
-//               buffered) and O += P_j V_j (M=128, N=d) with V read MN-major;
-//   warps 2-5   softmax, one thread per row (= tensor-memory lane): read S_j,
-//               mask, online max/sum in the log2 domain, write P_j to shared
-//               memory as bf16 hi + lo parts (so rounding P costs no
-//               accuracy). The running max is only moved (and O rescaled in
-//               tensor memory) when it grows by more than 2^8, which keeps
-//               every exponent <= 8 and the result exact in fp32.
-// The MMA warp issues S_{j+1} before PV_j, so the softmax of one tile
-// overlaps the tensor-core work of the previous one.
+//               swizzle) into a 4-stage shared-memory ring;
+//   warp 1      allocates all 512 tensor-memory columns and issues every MMA
+//               from one thread: S = Q K^T (M=128, N=64) and O += P V
+//               (M=128, N=d; P read from tensor memory, V MN-major);
+//   warps 2-9   two softmax warpgroups, one thread per row (tensor-memory
+//               lane). With more than 128 rows each group owns one 128-row
+//               half and both consume every tile; with at most 128 rows the
+//               groups take alternate tiles into separate O accumulators
+//               and merge them at the end (split-KV inside the block). Either
+//               way two softmax warps share each scheduler.
+// Softmax works in the log2 domain with 1/sqrt(d) folded into one FMA; the
+// running max only moves (and O is rescaled in tensor memory) when it grows
+// by more than 2^8, so the result is exact in fp32. P overwrites its S
+// columns in tensor memory as bf16 hi + lo parts (p = hi + lo to ~2^-16),
+// which keeps the PV product as accurate as an fp32 one.
 #include "dev_common.cuh"
 #include "umma.cuh"
 
 namespace pst {
 namespace dev {
 
-constexpr int kUWarps = 6;       // producer, MMA, 4 softmax warps
+constexpr int kUWarps = 10;      // producer, MMA, 2 x 4 softmax warps
 constexpr int kUStages = 4;
 constexpr int kUThreads = kUWarps * 32;
+constexpr int kURows = 256;      // rows per block (two 128-row MMA halves)
 constexpr float kLazyRescale = 8.f;
 
 template <int D>
@@ -40,21 +45,34 @@ struct UmmaLayout {
     static constexpr uint32_t kSlab = kTileTokens * 128;          // one 64-row slab
     static constexpr uint32_t kHalf = NSLAB * kSlab;              // K or V of a stage
     static constexpr uint32_t kStage = 2 * kHalf;
-    static constexpr uint32_t kQSlab = kTcRowsPerBlock * 128;
+    static constexpr uint32_t kQSlab = 128 * 128;                 // 128 rows x 128 B
     static constexpr uint32_t kRing = kUStages * kStage;
-    static constexpr uint32_t kQ = kRing;                         // Q: NSLAB x 128 rows x 128 B
-    static constexpr uint32_t kPhi = kQ + NSLAB * kQSlab;         // P hi: 128 rows x 64 tokens bf16
-    static constexpr uint32_t kPlo = kPhi + kTcRowsPerBlock * 128;
-    static constexpr uint32_t kBars = kPlo + kTcRowsPerBlock * 128;
-    // barriers: kv_full[ST], kv_empty[ST], q_ready, s_full[2], p_full, o_done, mma_done, tmem slot
-    static constexpr uint32_t kBytes = kBars + 8 * (2 * kUStages + 6) + 16;
-    static constexpr uint32_t kTmemCols = 256;                    // S0 | S1 | O (<= 128 columns)
-    static constexpr uint32_t kColS = 0, kColO = 128;
+    static constexpr uint32_t kQ = kRing;                         // Q: 2 halves x NSLAB slabs
+    static constexpr uint32_t kXchg = kQ + 2 * NSLAB * kQSlab;    // 128 x (m, l) for the split-KV merge
+    static constexpr uint32_t kBars = kXchg + 128 * 8;
+    // kv_full[ST], kv_empty[ST], q_ready, s_full[2][2], p_full[2][2], o_done[2], mma_done, tmem slot
+    static constexpr int kNumBars = 2 * kUStages + 12;
+    static constexpr uint32_t kBytes = kBars + 8 * kNumBars + 16;
+    static constexpr uint32_t kTmemCols = 512;
+    // tensor-memory columns: S[w][b] at 128w + 64b (P hi/lo alias its first/second 32), O[w] at 256 + D*w
+    __device__ static constexpr uint32_t colS(int w, int b) { return 128 * w + 64 * b; }
+    __device__ static constexpr uint32_t colO(int w) { return 256 + D * w; }
 };
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 template <int D>
@@ -66,29 +84,40 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(base);
-    const uint32_t ring = sbase, sQ = sbase + L::kQ, sPhi = sbase + L::kPhi, sPlo = sbase + L::kPlo;
+    const uint32_t ring = sbase, sQ = sbase + L::kQ;
     const uint32_t bars = sbase + L::kBars;
     const uint32_t kv_full = bars, kv_empty = bars + 8 * kUStages;
     const uint32_t q_ready = bars + 16 * kUStages;
-    const uint32_t s_full = q_ready + 8;            // 2 barriers
-    const uint32_t p_full = s_full + 16, o_done = p_full + 8, mma_done = o_done + 8;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kBars + 8 * (2 * kUStages + 6));
+    // One p_full per S buffer: a group can then never complete two phases of
+    // the same barrier before the MMA warp has waited for the first.
+    const uint32_t s_full = q_ready + 8;      // [w][b] at s_full + 8*(2w+b)
+    const uint32_t p_full = s_full + 32;      // [w][b] at p_full + 8*(2w+b)
+    const uint32_t o_done = p_full + 32;      // [w]
+    const uint32_t mma_done = o_done + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kBars + 8 * L::kNumBars);
+    float2* xchg = reinterpret_cast<float2*>(base + L::kXchg);
 
     const DevItem it = P.items[item_off + blockIdx.x];
     const DevChunk C = P.chunks[it.chunk];
     const int head = it.kv_head, rb = it.row_block;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int G = P.group, Hq = P.n_q_heads;
+    const int rows_total = C.n_q * G;
+    const int row0 = rb * kURows;
+    const int rows_here = min(kURows, rows_total - row0);
+    const bool split_rows = rows_here > 128;   // mode A: groups own row halves; else alternate tiles
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kUStages; ++s) {
             mbar_init(kv_full + 8 * s, 1);
             mbar_init(kv_empty + 8 * s, 1);
         }
-        mbar_init(q_ready, 128);
-        mbar_init(s_full, 1);
-        mbar_init(s_full + 8, 1);
-        mbar_init(p_full, 128);
-        mbar_init(o_done, 1);
+        mbar_init(q_ready, 256);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(s_full + 8 * i, 1);
+            mbar_init(p_full + 8 * i, 128);
+        }
+        for (int w = 0; w < 2; ++w) mbar_init(o_done + 8 * w, 1);
         mbar_init(mma_done, 1);
         fence_barrier_init();
     }
@@ -102,6 +131,9 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     const uint32_t tmem = *tmem_slot;
     const ChunkGeo geo = chunk_geo(C);
     const int n = geo.n_tiles;
+    // steps of softmax group w: tiles it consumes, in order
+    auto n_steps = [&](int w) { return split_rows ? n : (n - w + 1) / 2; };
+    auto tile_of = [&](int w, int k) { return split_rows ? k : 2 * k + w; };
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
@@ -114,68 +146,89 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idS = umma::idesc_bf16_f32(128, kTileTokens, 0, 0);
-            constexpr uint32_t idO = umma::idesc_bf16_f32(128, D, 0, 1);
+            constexpr uint32_t idO = umma::idesc_bf16_f32(128, D, 0, 1);   // V is MN-major
             bool ok = mbar_wait(q_ready, 0, P.status);
             umma::fence_after_sync();
-            auto issue_pv = [&](int jj) {
-                const uint32_t vb = ring + (jj % kUStages) * L::kStage + L::kHalf;
+            // Descriptors are built once; an MMA only adds a compile-time byte
+            // offset (>> 4) to the start-address field, which keeps the single
+            // issuing thread far ahead of the tensor pipe. Shared-memory
+            // addresses stay below 2^18, so the field never carries over.
+            const uint64_t dq_base[2] = {umma::smem_desc_sw128(sQ, 16, 1024),
+                                         umma::smem_desc_sw128(sQ + NSLAB * L::kQSlab, 16, 1024)};
+            const uint64_t dk_base = umma::smem_desc_sw128(ring, 16, 1024);
+            const uint64_t dv_base = umma::smem_desc_sw128(ring + L::kHalf, L::kSlab, 1024);
+            auto issue_s = [&](int w, int k, int j) {
+                const uint64_t dq = dq_base[split_rows ? w : 0];
+                const uint64_t dk = dk_base + (uint64_t)(((j % kUStages) * L::kStage) >> 4);
+                const uint32_t dst = tmem + L::colS(w, k & 1);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma::mma_bf16_ss(dst, dq + (((kk / 4) * L::kQSlab + (kk % 4) * 32) >> 4),
+                                      dk + (((kk / 4) * L::kSlab + (kk % 4) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
+                umma::commit(s_full + 8 * (2 * w + (k & 1)));
+            };
+            // PV of step k of group w (tile j): O[w] += P_hi V + P_lo V
+            auto issue_pv = [&](int w, int k, int j) -> bool {
+                if (!mbar_wait(p_full + 8 * (2 * w + (k & 1)), (k >> 1) & 1, P.status)) return false;
+                umma::fence_after_sync();
+                const uint64_t dv = dv_base + (uint64_t)(((j % kUStages) * L::kStage) >> 4);
+                const uint32_t ps = tmem + L::colS(w, k & 1);
+                const uint32_t dst = tmem + L::colO(w);
+                const uint32_t acc0 = k > 0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < kTileTokens / 16; ++kk) {
-                    const uint64_t dv = umma::smem_desc_sw128(vb + kk * 2048, L::kSlab, 1024);
-                    const uint64_t dh = umma::smem_desc_sw128(sPhi + kk * 32, 16, 1024);
-                    const uint64_t dl = umma::smem_desc_sw128(sPlo + kk * 32, 16, 1024);
-                    umma::mma_bf16_ss(tmem + L::kColO, dh, dv, idO, (jj > 0 || kk > 0) ? 1u : 0u);
-                    umma::mma_bf16_ss(tmem + L::kColO, dl, dv, idO, 1u);
+                    mma_bf16_ts(dst, ps + 8 * kk, dv + ((kk * 2048) >> 4), idO, kk > 0 ? 1u : acc0);
+                    mma_bf16_ts(dst, ps + 32 + 8 * kk, dv + ((kk * 2048) >> 4), idO, 1u);
                 }
-                umma::commit(o_done);
-                umma::commit(kv_empty + 8 * (jj % kUStages));
+                umma::commit(o_done + 8 * w);
+                return true;
             };
             for (int j = 0; j < n && ok; ++j) {
                 const int s = j % kUStages;
                 if (!mbar_wait(kv_full + 8 * s, (j / kUStages) & 1, P.status)) { ok = false; break; }
-                const uint32_t kb = ring + s * L::kStage;
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t dq = umma::smem_desc_sw128(sQ + (kk / 4) * L::kQSlab + (kk % 4) * 32, 16, 1024);
-                    const uint64_t dk = umma::smem_desc_sw128(kb + (kk / 4) * L::kSlab + (kk % 4) * 32, 16, 1024);
-                    umma::mma_bf16_ss(tmem + L::kColS + (j & 1) * kTileTokens, dq, dk, idS, kk > 0 ? 1u : 0u);
-                }
-                umma::commit(s_full + 8 * (j & 1));
-                if (j >= 1) {
-                    if (!mbar_wait(p_full, (j - 1) & 1, P.status)) { ok = false; break; }
-                    umma::fence_after_sync();
-                    issue_pv(j - 1);
+                if (split_rows) {
+                    issue_s(0, j, j);
+                    issue_s(1, j, j);
+                    if (j >= 1) {
+                        if (!issue_pv(0, j - 1, j - 1) || !issue_pv(1, j - 1, j - 1)) { ok = false; break; }
+                        umma::commit(kv_empty + 8 * ((j - 1) % kUStages));
+                    }
+                } else {
+                    issue_s(j & 1, j >> 1, j);
+                    if (j >= 1) {
+                        if (!issue_pv((j - 1) & 1, (j - 1) >> 1, j - 1)) { ok = false; break; }
+                        umma::commit(kv_empty + 8 * ((j - 1) % kUStages));
+                    }
                 }
             }
             if (ok && n >= 1) {
-                if (mbar_wait(p_full, (n - 1) & 1, P.status)) {
-                    umma::fence_after_sync();
-                    issue_pv(n - 1);
-                }
+                const int j = n - 1;
+                bool good = split_rows ? (issue_pv(0, j, j) && issue_pv(1, j, j)) : issue_pv(j & 1, j >> 1, j);
+                if (good) umma::commit(kv_empty + 8 * (j % kUStages));
             }
             // every MMA issued above has finished before tensor memory is released
             umma::commit(mma_done);
             mbar_wait(mma_done, 0, P.status);
         }
     } else {
-        // ------------------------------------------------------------ softmax warps
-        const int r = 32 * (warp % 4) + lane;       // row = tensor-memory lane
+        // ------------------------------------------------------------ softmax warpgroups
+        const int w = (warp - 2) / 4;                // group 0: warps 2-5, group 1: warps 6-9
+        const int r = 32 * (warp % 4) + lane;        // tensor-memory lane = row within the half
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp % 4)) << 16);
-        const int G = P.group, Hq = P.n_q_heads;
-        const int rows_total = C.n_q * G;
-        const int row0 = rb * kTcRowsPerBlock;
-        const int rows_here = min(kTcRowsPerBlock, rows_total - row0);
-        const bool row_ok = r < rows_here;
+        const int rloc = split_rows ? 128 * w + r : r;   // row within the block
+        const bool row_ok = rloc < rows_here;
         int qi = 0, gh = 0;
         uint64_t mask = ~0ull;
-        {
-            uint8_t* qdst = base + L::kQ;
+        if (row_ok) {
+            qi = (row0 + rloc) / G;
+            gh = (row0 + rloc) % G;
+            if (C.mask_base >= 0) mask = P.masks[C.mask_base + qi];
+        }
+        if (split_rows || w == 0) {
+            uint8_t* qdst = base + L::kQ + (split_rows ? w : 0) * NSLAB * L::kQSlab;
             if (row_ok) {
-                qi = (row0 + r) / G;
-                gh = (row0 + r) % G;
                 const int qid = P.chunk_q[C.q_base + qi];
                 const uint8_t* src = reinterpret_cast<const uint8_t*>(Q + ((int64_t)qid * Hq + head * G + gh) * D);
-                if (C.mask_base >= 0) mask = P.masks[C.mask_base + qi];
 #pragma unroll
                 for (int ch = 0; ch < NSLAB * 8; ++ch)
                     *reinterpret_cast<uint4*>(qdst + (ch / 8) * L::kQSlab + swz(r, ch % 8)) =
@@ -185,25 +238,28 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 for (int ch = 0; ch < NSLAB * 8; ++ch)
                     *reinterpret_cast<uint4*>(qdst + (ch / 8) * L::kQSlab + swz(r, ch % 8)) = make_uint4(0, 0, 0, 0);
             }
+            fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
         mbar_arrive(q_ready);
 
         const float sl = P.scale_log2;
         const bool masked_chunk = C.mask_base >= 0;
-        float m_ref = -INFINITY, l = 0.f;
+        const bool zero_v = split_rows ? (w == 0) : true;   // one group zeroes a tile's stray V rows
+        float m_ref = -INFINITY, l = 0.f;                      // raw-score units for m_ref
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
-            if (!mbar_wait(s_full + 8 * (j & 1), (j >> 1) & 1, P.status)) { ok = false; break; }
+        const int nk = n_steps(w);
+        for (int k = 0; k < nk; ++k) {
+            const int j = tile_of(w, k);
+            const int b = k & 1;
+            if (!mbar_wait(s_full + 8 * (2 * w + b), (k >> 1) & 1, P.status)) { ok = false; break; }
             umma::fence_after_sync();
             float x[kTileTokens];
             {
                 float v[32];
-                umma::ld32(lane_addr + L::kColS + (j & 1) * kTileTokens, v);
-                umma::wait_ld();
+                umma::ld32(lane_addr + L::colS(w, b), v);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) x[c] = v[c];
-                umma::ld32(lane_addr + L::kColS + (j & 1) * kTileTokens + 32, v);
+                umma::ld32(lane_addr + L::colS(w, b) + 32, v);
                 umma::wait_ld();
 #pragma unroll
                 for (int c = 0; c < 32; ++c) x[32 + c] = v[c];
@@ -217,90 +273,121 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                     const int pos = tpos + c;
                     const int t = pos - geo.pos_begin;
                     const bool vis = pos >= geo.pos_begin && pos < geo.pos_end && (t >= 64 || ((mask >> (t & 63)) & 1ull));
-                    x[c] = vis ? x[c] * sl : -INFINITY;
+                    x[c] = vis ? x[c] : -INFINITY;
                     mx = fmaxf(mx, x[c]);
                 }
             } else {
 #pragma unroll
-                for (int c = 0; c < kTileTokens; ++c) {
-                    x[c] *= sl;
-                    mx = fmaxf(mx, x[c]);
-                }
+                for (int c = 0; c < kTileTokens; ++c) mx = fmaxf(mx, x[c]);
             }
-            // PV_{j-1} must have finished: it reads the P buffer and writes O
-            if (j >= 1) {
-                if (!mbar_wait(o_done, (j - 1) & 1, P.status)) { ok = false; break; }
-                umma::fence_after_sync();
-            }
-            const bool grow = (m_ref == -INFINITY) ? (mx != -INFINITY) : (mx > m_ref + kLazyRescale);
+            // P_k overwrites the S columns of step k-2, whose PV finished before
+            // S_k (issued later on the same in-order tensor pipe) completed.
+            const float mxs = mx * sl;   // scale > 0: max commutes with it
+            const bool grow = (m_ref == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref + kLazyRescale);
             bool rescaled = false;
             if (grow) {
-                const float alpha = fast_exp2(m_ref - mx);   // 0 when nothing was accumulated
-                if (j >= 1 && m_ref != -INFINITY) {
+                const float alpha = fast_exp2(m_ref - mxs);   // 0 when nothing was accumulated
+                if (k >= 1 && m_ref != -INFINITY) {
+                    // O is about to be rescaled: the previous PV of this group must be
+                    // done. When S_k has completed, every PV before step k-1 has too,
+                    // so o_done is at most one phase behind and the parity wait is exact.
+                    if (!mbar_wait(o_done + 8 * w, (k - 1) & 1, P.status)) { ok = false; break; }
+                    umma::fence_after_sync();
 #pragma unroll 1
                     for (int c = 0; c < D / 32; ++c) {
                         float o[32];
-                        umma::ld32(lane_addr + L::kColO + 32 * c, o);
+                        umma::ld32(lane_addr + L::colO(w) + 32 * c, o);
                         umma::wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        umma::st32(lane_addr + L::kColO + 32 * c, o);
+                        umma::st32(lane_addr + L::colO(w) + 32 * c, o);
                     }
                     rescaled = true;
                 }
                 l *= alpha;
-                m_ref = mx;
+                m_ref = mxs;
             }
-            const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-            uint8_t* phi = base + L::kPhi;
-            uint8_t* plo = base + L::kPlo;
+            const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
+            float hi[32], lo[32];
             float sum = 0.f;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                uint32_t h[4], lo[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const float a = fast_exp2(x[8 * ch + 2 * k] - mu);
-                    const float b = fast_exp2(x[8 * ch + 2 * k + 1] - mu);
-                    sum += a + b;
-                    h[k] = bf16x2_bits(a, b);
-                    lo[k] = bf16x2_bits(a - __uint_as_float(h[k] << 16), b - __uint_as_float(h[k] & 0xffff0000u));
-                }
-                *reinterpret_cast<uint4*>(phi + swz(r, ch)) = make_uint4(h[0], h[1], h[2], h[3]);
-                *reinterpret_cast<uint4*>(plo + swz(r, ch)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            for (int c = 0; c < 32; ++c) {
+                const float a = fast_exp2(fmaf(x[2 * c], sl, nmu));
+                const float bb = fast_exp2(fmaf(x[2 * c + 1], sl, nmu));
+                sum += a + bb;
+                const uint32_t h = bf16x2_bits(a, bb);
+                hi[c] = __uint_as_float(h);
+                lo[c] = __uint_as_float(bf16x2_bits(a - __uint_as_float(h << 16), bb - __uint_as_float(h & 0xffff0000u)));
             }
             l += sum;
-            if (edge) {
+            umma::st32(lane_addr + L::colS(w, b), hi);
+            umma::st32(lane_addr + L::colS(w, b) + 32, lo);
+            bool zeroed = false;
+            if (edge && zero_v) {
                 // V rows outside the chunk may hold stale or non-finite values:
-                // zero them before PV_j multiplies them by P = 0.
+                // zero them before the PV of this tile multiplies them by P = 0.
                 const int s = j % kUStages;
                 if (!mbar_wait(kv_full + 8 * s, (j / kUStages) & 1, P.status)) { ok = false; break; }
-                if (r < kTileTokens * NSLAB) {
+                if (r < kTileTokens * NSLAB) {          // one 128-byte slab row per thread
                     const int t = r % kTileTokens, sl_i = r / kTileTokens;
                     const int pos = tpos + t;
                     if (pos < geo.pos_begin || pos >= geo.pos_end) {
                         uint8_t* vrow = base + s * L::kStage + L::kHalf + sl_i * L::kSlab + t * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0, 0, 0, 0);
+                        zeroed = true;
                     }
                 }
             }
-            if (rescaled) umma::wait_st();
-            fence_proxy_async_smem();
+            umma::wait_st();
+            (void)rescaled;
+            if (zeroed) fence_proxy_async_smem();
             umma::fence_before_sync();
-            mbar_arrive(p_full);
+            mbar_arrive(p_full + 8 * (2 * w + b));
         }
-        // ---- epilogue: O / l to the partial-output rows
-        if (ok && n >= 1 && mbar_wait(o_done, (n - 1) & 1, P.status)) {
-            umma::fence_after_sync();
+        // ---- epilogue: wait for the MMA warp's final commit (every MMA done)
+        bool have = ok && nk >= 1 && mbar_wait(mma_done, 0, P.status);
+        if (have) umma::fence_after_sync();
+        if (!split_rows) {
+            // split-KV inside the block: group 1 hands (m, l) to group 0, which
+            // reads both O accumulators (same lanes) and merges them
+            if (w == 1) {
+                xchg[r] = make_float2(have ? m_ref : -INFINITY, have ? l : 0.f);
+                asm volatile("bar.arrive 1, 256;" ::: "memory");
+            } else {
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+            }
+        }
+        if (have && (split_rows || w == 0)) {
+            float m1 = -INFINITY, l1 = 0.f;
+            if (!split_rows) {
+                const float2 ml = xchg[r];
+                m1 = ml.x;
+                l1 = ml.y;
+            }
+            const bool use1 = !split_rows && n >= 2;   // group 1's accumulator is complete (mma_done)
+            const float M = fmaxf(m_ref, m1);
+            const float Mu = M == -INFINITY ? 0.f : M;
+            const float a0 = fast_exp2(m_ref - Mu), a1 = fast_exp2(m1 - Mu);
+            const float Lt = l * a0 + l1 * a1;
+            const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
             const int64_t prow = (int64_t)C.part_base + (int64_t)qi * Hq + head * G + gh;
-            const float inv = l > 0.f ? 1.f / l : 0.f;
             float* dst = P.part_o + prow * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];
-                umma::ld32(lane_addr + L::kColO + 32 * c, o);
+                umma::ld32(lane_addr + L::colO(w) + 32 * c, o);
                 umma::wait_ld();
+                if (use1) {
+                    float o1[32];
+                    umma::ld32(lane_addr + L::colO(1) + 32 * c, o1);
+                    umma::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = o[i] * a0 + o1[i] * a1;
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= a0;
+                }
                 if (row_ok) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 4)
@@ -308,7 +395,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                             make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
                 }
             }
-            if (row_ok) P.part_lse[prow] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+            if (row_ok) P.part_lse[prow] = Lt > 0.f ? M + __log2f(Lt) : -INFINITY;
         }
     }
     umma::fence_before_sync();

@@ -62,8 +62,15 @@ static double analytic_cost(int kind, double rows, double tokens, double bytes_p
     const double mem = tokens * bytes_per_tok / bw_sm;
     double cmp;
     if (kind == 1) {
-        const double rpad = std::ceil(rows / 16.0) * 16.0;
-        cmp = tokens * rpad * 4.0 * d / (3.0e6);               // flop per us per SM (mma.sync)
+        // tcgen05 (measured on GB300): a 64-token tile costs ~3300 clk with
+        // two 128-row halves (S = Q K^T and the hi and lo PV products share
+        // the tensor pipe and tensor memory with the softmax's loads and
+        // stores) and ~1000 clk with one half split over the two softmax
+        // groups; ~2 GHz
+        const double per_tok = rows > 128 ? 52.0 : 16.0;
+        const double t_mma = tokens * per_tok * (d / 128.0) / 2000.0;
+        const double t_sfu = tokens * rows / (16.0 * 2000.0);
+        cmp = std::max(t_mma, t_sfu);
     } else {
         const double instr = 8.0 + 11.0 * rows;                // warp instructions per token
         cmp = tokens * instr * (d / 128.0) / (4.0 * 1800.0);   // 4 issue/clk at 1.8 GHz
@@ -220,7 +227,7 @@ struct Planner {
     }
 
     int rows_per_block(const Task& t) const {
-        return t.kind == 1 ? kTcRowsPerBlock : cc_row_tile(t.rows);
+        return t.kind == 1 ? tc_rows_per_block(P.opts.tc_engine) : cc_row_tile(t.rows);
     }
 
     // per-item cost and item count of task t split b ways
@@ -584,7 +591,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
                 c.dev.q_base = (int32_t)P->chunk_q.size();
                 c.dev.n_q = t.n_q;
                 c.dev.mask_base = -1;
-                c.dev.r_tile = t.kind == 1 ? kTcRowsPerBlock : cc_row_tile(t.rows);
+                c.dev.r_tile = t.kind == 1 ? tc_rows_per_block(o.tc_engine) : cc_row_tile(t.rows);
                 P->chunk_q.insert(P->chunk_q.end(), P->nodeq.begin() + P->nodeq_ptr[t.node],
                                   P->nodeq.begin() + P->nodeq_ptr[t.node + 1]);
                 P->chunks.push_back(c);
@@ -604,7 +611,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
             c.dev.q_base = (int32_t)P->chunk_q.size();
             c.dev.n_q = t.n_q;
             c.dev.mask_base = (int32_t)P->masks.size();
-            c.dev.r_tile = t.kind == 1 ? kTcRowsPerBlock : cc_row_tile(t.rows);
+            c.dev.r_tile = t.kind == 1 ? tc_rows_per_block(o.tc_engine) : cc_row_tile(t.rows);
             P->chunk_q.insert(P->chunk_q.end(), g.queries.begin(), g.queries.end());
             P->masks.insert(P->masks.end(), g.mask.begin(), g.mask.end());
             P->chunks.push_back(c);
@@ -696,7 +703,14 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     return PST_OK;
 }
 
-extern "C" void pst_plan_destroy(pst_plan* p) { delete p; }
+namespace pst {
+void release_plan_streams(pst_plan* p);  // attn.cu
+}
+extern "C" void pst_plan_destroy(pst_plan* p) {
+    if (!p) return;
+    pst::release_plan_streams(p);
+    delete p;
+}
 
 extern "C" int64_t pst_plan_workspace_bytes(const pst_plan* p) { return p ? p->ws.total : -1; }
 

@@ -6,12 +6,15 @@
 #include <string>
 #include <vector>
 
-#include "../../include/pst.h"
+#include "pst.h"
 
 namespace pst {
 
-// Rows of the tensor-core PAC per thread block (8 warps x 16 rows).
+// Rows of the tensor-core PAC per thread block: 128 for the mma.sync kernel
+// (8 warps x 16 rows), 256 for the tcgen05 kernel (two M=128 halves).
 constexpr int kTcRowsPerBlock = 128;
+constexpr int kUmmaRowsPerBlock = 256;
+inline int tc_rows_per_block(int tc_engine) { return tc_engine == 1 ? kTcRowsPerBlock : kUmmaRowsPerBlock; }
 // Rows of the CUDA-core PAC per thread block (largest row tile).
 constexpr int kCcRowsPerBlock = 8;
 // KV tokens per pipeline stage of both PAC kernels (4 boxes of 16 rows).
@@ -165,6 +168,11 @@ struct pst_plan {
     pst::WsLayout ws;
     std::vector<uint8_t> meta_blob;    // staged metadata image [0, meta_end)
     void* d_ws = nullptr;
+    // side stream and fork/join events (cudaStream_t / cudaEvent_t) used to run
+    // the CUDA-core PAC next to the tensor-core PAC; created on first use
+    mutable void* side_stream = nullptr;
+    mutable void* ev_fork = nullptr;
+    mutable void* ev_join = nullptr;
     // cached TMA descriptors (built on first decode for a pool pointer)
     mutable const void* tmap_k_ptr = nullptr;
     mutable const void* tmap_v_ptr = nullptr;
