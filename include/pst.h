@@ -69,6 +69,8 @@ typedef struct {
                                list schedule; 0: default (1)                         */
     int32_t tc_engine;      /* tensor-core PAC: 0 (default) tcgen05 + tensor memory,
                                1 legacy mma.sync (kept for comparison)               */
+    int32_t tc_block_rows;  /* tcgen05 PAC rows per thread block: 256 (default; two
+                               128-row halves share each K/V tile) or 128            */
 } pst_plan_opts;
 
 /* Fill `o` with the defaults above. */

@@ -161,5 +161,48 @@ __device__ void produce_chunk(const DevPlan& P, const DevChunk& C, int head, uin
     }
 }
 
+// TMA producer for one operand (K when `vee` is false, V when true) with its
+// own full/empty barriers, so K stages can be refilled as soon as Q K^T has
+// read them while V stages wait for P V. Stage s holds K at
+// ring + s*stage_bytes and V right after it (NSLAB slabs each).
+template <int NSLAB, int STAGES, int ELEMS_PER_SLAB>
+__device__ void produce_operand(const DevPlan& P, const DevChunk& C, int head, uint32_t ring, uint32_t stage_bytes,
+                                uint32_t bar_full, uint32_t bar_empty, const CUtensorMap* map, bool vee) {
+    constexpr uint32_t kSlabBytes = kTileTokens * 128;
+    constexpr uint32_t kHalf = NSLAB * kSlabBytes;
+    const ChunkGeo g = chunk_geo(C);
+    const int ps = P.page_size;
+    const int n_list = (g.pos_end - 1) / ps + 1;
+    for (int i = 0; i < g.n_tiles; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES) {
+            if (!mbar_wait(bar_empty + 8 * s, ((i / STAGES) - 1) & 1, P.status)) return;
+        }
+        const int tpos = g.tile0 + i * kTileTokens;
+        uint32_t nbox = 0;
+#pragma unroll
+        for (int b = 0; b < kTileTokens / kBoxRows; ++b) {
+            const int pos = tpos + b * kBoxRows;
+            if (pos + kBoxRows > g.pos_begin && pos < g.pos_end) ++nbox;
+        }
+        const uint32_t full = bar_full + 8 * s;
+        mbar_arrive_expect_tx(full, nbox * NSLAB * kBoxRows * 128u);
+        const uint32_t dst0 = ring + s * stage_bytes + (vee ? kHalf : 0);
+#pragma unroll
+        for (int b = 0; b < kTileTokens / kBoxRows; ++b) {
+            const int pos = tpos + b * kBoxRows;
+            if (!(pos + kBoxRows > g.pos_begin && pos < g.pos_end)) continue;
+            const int li = pos / ps;
+            int page = 0;
+            if (li < n_list) page = P.pages[C.page_base + li];
+            const int slab_z = page * P.n_kv_heads + head;
+            const int row0 = pos % ps;
+#pragma unroll
+            for (int sl = 0; sl < NSLAB; ++sl)
+                tma_load_3d(dst0 + sl * kSlabBytes + b * kBoxRows * 128, map, sl * ELEMS_PER_SLAB, row0, slab_z, full);
+        }
+    }
+}
+
 }  // namespace dev
 }  // namespace pst

@@ -25,6 +25,28 @@ namespace dev {
 constexpr int kCcWarps = 4;
 constexpr int kCcStages = 2;
 
+using u64 = unsigned long long;
+
+// Two floats in one 64-bit register pair, for Blackwell's packed f32x2 ALU ops.
+__device__ __forceinline__ u64 pk2(float a, float b) {
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(u64 r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+    u64 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+    u64 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 template <typename T>
 struct ElemTraits;
 template <>
@@ -37,6 +59,13 @@ struct ElemTraits<__nv_bfloat16> {
         out[4] = bf16lo(v.z); out[5] = bf16hi(v.z);
         out[6] = bf16lo(v.w); out[7] = bf16hi(v.w);
     }
+    // 16-byte chunk -> 4 packed pairs (element order kept)
+    __device__ __forceinline__ static void unpack2(const uint4& v, u64* out) {
+        out[0] = pk2(bf16lo(v.x), bf16hi(v.x));
+        out[1] = pk2(bf16lo(v.y), bf16hi(v.y));
+        out[2] = pk2(bf16lo(v.z), bf16hi(v.z));
+        out[3] = pk2(bf16lo(v.w), bf16hi(v.w));
+    }
 };
 template <>
 struct ElemTraits<float> {
@@ -44,6 +73,10 @@ struct ElemTraits<float> {
     __device__ __forceinline__ static void unpack(const uint4& v, float* out) {
         out[0] = __uint_as_float(v.x); out[1] = __uint_as_float(v.y);
         out[2] = __uint_as_float(v.z); out[3] = __uint_as_float(v.w);
+    }
+    __device__ __forceinline__ static void unpack2(const uint4& v, u64* out) {
+        out[0] = (u64)v.x | ((u64)v.y << 32);
+        out[1] = (u64)v.z | ((u64)v.w << 32);
     }
 };
 
@@ -112,12 +145,15 @@ __device__ __forceinline__ void cc_consume(const DevPlan& P, const DevChunk& C, 
     const int rows_total = C.n_q * G;
     const int own = j >> SH;                // row whose score this lane holds
 
-    // ---- queries of this row block, channels of this lane, pre-scaled to log2 units
-    float q[RT][EPL];
+    // ---- queries of this row block, channels of this lane, pre-scaled to log2
+    // units, kept as packed pairs for the f32x2 FMA
+    constexpr int EP2 = EPL / 2;
+    u64 q2[RT][EP2];
     uint64_t own_mask = ~0ull;
 #pragma unroll
     for (int r = 0; r < RT; ++r) {
         const int row = rb * RT + r;
+        float qf[EPL];
         if (row < rows_total) {
             const int qi = row / G, gh = row % G;
             const int qid = P.chunk_q[C.q_base + qi];
@@ -126,27 +162,38 @@ __device__ __forceinline__ void cc_consume(const DevPlan& P, const DevChunk& C, 
             for (int k = 0; k < CPL; ++k) {
                 const int gc = j + k * LPT;
                 const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(qrow) + gc * 16);
-                float f[EPC];
-                ElemTraits<T>::unpack(v, f);
-#pragma unroll
-                for (int e = 0; e < EPC; ++e) q[r][k * EPC + e] = f[e] * P.scale_log2;
+                ElemTraits<T>::unpack(v, qf + k * EPC);
             }
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) qf[e] *= P.scale_log2;
             if (r == own && C.mask_base >= 0) own_mask = P.masks[C.mask_base + qi];
         } else {
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) q[r][e] = 0.f;
+            for (int e = 0; e < EPL; ++e) qf[e] = 0.f;
         }
+#pragma unroll
+        for (int e = 0; e < EP2; ++e) q2[r][e] = pk2(qf[2 * e], qf[2 * e + 1]);
     }
 
-    float o[RT][EPL];
+    u64 o2[RT][EP2];
 #pragma unroll
     for (int r = 0; r < RT; ++r)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) o[r][e] = 0.f;
+        for (int e = 0; e < EP2; ++e) o2[r][e] = 0ull;
     float m_run = -INFINITY, l_run = 0.f;
 
     const ChunkGeo g = chunk_geo(C);
     const int owner_base = grp * LPT;
+    // shared-memory byte offsets of this lane's chunks in the rows it reads
+    // (row & 7 only depends on grp and b, the tile base is 1024-aligned)
+    uint32_t off[BT][CPL];
+#pragma unroll
+    for (int b = 0; b < BT; ++b)
+#pragma unroll
+        for (int k = 0; k < CPL; ++k) {
+            const int row = warp * 16 + grp + TPI * b, gc = j + k * LPT;
+            off[b][k] = (gc / 8) * kSlabBytes + swz(row, gc % 8);
+        }
     bool ok = true;
     for (int i = 0; i < g.n_tiles; ++i) {
         const int s = i % kCcStages;
@@ -154,32 +201,36 @@ __device__ __forceinline__ void cc_consume(const DevPlan& P, const DevChunk& C, 
         const uint8_t* kb = ring_ptr + s * 2 * kHalf;
         const uint8_t* vb = kb + kHalf;
         const int tpos = g.tile0 + i * kTileTokens;
+        const bool edge = tpos < g.pos_begin || tpos + kTileTokens > g.pos_end || C.mask_base >= 0;
 
         float sc[BT];
 #pragma unroll
         for (int b = 0; b < BT; ++b) {
-            const int row = warp * 16 + grp + TPI * b;
-            float kf[EPL];
+            u64 k2[EP2];
 #pragma unroll
             for (int k = 0; k < CPL; ++k) {
-                const int gc = j + k * LPT;
-                const uint4 v = *reinterpret_cast<const uint4*>(kb + (gc / 8) * kSlabBytes + swz(row, gc % 8));
-                ElemTraits<T>::unpack(v, kf + k * EPC);
+                const uint4 v = *reinterpret_cast<const uint4*>(kb + off[b][k]);
+                ElemTraits<T>::unpack2(v, k2 + k * (EPC / 2));
             }
             float pd[RT];
 #pragma unroll
             for (int r = 0; r < RT; ++r) {
-                float acc = 0.f;
+                u64 acc = fma2(q2[r][0], k2[0], 0ull);
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) acc = fmaf(q[r][e], kf[e], acc);
-                pd[r] = acc;
+                for (int e = 1; e < EP2; ++e) acc = fma2(q2[r][e], k2[e], acc);
+                float a0, a1;
+                upk2(acc, a0, a1);
+                pd[r] = a0 + a1;
             }
             const float sv = reduce_transpose<LPT, RT>(pd, j);
-            const int pos = tpos + row;
-            const int t = pos - g.pos_begin;
-            bool valid = pos >= g.pos_begin && pos < g.pos_end;
-            if (valid && t < 64) valid = (own_mask >> t) & 1ull;
-            sc[b] = valid ? sv : -INFINITY;
+            sc[b] = sv;
+            if (edge) {
+                const int pos = tpos + warp * 16 + grp + TPI * b;
+                const int t = pos - g.pos_begin;
+                bool valid = pos >= g.pos_begin && pos < g.pos_end;
+                if (valid && t < 64) valid = (own_mask >> t) & 1ull;
+                sc[b] = valid ? sv : -INFINITY;
+            }
         }
         float mb = sc[0];
 #pragma unroll
@@ -196,34 +247,43 @@ __device__ __forceinline__ void cc_consume(const DevPlan& P, const DevChunk& C, 
 #pragma unroll
         for (int r = 0; r < RT; ++r) {
             const float ar = __shfl_sync(0xffffffffu, alpha, owner_base + (r << SH));
+            const u64 a2 = pk2(ar, ar);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) o[r][e] *= ar;
+            for (int e = 0; e < EP2; ++e) o2[r][e] = mul2(o2[r][e], a2);
         }
 #pragma unroll
         for (int b = 0; b < BT; ++b) {
-            const int row = warp * 16 + grp + TPI * b;
-            const int pos = tpos + row;
-            const bool tok_ok = pos >= g.pos_begin && pos < g.pos_end;
             float pr[RT];
 #pragma unroll
             for (int r = 0; r < RT; ++r) pr[r] = __shfl_sync(0xffffffffu, p[b], owner_base + (r << SH));
+            bool tok_ok = true;
+            if (edge) {
+                const int pos = tpos + warp * 16 + grp + TPI * b;
+                tok_ok = pos >= g.pos_begin && pos < g.pos_end;
+            }
             if (tok_ok) {
-                float vf[EPL];
+                u64 v2[EP2];
 #pragma unroll
                 for (int k = 0; k < CPL; ++k) {
-                    const int gc = j + k * LPT;
-                    const uint4 v = *reinterpret_cast<const uint4*>(vb + (gc / 8) * kSlabBytes + swz(row, gc % 8));
-                    ElemTraits<T>::unpack(v, vf + k * EPC);
+                    const uint4 v = *reinterpret_cast<const uint4*>(vb + off[b][k]);
+                    ElemTraits<T>::unpack2(v, v2 + k * (EPC / 2));
                 }
 #pragma unroll
-                for (int r = 0; r < RT; ++r)
+                for (int r = 0; r < RT; ++r) {
+                    const u64 p2 = pk2(pr[r], pr[r]);
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) o[r][e] = fmaf(pr[r], vf[e], o[r][e]);
+                    for (int e = 0; e < EP2; ++e) o2[r][e] = fma2(p2, v2[e], o2[r][e]);
+                }
             }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(bar_empty + 8 * s);
     }
+    float o[RT][EPL];
+#pragma unroll
+    for (int r = 0; r < RT; ++r)
+#pragma unroll
+        for (int e = 0; e < EP2; ++e) upk2(o2[r][e], o[r][2 * e], o[r][2 * e + 1]);
 
     // ---- merge the groups of this warp (butterfly over the group bits)
     float mr[RT], lr[RT];
@@ -304,7 +364,7 @@ pac_cc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring = smem_u32(base);
     float* scratch = reinterpret_cast<float*>(base + kCcStages * kStage);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(base + kCcStages * kStage + kCcWarps * 8 * (D + 2) * 4);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(base + kCcStages * kStage + kCcWarps * RT * (D + 2) * 4);
     const uint32_t bar_full = smem_u32(bars), bar_empty = smem_u32(bars + kCcStages);
 
     const DevItem it = P.items[item_off + blockIdx.x];
@@ -334,17 +394,17 @@ pac_cc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
     cc_consume<T, D, LPT, RT>(P, C, it.kv_head, it.row_block, Q, ring, base, bar_full, bar_empty, scratch);
 }
 
-template <typename T, int D>
+template <typename T, int D, int RT>
 size_t cc_smem_bytes() {
     constexpr int EB = ElemTraits<T>::kBytes;
     constexpr int NSLAB = D * EB / 128;
-    return 1024 + kCcStages * 2 * NSLAB * kTileTokens * 128 + kCcWarps * 8 * (D + 2) * 4 + 2 * kCcStages * 8;
+    return 1024 + kCcStages * 2 * NSLAB * kTileTokens * 128 + kCcWarps * RT * (D + 2) * 4 + 2 * kCcStages * 8;
 }
 
 template <typename T, int D, int RT>
 cudaError_t launch_cc_rt(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q,
                          int n_items, int item_off, cudaStream_t st) {
-    const size_t smem = cc_smem_bytes<T, D>();
+    const size_t smem = cc_smem_bytes<T, D, RT>();
     static bool attr_set = false;  // once per process (single device per process)
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(pac_cc_kernel<T, D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -10,12 +10,13 @@
 // visibility inside packed draft-token chunks.
 //
 // One thread block per (chunk, kv head, block of up to 256 rows), warp-
-// specialised (10 warps):
-//   warp 0      TMA producer: 64-token K/V tiles (16-row page boxes, 128B
-//               swizzle) into a 4-stage shared-memory ring;
+// specialised (11 warps):
+//   warps 0, 10 TMA producers of K and of V: 64-token tiles (16-row page
+//               boxes, 128B swizzle) into 3-stage rings; a K stage is
+//               refilled as soon as Q K^T has read it, a V stage after P V;
 //   warp 1      allocates all 512 tensor-memory columns and issues every MMA
 //               from one thread: S = Q K^T (M=128, N=64) and O += P V
-//               (M=128, N=d; P read from tensor memory, V MN-major);
+//               (M=128, N=d; P from shared memory, V MN-major);
 //   warps 2-9   two softmax warpgroups, one thread per row (tensor-memory
 //               lane). With more than 128 rows each group owns one 128-row
 //               half and both consume every tile; with at most 128 rows the
@@ -24,19 +25,20 @@
 //               way two softmax warps share each scheduler.
 // Softmax works in the log2 domain with 1/sqrt(d) folded into one FMA; the
 // running max only moves (and O is rescaled in tensor memory) when it grows
-// by more than 2^8, so the result is exact in fp32. P overwrites its S
-// columns in tensor memory as bf16 hi + lo parts (p = hi + lo to ~2^-16),
-// which keeps the PV product as accurate as an fp32 one.
+// by more than 2^8, so the result is exact in fp32. P goes to shared memory
+// as bf16 hi + lo parts (p = hi + lo to ~2^-16), which keeps the PV product
+// as accurate as an fp32 one. (Measured on GB300: with P kept in tensor
+// memory instead, the PV MMAs reading it ran at about half rate while the
+// softmax warps loaded S and stored P; from shared memory they run at full rate.)
 #include "dev_common.cuh"
 #include "umma.cuh"
 
 namespace pst {
 namespace dev {
 
-constexpr int kUWarps = 10;      // producer, MMA, 2 x 4 softmax warps
-constexpr int kUStages = 4;
+constexpr int kUWarps = 11;      // K producer, MMA, 2 x 4 softmax warps, V producer
+constexpr int kUStages = 3;
 constexpr int kUThreads = kUWarps * 32;
-constexpr int kURows = 256;      // rows per block (two 128-row MMA halves)
 constexpr float kLazyRescale = 8.f;
 
 template <int D>
@@ -48,13 +50,17 @@ struct UmmaLayout {
     static constexpr uint32_t kQSlab = 128 * 128;                 // 128 rows x 128 B
     static constexpr uint32_t kRing = kUStages * kStage;
     static constexpr uint32_t kQ = kRing;                         // Q: 2 halves x NSLAB slabs
-    static constexpr uint32_t kXchg = kQ + 2 * NSLAB * kQSlab;    // 128 x (m, l) for the split-KV merge
+    static constexpr uint32_t kP = kQ + 2 * NSLAB * kQSlab;       // P[w][hi|lo]: 128 rows x 64 tokens bf16
+    static constexpr uint32_t kPBuf = 128 * 128;
+    static constexpr uint32_t kXchg = kP + 4 * kPBuf;             // 128 x (m, l) for the split-KV merge
     static constexpr uint32_t kBars = kXchg + 128 * 8;
-    // kv_full[ST], kv_empty[ST], q_ready, s_full[2][2], p_full[2][2], o_done[2], mma_done, tmem slot
-    static constexpr int kNumBars = 2 * kUStages + 12;
+    // k_full[ST], k_empty[ST], v_full[ST], v_empty[ST], q_ready, s_full[2][2], p_full[2][2],
+    // o_done[2], mma_done, tmem slot
+    static constexpr int kNumBars = 4 * kUStages + 12;
     static constexpr uint32_t kBytes = kBars + 8 * kNumBars + 16;
+    static_assert(kBytes + 1024 <= 232448, "shared memory");
     static constexpr uint32_t kTmemCols = 512;
-    // tensor-memory columns: S[w][b] at 128w + 64b (P hi/lo alias its first/second 32), O[w] at 256 + D*w
+    // tensor-memory columns: S[w][b] at 128w + 64b, O[w] at 256 + D*w
     __device__ static constexpr uint32_t colS(int w, int b) { return 128 * w + 64 * b; }
     __device__ static constexpr uint32_t colO(int w) { return 256 + D * w; }
 };
@@ -62,17 +68,6 @@ struct UmmaLayout {
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 
 template <int D>
@@ -84,10 +79,13 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(base);
-    const uint32_t ring = sbase, sQ = sbase + L::kQ;
+    const uint32_t ring = sbase, sQ = sbase + L::kQ, sP = sbase + L::kP;
     const uint32_t bars = sbase + L::kBars;
-    const uint32_t kv_full = bars, kv_empty = bars + 8 * kUStages;
-    const uint32_t q_ready = bars + 16 * kUStages;
+    // K and V stages have separate barriers: a K stage is refilled once Q K^T
+    // has read it, a V stage once P V has.
+    const uint32_t k_full = bars, k_empty = bars + 8 * kUStages;
+    const uint32_t v_full = bars + 16 * kUStages, v_empty = bars + 24 * kUStages;
+    const uint32_t q_ready = bars + 32 * kUStages;
     // One p_full per S buffer: a group can then never complete two phases of
     // the same barrier before the MMA warp has waited for the first.
     const uint32_t s_full = q_ready + 8;      // [w][b] at s_full + 8*(2w+b)
@@ -103,14 +101,16 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int G = P.group, Hq = P.n_q_heads;
     const int rows_total = C.n_q * G;
-    const int row0 = rb * kURows;
-    const int rows_here = min(kURows, rows_total - row0);
+    const int row0 = rb * C.r_tile;                 // C.r_tile: 256 or 128 rows per block
+    const int rows_here = min(C.r_tile, rows_total - row0);
     const bool split_rows = rows_here > 128;   // mode A: groups own row halves; else alternate tiles
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kUStages; ++s) {
-            mbar_init(kv_full + 8 * s, 1);
-            mbar_init(kv_empty + 8 * s, 1);
+            mbar_init(k_full + 8 * s, 1);
+            mbar_init(k_empty + 8 * s, 1);
+            mbar_init(v_full + 8 * s, 1);
+            mbar_init(v_empty + 8 * s, 1);
         }
         mbar_init(q_ready, 256);
         for (int i = 0; i < 4; ++i) {
@@ -135,12 +135,15 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     auto n_steps = [&](int w) { return split_rows ? n : (n - w + 1) / 2; };
     auto tile_of = [&](int w, int k) { return split_rows ? k : 2 * k + w; };
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == 0 || warp == kUWarps - 1) {
+        // ------------------------------------------------------------ TMA producers
+        // warp 0 streams K, the last warp streams V, each at its own pace (two
+        // lanes of one warp would reconverge and tie the two streams together)
         if (lane == 0) {
-            prefetch_tmap(&tk);
-            prefetch_tmap(&tv);
-            produce_chunk<NSLAB, kUStages, 64>(P, C, head, ring, kv_full, kv_empty, &tk, &tv);
+            const bool vee = warp != 0;
+            prefetch_tmap(vee ? &tv : &tk);
+            produce_operand<NSLAB, kUStages, 64>(P, C, head, ring, L::kStage, vee ? v_full : k_full,
+                                                 vee ? v_empty : k_empty, vee ? &tv : &tk, vee);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
@@ -157,6 +160,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                                          umma::smem_desc_sw128(sQ + NSLAB * L::kQSlab, 16, 1024)};
             const uint64_t dk_base = umma::smem_desc_sw128(ring, 16, 1024);
             const uint64_t dv_base = umma::smem_desc_sw128(ring + L::kHalf, L::kSlab, 1024);
+            const uint64_t dp_base = umma::smem_desc_sw128(sP, 16, 1024);
             auto issue_s = [&](int w, int k, int j) {
                 const uint64_t dq = dq_base[split_rows ? w : 0];
                 const uint64_t dk = dk_base + (uint64_t)(((j % kUStages) * L::kStage) >> 4);
@@ -170,41 +174,42 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             // PV of step k of group w (tile j): O[w] += P_hi V + P_lo V
             auto issue_pv = [&](int w, int k, int j) -> bool {
                 if (!mbar_wait(p_full + 8 * (2 * w + (k & 1)), (k >> 1) & 1, P.status)) return false;
+                if (!mbar_wait(v_full + 8 * (j % kUStages), (j / kUStages) & 1, P.status)) return false;
                 umma::fence_after_sync();
                 const uint64_t dv = dv_base + (uint64_t)(((j % kUStages) * L::kStage) >> 4);
-                const uint32_t ps = tmem + L::colS(w, k & 1);
+                const uint64_t dh = dp_base + (uint64_t)((2 * w * L::kPBuf) >> 4);
+                const uint64_t dl = dh + (uint64_t)(L::kPBuf >> 4);
                 const uint32_t dst = tmem + L::colO(w);
                 const uint32_t acc0 = k > 0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < kTileTokens / 16; ++kk) {
-                    mma_bf16_ts(dst, ps + 8 * kk, dv + ((kk * 2048) >> 4), idO, kk > 0 ? 1u : acc0);
-                    mma_bf16_ts(dst, ps + 32 + 8 * kk, dv + ((kk * 2048) >> 4), idO, 1u);
+                    umma::mma_bf16_ss(dst, dh + ((kk * 32) >> 4), dv + ((kk * 2048) >> 4), idO, kk > 0 ? 1u : acc0);
+                    umma::mma_bf16_ss(dst, dl + ((kk * 32) >> 4), dv + ((kk * 2048) >> 4), idO, 1u);
                 }
                 umma::commit(o_done + 8 * w);
                 return true;
             };
             for (int j = 0; j < n && ok; ++j) {
                 const int s = j % kUStages;
-                if (!mbar_wait(kv_full + 8 * s, (j / kUStages) & 1, P.status)) { ok = false; break; }
+                if (!mbar_wait(k_full + 8 * s, (j / kUStages) & 1, P.status)) { ok = false; break; }
                 if (split_rows) {
                     issue_s(0, j, j);
                     issue_s(1, j, j);
-                    if (j >= 1) {
-                        if (!issue_pv(0, j - 1, j - 1) || !issue_pv(1, j - 1, j - 1)) { ok = false; break; }
-                        umma::commit(kv_empty + 8 * ((j - 1) % kUStages));
-                    }
                 } else {
                     issue_s(j & 1, j >> 1, j);
-                    if (j >= 1) {
-                        if (!issue_pv((j - 1) & 1, (j - 1) >> 1, j - 1)) { ok = false; break; }
-                        umma::commit(kv_empty + 8 * ((j - 1) % kUStages));
-                    }
+                }
+                umma::commit(k_empty + 8 * s);     // K stage free once these S MMAs complete
+                if (j >= 1) {
+                    const bool good = split_rows ? (issue_pv(0, j - 1, j - 1) && issue_pv(1, j - 1, j - 1))
+                                                 : issue_pv((j - 1) & 1, (j - 1) >> 1, j - 1);
+                    if (!good) { ok = false; break; }
+                    umma::commit(v_empty + 8 * ((j - 1) % kUStages));
                 }
             }
             if (ok && n >= 1) {
                 const int j = n - 1;
                 bool good = split_rows ? (issue_pv(0, j, j) && issue_pv(1, j, j)) : issue_pv(j & 1, j >> 1, j);
-                if (good) umma::commit(kv_empty + 8 * (j % kUStages));
+                if (good) umma::commit(v_empty + 8 * (j % kUStages));
             }
             // every MMA issued above has finished before tensor memory is released
             umma::commit(mma_done);
@@ -280,8 +285,6 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
 #pragma unroll
                 for (int c = 0; c < kTileTokens; ++c) mx = fmaxf(mx, x[c]);
             }
-            // P_k overwrites the S columns of step k-2, whose PV finished before
-            // S_k (issued later on the same in-order tensor pipe) completed.
             const float mxs = mx * sl;   // scale > 0: max commutes with it
             const bool grow = (m_ref == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref + kLazyRescale);
             bool rescaled = false;
@@ -289,8 +292,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 const float alpha = fast_exp2(m_ref - mxs);   // 0 when nothing was accumulated
                 if (k >= 1 && m_ref != -INFINITY) {
                     // O is about to be rescaled: the previous PV of this group must be
-                    // done. When S_k has completed, every PV before step k-1 has too,
-                    // so o_done is at most one phase behind and the parity wait is exact.
+                    // done (waited for just below in any case).
                     if (!mbar_wait(o_done + 8 * w, (k - 1) & 1, P.status)) { ok = false; break; }
                     umma::fence_after_sync();
 #pragma unroll 1
@@ -308,7 +310,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 m_ref = mxs;
             }
             const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
-            float hi[32], lo[32];
+            uint32_t hi[32], lo[32];
             float sum = 0.f;
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
@@ -316,18 +318,35 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 const float bb = fast_exp2(fmaf(x[2 * c + 1], sl, nmu));
                 sum += a + bb;
                 const uint32_t h = bf16x2_bits(a, bb);
-                hi[c] = __uint_as_float(h);
-                lo[c] = __uint_as_float(bf16x2_bits(a - __uint_as_float(h << 16), bb - __uint_as_float(h & 0xffff0000u)));
+                hi[c] = h;
+                lo[c] = bf16x2_bits(a - __uint_as_float(h << 16), bb - __uint_as_float(h & 0xffff0000u));
             }
             l += sum;
-            umma::st32(lane_addr + L::colS(w, b), hi);
-            umma::st32(lane_addr + L::colS(w, b) + 32, lo);
+            // P's shared-memory buffer is reused every step: the previous PV of
+            // this group must have read it. When S_k has completed, every PV
+            // before step k-1 has too, so o_done is at most one phase behind and
+            // the parity wait is exact.
+            if (k >= 1 && !rescaled) {
+                if (!mbar_wait(o_done + 8 * w, (k - 1) & 1, P.status)) { ok = false; break; }
+            }
+            {
+                // row r of P (64 tokens = 128 bytes), K-major with the 128B swizzle
+                uint8_t* ph = base + L::kP + 2 * w * L::kPBuf;
+                uint8_t* pl = ph + L::kPBuf;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    *reinterpret_cast<uint4*>(ph + swz(r, ch)) =
+                        make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
+                    *reinterpret_cast<uint4*>(pl + swz(r, ch)) =
+                        make_uint4(lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
+                }
+            }
             bool zeroed = false;
             if (edge && zero_v) {
                 // V rows outside the chunk may hold stale or non-finite values:
                 // zero them before the PV of this tile multiplies them by P = 0.
                 const int s = j % kUStages;
-                if (!mbar_wait(kv_full + 8 * s, (j / kUStages) & 1, P.status)) { ok = false; break; }
+                if (!mbar_wait(v_full + 8 * s, (j / kUStages) & 1, P.status)) { ok = false; break; }
                 if (r < kTileTokens * NSLAB) {          // one 128-byte slab row per thread
                     const int t = r % kTileTokens, sl_i = r / kTileTokens;
                     const int pos = tpos + t;
@@ -339,9 +358,9 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                     }
                 }
             }
-            umma::wait_st();
-            (void)rescaled;
-            if (zeroed) fence_proxy_async_smem();
+            if (rescaled) umma::wait_st();
+            (void)zeroed;
+            fence_proxy_async_smem();   // P (and zeroed V rows) are read by the tensor core
             umma::fence_before_sync();
             mbar_arrive(p_full + 8 * (2 * w + b));
         }

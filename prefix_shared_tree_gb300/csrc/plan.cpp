@@ -149,6 +149,7 @@ extern "C" void pst_plan_opts_default(pst_plan_opts* o) {
     o->num_sms = 0;
     o->slots_per_sm = 1;
     o->tc_engine = 0;
+    o->tc_block_rows = 256;
 }
 
 namespace {
@@ -227,7 +228,7 @@ struct Planner {
     }
 
     int rows_per_block(const Task& t) const {
-        return t.kind == 1 ? tc_rows_per_block(P.opts.tc_engine) : cc_row_tile(t.rows);
+        return t.kind == 1 ? tc_rows_per_block(P.opts) : cc_row_tile(t.rows);
     }
 
     // per-item cost and item count of task t split b ways
@@ -412,6 +413,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     if (opts) o = *opts;
     if (o.tc_min_rows <= 0) o.tc_min_rows = 16;
     if (o.slots_per_sm <= 0) o.slots_per_sm = 1;
+    if (o.tc_block_rows != 128) o.tc_block_rows = 256;
     if (o.split_policy == PST_SPLIT_UNIFORM && (o.fixed_chunk <= 0 || o.fixed_chunk % kTileTokens))
         return fail(PST_EINVAL, "plan_create: fixed_chunk must be a positive multiple of 64");
 
@@ -591,7 +593,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
                 c.dev.q_base = (int32_t)P->chunk_q.size();
                 c.dev.n_q = t.n_q;
                 c.dev.mask_base = -1;
-                c.dev.r_tile = t.kind == 1 ? tc_rows_per_block(o.tc_engine) : cc_row_tile(t.rows);
+                c.dev.r_tile = t.kind == 1 ? tc_rows_per_block(o) : cc_row_tile(t.rows);
                 P->chunk_q.insert(P->chunk_q.end(), P->nodeq.begin() + P->nodeq_ptr[t.node],
                                   P->nodeq.begin() + P->nodeq_ptr[t.node + 1]);
                 P->chunks.push_back(c);
@@ -611,7 +613,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
             c.dev.q_base = (int32_t)P->chunk_q.size();
             c.dev.n_q = t.n_q;
             c.dev.mask_base = (int32_t)P->masks.size();
-            c.dev.r_tile = t.kind == 1 ? tc_rows_per_block(o.tc_engine) : cc_row_tile(t.rows);
+            c.dev.r_tile = t.kind == 1 ? tc_rows_per_block(o) : cc_row_tile(t.rows);
             P->chunk_q.insert(P->chunk_q.end(), g.queries.begin(), g.queries.end());
             P->masks.insert(P->masks.end(), g.mask.begin(), g.mask.end());
             P->chunks.push_back(c);

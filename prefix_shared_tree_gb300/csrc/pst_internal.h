@@ -14,7 +14,9 @@ namespace pst {
 // (8 warps x 16 rows), 256 for the tcgen05 kernel (two M=128 halves).
 constexpr int kTcRowsPerBlock = 128;
 constexpr int kUmmaRowsPerBlock = 256;
-inline int tc_rows_per_block(int tc_engine) { return tc_engine == 1 ? kTcRowsPerBlock : kUmmaRowsPerBlock; }
+inline int tc_rows_per_block(const pst_plan_opts& o) {
+    return o.tc_engine == 1 ? kTcRowsPerBlock : (o.tc_block_rows == 128 ? 128 : kUmmaRowsPerBlock);
+}
 // Rows of the CUDA-core PAC per thread block (largest row tile).
 constexpr int kCcRowsPerBlock = 8;
 // KV tokens per pipeline stage of both PAC kernels (4 boxes of 16 rows).

@@ -33,7 +33,7 @@ class PstError(RuntimeError):
 class PlanOpts(C.Structure):
     _fields_ = [("split_policy", C.c_int32), ("fixed_chunk", C.c_int32), ("tc_min_rows", C.c_int32),
                 ("pack_masks", C.c_int32), ("num_sms", C.c_int32), ("slots_per_sm", C.c_int32),
-                ("tc_engine", C.c_int32)]
+                ("tc_engine", C.c_int32), ("tc_block_rows", C.c_int32)]
 
 
 class PlanStats(C.Structure):
@@ -206,7 +206,7 @@ class Plan:
 def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int, dtype: str = "bf16",
                 split_policy: str = "cost_model", fixed_chunk: int | None = None,
                 tc_min_rows: int | None = None, pack_masks: bool | None = None, num_sms: int = 0,
-                slots_per_sm: int = 0, tc_engine: str = "tcgen05") -> Plan:
+                slots_per_sm: int = 0, tc_engine: str = "tcgen05", tc_block_rows: int = 256) -> Plan:
     o = plan_opts_default()
     o.split_policy = SPLIT[split_policy]
     if fixed_chunk is not None:
@@ -218,6 +218,7 @@ def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int,
     o.num_sms = num_sms
     o.slots_per_sm = slots_per_sm
     o.tc_engine = {"tcgen05": 0, "mma_sync": 1}[tc_engine]
+    o.tc_block_rows = tc_block_rows
     qn, qnp = _arr(query_node, np.int32)
     h = C.c_void_p()
     _check(lib().pst_plan_create(tree._h, len(qn), qnp, n_q_heads, n_kv_heads, d, DTYPES[dtype],
