@@ -307,11 +307,18 @@ def run_ours(args, rank, world):
     per_tok = wl.n_kv_heads * 2 * wl.d * wl.elem_bytes
     ntok = np.diff(ex["chunk_tok_ptr"])
     kinds = ex["chunk_kind"]
-    alg = {"pac_tc": int(ntok[kinds == 1].sum()) * per_tok, "pac_cc": int(ntok[kinds == 0].sum()) * per_tok,
+    # tensor-core chunks shorter than p_bf16_min_tokens run in the exact-P launch (tcgen05 engine)
+    thr = int(plan_opts.get("p_bf16_min_tokens", 0)) or 1024
+    thr = np.inf if thr < 0 else thr
+    exact = (kinds == 1) & (ntok < thr) & (plan_opts.get("tc_engine", "tcgen05") == "tcgen05")
+    alg = {"pac_tc": int(ntok[(kinds == 1) & ~exact].sum()) * per_tok,
+           "pac_tc_exact": int(ntok[exact].sum()) * per_tok,
+           "pac_cc": int(ntok[kinds == 0].sum()) * per_tok,
            "por": int(st["n_partial_rows"]) * (wl.d * 4 + 4) + wl.n_queries * wl.n_q_heads * (wl.d * 4 + 4)}
-    launches = {"pac_tc": 1 if st["n_tc_items"] else 0, "pac_cc": max(0, st["n_launches"] - 1 - (1 if st["n_tc_items"] else 0)), "por": 1}
     shares = {k: v / max(1e-9, sum(kern_ms.values())) for k, v in kern_ms.items()}
-    dom = max((k for k in ("pac_tc", "pac_cc") if launches[k]), key=lambda k: kern_ms[k])
+    # the PAC launch groups start together; each group's time runs from the
+    # call's start to its end. The dominant kernel is the one with the most bytes.
+    dom = max(("pac_tc", "pac_tc_exact", "pac_cc"), key=lambda k: alg[k])
     dom_ms = kern_ms[dom] / max(1, kern_calls)
     dom_achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
     traffic = recorded_traffic(dom, args.workload)

@@ -71,6 +71,11 @@ typedef struct {
                                1 legacy mma.sync (kept for comparison)               */
     int32_t tc_block_rows;  /* tcgen05 PAC rows per thread block: 256 (default; two
                                128-row halves share each K/V tile) or 128            */
+    int32_t p_bf16_min_tokens; /* tcgen05 PAC: chunks of at least this many tokens
+                               multiply V by the softmax weights P rounded once to
+                               bf16; shorter chunks split P into bf16 hi + lo parts,
+                               which keeps P V as accurate as an fp32 product.
+                               0: default (1024); -1: always split               */
 } pst_plan_opts;
 
 /* Fill `o` with the defaults above. */
@@ -170,10 +175,18 @@ int pst_plan_check_status(const pst_plan* p, void* stream, int32_t* code);
 /* ---------------------------------------------------------------- timing
  * Per-kernel device times of pst_decode_attn, for roofline accounting. A timer
  * holds CUDA events for up to `max_calls` calls; pst_decode_attn_timed records
- * an event before the first kernel and after each kernel on `stream`.
+ * an event at the start of the call, after each PAC launch group (on the
+ * stream that ran it) and around POR. Slots (pst_timer_kernel_name):
+ *   0 "pac_tc"        tensor-core PAC that rounds P once to bf16 (every
+ *                     tensor-core item of the mma.sync engine)
+ *   1 "pac_tc_exact"  tensor-core PAC with P split into bf16 hi + lo
+ *   2 "pac_cc"        CUDA-core PAC (all row-tile launches)
+ *   3 "por"           partial-output reduction
+ * The PAC groups run side by side on forked streams, so slots 0-2 give the
+ * time from the call's start to the end of that group; slot 3 is POR alone.
  * pst_timer_read synchronises on the last event, writes the summed
- * milliseconds per kernel slot into ms[0..n-1], the number of timed calls into
- * *calls, and resets the timer. Kernel slot names: pst_timer_kernel_name(). */
+ * milliseconds per slot into ms[0..n-1], the number of timed calls into
+ * *calls, and resets the timer. */
 int pst_timer_create(int32_t max_calls, pst_timer** out);
 void pst_timer_destroy(pst_timer* t);
 int pst_decode_attn_timed(const pst_plan* p, const void* Q, const void* K_pool,

@@ -13,6 +13,7 @@
 #include <cudaTypedefs.h>
 
 #include <chrono>
+#include <cstdint>
 #include <cmath>
 #include <mutex>
 #include <new>
@@ -28,7 +29,30 @@ cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const 
 cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
                           int item_off, cudaStream_t st);
 cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
-                            int item_off, cudaStream_t st);
+                            int item_off, bool exact_p, cudaStream_t st);
+
+// Tensor-core PAC items of one launch group: those that round P once to bf16
+// (`exact` false; every item of the mma.sync engine) or the exact-P ones.
+cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
+                            bool exact, cudaStream_t st) {
+    const int64_t n_fast = p->n_tc_items - p->n_tc_exact;
+    const int n = (int)(exact ? p->n_tc_exact : n_fast);
+    const int off = exact ? (int)n_fast : 0;
+    if (n == 0) return cudaSuccess;
+    if (p->opts.tc_engine == 1) return launch_pac_tc(dp, tk, tv, Q, n, off, st);
+    return launch_pac_umma(dp, tk, tv, Q, n, off, exact, st);
+}
+
+cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
+                            cudaStream_t st) {
+    for (int k = 0; k < 4; ++k) {
+        if (p->cc_class_cnt[k] == 0) continue;
+        cudaError_t e = launch_pac_cc(dp, p->dtype, tk, tv, Q, 8 >> k, (int)p->cc_class_cnt[k],
+                                      (int)p->cc_class_off[k], st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
 
 namespace dev {
 
@@ -145,29 +169,6 @@ static int make_pool_map(const pst_plan* p, const void* pool, unsigned char* out
     return PST_OK;
 }
 
-static DevPlan dev_plan(const pst_plan* p) {
-    uint8_t* b = static_cast<uint8_t*>(p->d_ws);
-    DevPlan d;
-    d.items = reinterpret_cast<const DevItem*>(b + p->ws.items);
-    d.chunks = reinterpret_cast<const DevChunk*>(b + p->ws.chunks);
-    d.pages = reinterpret_cast<const int32_t*>(b + p->ws.pages);
-    d.chunk_q = reinterpret_cast<const int32_t*>(b + p->ws.chunk_q);
-    d.masks = reinterpret_cast<const uint64_t*>(b + p->ws.masks);
-    d.merge_ptr = reinterpret_cast<const int32_t*>(b + p->ws.merge_ptr);
-    d.merge_row = reinterpret_cast<const int32_t*>(b + p->ws.merge_row);
-    d.part_o = reinterpret_cast<float*>(b + p->ws.part_o);
-    d.part_lse = reinterpret_cast<float*>(b + p->ws.part_lse);
-    d.status = reinterpret_cast<int32_t*>(b + p->ws.status);
-    d.n_queries = p->n_queries;
-    d.n_q_heads = p->hq;
-    d.n_kv_heads = p->hkv;
-    d.group = p->group;
-    d.d = p->d;
-    d.page_size = p->page_size;
-    d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->d));
-    return d;
-}
-
 // For entry points that run a plan out of device memory other than its bound
 // workspace (same layout, base `ws`).
 int encode_pool_map(const pst_plan* p, const void* pool, unsigned char* out) { return make_pool_map(p, pool, out); }
@@ -192,8 +193,11 @@ DevPlan dev_plan_at(const pst_plan* p, void* ws) {
     d.d = p->d;
     d.page_size = p->page_size;
     d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->d));
+    d.p_bf16_min_tokens = p->opts.p_bf16_min_tokens < 0 ? INT32_MAX : p->opts.p_bf16_min_tokens;
     return d;
 }
+
+static DevPlan dev_plan(const pst_plan* p) { return dev_plan_at(p, p->d_ws); }
 
 cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, cudaStream_t st) {
     const int64_t warps = (int64_t)dp.n_queries * dp.n_q_heads;
@@ -205,13 +209,16 @@ cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, cudaStream_t st)
 
 }  // namespace pst
 
+// Per recorded call, events: [0] start, [1] end of the tensor-core PAC,
+// [2] end of the exact-P tensor-core PAC, [3] end of the CUDA-core PAC (each on
+// the stream that ran it), [4] POR start (after the join), [5] POR end. The PAC
+// slots report time from the call's start to the end of their group (the
+// groups run side by side); the POR slot reports POR alone.
 struct pst_timer {
     int32_t max_calls = 0;
     int32_t calls = 0;
-    int32_t n_slots = 0;                 // kernels per call in the recorded calls
-    int32_t forked = 0;                  // the CUDA-core PAC ran beside the tensor-core PAC
-    std::vector<cudaEvent_t> ev;         // max_calls x (1 + kMaxKernels)
-    static constexpr int kMaxKernels = 4;
+    std::vector<cudaEvent_t> ev;         // max_calls x kEvents
+    static constexpr int kEvents = 6;
 };
 
 using namespace pst;
@@ -256,64 +263,62 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
     cudaEvent_t* ev = nullptr;
     if (timer) {
         if (timer->calls >= timer->max_calls) return fail(PST_EINVAL, "decode_attn_timed: timer is full");
-        ev = timer->ev.data() + (size_t)timer->calls * (1 + pst_timer::kMaxKernels);
+        ev = timer->ev.data() + (size_t)timer->calls * pst_timer::kEvents;
         cudaEventRecord(ev[0], st);
     }
     cudaError_t e;
-    // Both PAC kernels write disjoint partial rows; when a plan has both
-    // kinds, the CUDA-core PAC runs on a side stream forked from `st` so its
-    // blocks fill the SMs the tensor-core blocks leave idle, and POR waits on
-    // the join. Timer events: [0] start, [1] after the tensor-core PAC (st),
-    // [2] after the CUDA-core PAC (its stream), [3] after POR (st).
-    const bool fork = p->n_tc_items > 0 && p->n_cc_items > 0;
-    cudaStream_t cc_st = st;
-    if (fork) {
-        if (!p->side_stream) {
+    // The three PAC launch groups write disjoint partial rows. The first
+    // non-empty one runs on `st`, the others on side streams forked from it,
+    // so their blocks fill the SMs the first group's blocks leave idle; POR
+    // waits on the joins.
+    const bool has[3] = {p->n_tc_items - p->n_tc_exact > 0, p->n_tc_exact > 0, p->n_cc_items > 0};
+    cudaStream_t gst[3] = {st, st, st};
+    int n_side = 0;
+    bool first = true;
+    for (int g = 0; g < 3; ++g) {
+        if (!has[g]) continue;
+        if (first) { first = false; continue; }
+        if (!p->side_stream[n_side]) {
             cudaStream_t s2;
-            cudaEvent_t a, b;
+            cudaEvent_t j;
             if ((e = cudaStreamCreateWithFlags(&s2, cudaStreamNonBlocking)) != cudaSuccess)
                 return cuda_fail("decode_attn: side stream", e);
-            if ((e = cudaEventCreateWithFlags(&a, cudaEventDisableTiming)) != cudaSuccess ||
-                (e = cudaEventCreateWithFlags(&b, cudaEventDisableTiming)) != cudaSuccess)
-                return cuda_fail("decode_attn: fork/join events", e);
-            p->side_stream = s2;
-            p->ev_fork = a;
-            p->ev_join = b;
+            if ((e = cudaEventCreateWithFlags(&j, cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail("decode_attn: join event", e);
+            p->side_stream[n_side] = s2;
+            p->ev_join[n_side] = j;
         }
-        cc_st = static_cast<cudaStream_t>(p->side_stream);
+        if (!p->ev_fork) {
+            cudaEvent_t f;
+            if ((e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail("decode_attn: fork event", e);
+            p->ev_fork = f;
+        }
+        gst[g] = static_cast<cudaStream_t>(p->side_stream[n_side++]);
+    }
+    if (n_side > 0) {
         cudaEventRecord(static_cast<cudaEvent_t>(p->ev_fork), st);
-        cudaStreamWaitEvent(cc_st, static_cast<cudaEvent_t>(p->ev_fork), 0);
+        for (int k = 0; k < n_side; ++k)
+            cudaStreamWaitEvent(static_cast<cudaStream_t>(p->side_stream[k]), static_cast<cudaEvent_t>(p->ev_fork), 0);
     }
-    if (p->n_tc_items > 0) {
-        e = p->opts.tc_engine == 1 ? launch_pac_tc(dp, p->tmap_k, p->tmap_v, Q, (int)p->n_tc_items, 0, st)
-                                   : launch_pac_umma(dp, p->tmap_k, p->tmap_v, Q, (int)p->n_tc_items, 0, st);
-        if (e != cudaSuccess) return cuda_fail("decode_attn: PAC (tensor core) launch", e);
+    for (int g = 0; g < 3; ++g) {
+        if (has[g]) {
+            e = g < 2 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g == 1, gst[g])
+                      : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, gst[g]);
+            if (e != cudaSuccess) return cuda_fail(g < 2 ? "decode_attn: PAC (tensor core) launch"
+                                                         : "decode_attn: PAC (CUDA core) launch", e);
+        }
+        if (ev) cudaEventRecord(ev[1 + g], gst[g]);
     }
-    if (ev) cudaEventRecord(ev[1], st);
-    for (int k = 0; k < 4; ++k) {
-        if (p->cc_class_cnt[k] == 0) continue;
-        e = launch_pac_cc(dp, p->dtype, p->tmap_k, p->tmap_v, Q, 8 >> k, (int)p->cc_class_cnt[k],
-                          (int)p->cc_class_off[k], cc_st);
-        if (e != cudaSuccess) return cuda_fail("decode_attn: PAC (CUDA core) launch", e);
+    for (int k = 0; k < n_side; ++k) {
+        cudaEventRecord(static_cast<cudaEvent_t>(p->ev_join[k]), static_cast<cudaStream_t>(p->side_stream[k]));
+        cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(p->ev_join[k]), 0);
     }
-    if (ev) cudaEventRecord(ev[2], cc_st);
-    if (fork) {
-        cudaEventRecord(static_cast<cudaEvent_t>(p->ev_join), cc_st);
-        cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(p->ev_join), 0);
-    }
-    int slot = 2;
-    {
-        const int64_t warps = (int64_t)p->n_queries * p->hq;
-        const int blocks = (int)((warps + dev::kPorWarps - 1) / dev::kPorWarps);
-        if (p->d == 128) dev::por_kernel<128><<<blocks, dev::kPorWarps * 32, 0, st>>>(dp, O, LSE);
-        else dev::por_kernel<64><<<blocks, dev::kPorWarps * 32, 0, st>>>(dp, O, LSE);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return cuda_fail("decode_attn: POR launch", e);
-    }
+    if (ev) cudaEventRecord(ev[4], st);
+    e = launch_por(dp, O, LSE, st);
+    if (e != cudaSuccess) return cuda_fail("decode_attn: POR launch", e);
     if (ev) {
-        cudaEventRecord(ev[++slot], st);
-        timer->n_slots = slot;
-        timer->forked = fork ? 1 : 0;
+        cudaEventRecord(ev[5], st);
         timer->calls++;
     }
     return PST_OK;
@@ -321,10 +326,13 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
 
 namespace pst {
 void release_plan_streams(pst_plan* p) {
-    if (p->side_stream) cudaStreamDestroy(static_cast<cudaStream_t>(p->side_stream));
+    for (int k = 0; k < 2; ++k) {
+        if (p->side_stream[k]) cudaStreamDestroy(static_cast<cudaStream_t>(p->side_stream[k]));
+        if (p->ev_join[k]) cudaEventDestroy(static_cast<cudaEvent_t>(p->ev_join[k]));
+        p->side_stream[k] = p->ev_join[k] = nullptr;
+    }
     if (p->ev_fork) cudaEventDestroy(static_cast<cudaEvent_t>(p->ev_fork));
-    if (p->ev_join) cudaEventDestroy(static_cast<cudaEvent_t>(p->ev_join));
-    p->side_stream = p->ev_fork = p->ev_join = nullptr;
+    p->ev_fork = nullptr;
 }
 }  // namespace pst
 
@@ -358,7 +366,7 @@ extern "C" int pst_timer_create(int32_t max_calls, pst_timer** out) {
     pst_timer* t = new (std::nothrow) pst_timer();
     if (!t) return fail(PST_ENOMEM, "timer_create: out of memory");
     t->max_calls = max_calls;
-    t->ev.resize((size_t)max_calls * (1 + pst_timer::kMaxKernels), nullptr);
+    t->ev.resize((size_t)max_calls * pst_timer::kEvents, nullptr);
     for (auto& e : t->ev) {
         cudaError_t r = cudaEventCreate(&e);
         if (r != cudaSuccess) {
@@ -380,17 +388,17 @@ extern "C" void pst_timer_destroy(pst_timer* t) {
 extern "C" int pst_timer_read(pst_timer* t, float* ms, int32_t n, int32_t* calls) {
     if (!t) return fail(PST_EINVAL, "timer_read: timer is null");
     for (int k = 0; k < n; ++k) ms[k] = 0.f;
-    const int stride = 1 + pst_timer::kMaxKernels;
+    const int stride = pst_timer::kEvents;
     if (t->calls > 0) {
-        cudaError_t e = cudaEventSynchronize(t->ev[(size_t)(t->calls - 1) * stride + t->n_slots]);
+        cudaError_t e = cudaEventSynchronize(t->ev[(size_t)(t->calls - 1) * stride + stride - 1]);
         if (e != cudaSuccess) return cuda_fail("timer_read: cudaEventSynchronize", e);
     }
+    // slot k: (from, to) events
+    static const int from[4] = {0, 0, 0, 4}, to[4] = {1, 2, 3, 5};
     for (int c = 0; c < t->calls; ++c) {
-        for (int k = 0; k < t->n_slots && k < n; ++k) {
+        for (int k = 0; k < 4 && k < n; ++k) {
             float x = 0.f;
-            // a forked CUDA-core PAC starts with the call, not after the tensor-core PAC
-            const int from = (k == 1 && t->forked) ? 0 : k;
-            cudaError_t e = cudaEventElapsedTime(&x, t->ev[(size_t)c * stride + from], t->ev[(size_t)c * stride + k + 1]);
+            cudaError_t e = cudaEventElapsedTime(&x, t->ev[(size_t)c * stride + from[k]], t->ev[(size_t)c * stride + to[k]]);
             if (e != cudaSuccess) return cuda_fail("timer_read: cudaEventElapsedTime", e);
             ms[k] += x;
         }
@@ -403,8 +411,9 @@ extern "C" int pst_timer_read(pst_timer* t, float* ms, int32_t n, int32_t* calls
 extern "C" const char* pst_timer_kernel_name(int32_t slot) {
     switch (slot) {
         case 0: return "pac_tc";
-        case 1: return "pac_cc";
-        case 2: return "por";
+        case 1: return "pac_tc_exact";
+        case 2: return "pac_cc";
+        case 3: return "por";
         default: return "";
     }
 }

@@ -51,6 +51,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the hardware may suspend the thread (without taking
+// issue slots from the warps that do work) until the phase completes or about
+// `ns` nanoseconds have passed.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(ns)
+        : "memory");
+    return ok != 0;
+}
+
 // A wait gives up after this many SM cycles (about two seconds), sets the
 // status word and lets the caller leave the kernel.
 constexpr long long kWaitCycles = 4000000000LL;
@@ -60,8 +75,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t
     const long long t0 = clock64();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 16; ++i)
+            if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
         if (clock64() - t0 > kWaitCycles) {
             atomicOr(status, kStatusWaitTimeout);
             return false;
@@ -93,6 +108,13 @@ __device__ __forceinline__ uint32_t swz(int row, int c) {
 __device__ __forceinline__ float bf16lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
+// max(a, b, c) in one instruction (sm_100 family)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -100,17 +122,18 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // Chunk geometry in page space: the chunk covers positions
-// [pos_begin, pos_end); tiles of kTileTokens start at multiples of the tile.
+// [pos_begin, pos_end); tiles of TT tokens start at multiples of TT.
 struct ChunkGeo {
     int pos_begin, pos_end, tile0, n_tiles;
 };
 
+template <int TT = kTileTokens>
 __device__ __forceinline__ ChunkGeo chunk_geo(const DevChunk& c) {
     ChunkGeo g;
     g.pos_begin = c.pos_begin;
     g.pos_end = c.pos_begin + c.n_tok;
-    g.tile0 = (c.pos_begin / kTileTokens) * kTileTokens;
-    g.n_tiles = (g.pos_end - g.tile0 + kTileTokens - 1) / kTileTokens;
+    g.tile0 = (c.pos_begin / TT) * TT;
+    g.n_tiles = (g.pos_end - g.tile0 + TT - 1) / TT;
     return g;
 }
 
@@ -161,16 +184,16 @@ __device__ void produce_chunk(const DevPlan& P, const DevChunk& C, int head, uin
     }
 }
 
-// TMA producer for one operand (K when `vee` is false, V when true) with its
-// own full/empty barriers, so K stages can be refilled as soon as Q K^T has
-// read them while V stages wait for P V. Stage s holds K at
-// ring + s*stage_bytes and V right after it (NSLAB slabs each).
-template <int NSLAB, int STAGES, int ELEMS_PER_SLAB>
-__device__ void produce_operand(const DevPlan& P, const DevChunk& C, int head, uint32_t ring, uint32_t stage_bytes,
-                                uint32_t bar_full, uint32_t bar_empty, const CUtensorMap* map, bool vee) {
-    constexpr uint32_t kSlabBytes = kTileTokens * 128;
-    constexpr uint32_t kHalf = NSLAB * kSlabBytes;
-    const ChunkGeo g = chunk_geo(C);
+// TMA producer for one operand (K or V) with its own full/empty barriers:
+// tiles of TT tokens go round a ring of STAGES stages; stage s starts at
+// ring + s * NSLAB * TT * 128 and holds NSLAB slabs of TT rows x 128 bytes.
+// Boxes entirely outside the chunk are skipped.
+template <int NSLAB, int TT, int STAGES>
+__device__ void produce_tiles(const DevPlan& P, const DevChunk& C, int head, uint32_t ring, uint32_t bar_full,
+                              uint32_t bar_empty, const CUtensorMap* map) {
+    constexpr uint32_t kSlabBytes = TT * 128;
+    constexpr uint32_t kStageBytes = NSLAB * kSlabBytes;
+    const ChunkGeo g = chunk_geo<TT>(C);
     const int ps = P.page_size;
     const int n_list = (g.pos_end - 1) / ps + 1;
     for (int i = 0; i < g.n_tiles; ++i) {
@@ -178,30 +201,58 @@ __device__ void produce_operand(const DevPlan& P, const DevChunk& C, int head, u
         if (i >= STAGES) {
             if (!mbar_wait(bar_empty + 8 * s, ((i / STAGES) - 1) & 1, P.status)) return;
         }
-        const int tpos = g.tile0 + i * kTileTokens;
+        const int tpos = g.tile0 + i * TT;
+        int page[TT / kBoxRows];
         uint32_t nbox = 0;
 #pragma unroll
-        for (int b = 0; b < kTileTokens / kBoxRows; ++b) {
+        for (int b = 0; b < TT / kBoxRows; ++b) {
             const int pos = tpos + b * kBoxRows;
-            if (pos + kBoxRows > g.pos_begin && pos < g.pos_end) ++nbox;
+            const bool in = pos + kBoxRows > g.pos_begin && pos < g.pos_end;
+            const int li = pos / ps;
+            page[b] = (in && li < n_list) ? P.pages[C.page_base + li] : 0;
+            nbox += in ? 1u : 0u;
         }
         const uint32_t full = bar_full + 8 * s;
         mbar_arrive_expect_tx(full, nbox * NSLAB * kBoxRows * 128u);
-        const uint32_t dst0 = ring + s * stage_bytes + (vee ? kHalf : 0);
+        const uint32_t dst0 = ring + s * kStageBytes;
 #pragma unroll
-        for (int b = 0; b < kTileTokens / kBoxRows; ++b) {
+        for (int b = 0; b < TT / kBoxRows; ++b) {
             const int pos = tpos + b * kBoxRows;
             if (!(pos + kBoxRows > g.pos_begin && pos < g.pos_end)) continue;
-            const int li = pos / ps;
-            int page = 0;
-            if (li < n_list) page = P.pages[C.page_base + li];
-            const int slab_z = page * P.n_kv_heads + head;
+            const int slab_z = page[b] * P.n_kv_heads + head;
             const int row0 = pos % ps;
 #pragma unroll
             for (int sl = 0; sl < NSLAB; ++sl)
-                tma_load_3d(dst0 + sl * kSlabBytes + b * kBoxRows * 128, map, sl * ELEMS_PER_SLAB, row0, slab_z, full);
+                tma_load_3d(dst0 + sl * kSlabBytes + b * kBoxRows * 128, map, sl * 64, row0, slab_z, full);
         }
     }
+}
+
+using u64 = unsigned long long;
+
+// Two floats in one 64-bit register pair, for Blackwell's packed f32x2 ALU ops.
+__device__ __forceinline__ u64 pk2(float a, float b) {
+    u64 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(u64 r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+    u64 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+    u64 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ u64 add2(u64 a, u64 b) {
+    u64 d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
 }
 
 }  // namespace dev

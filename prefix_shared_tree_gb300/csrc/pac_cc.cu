@@ -25,28 +25,6 @@ namespace dev {
 constexpr int kCcWarps = 4;
 constexpr int kCcStages = 2;
 
-using u64 = unsigned long long;
-
-// Two floats in one 64-bit register pair, for Blackwell's packed f32x2 ALU ops.
-__device__ __forceinline__ u64 pk2(float a, float b) {
-    u64 r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-    return r;
-}
-__device__ __forceinline__ void upk2(u64 r, float& a, float& b) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
-}
-__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
-    u64 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
-    u64 d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
 template <typename T>
 struct ElemTraits;
 template <>

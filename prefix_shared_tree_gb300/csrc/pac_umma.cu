@@ -10,58 +10,72 @@
 // visibility inside packed draft-token chunks.
 //
 // One thread block per (chunk, kv head, block of up to 256 rows), warp-
-// specialised (11 warps):
-//   warps 0, 10 TMA producers of K and of V: 64-token tiles (16-row page
-//               boxes, 128B swizzle) into 3-stage rings; a K stage is
+// specialised (12 warps, three warpgroups):
+//   warps 0, 2  TMA producers of K and of V: 128-token tiles (16-row page
+//               boxes, 128B swizzle) into their own rings; a K stage is
 //               refilled as soon as Q K^T has read it, a V stage after P V;
 //   warp 1      allocates all 512 tensor-memory columns and issues every MMA
-//               from one thread: S = Q K^T (M=128, N=64) and O += P V
-//               (M=128, N=d; P from shared memory, V MN-major);
-//   warps 2-9   two softmax warpgroups, one thread per row (tensor-memory
+//               from one thread: S = Q K^T (M=128, N=128, Q and K from shared
+//               memory) and O += P V (M=128, N=d, P from tensor memory, V
+//               MN-major from shared memory);
+//   warps 4-11  two softmax warpgroups, one thread per row (tensor-memory
 //               lane). With more than 128 rows each group owns one 128-row
-//               half and both consume every tile; with at most 128 rows the
-//               groups take alternate tiles into separate O accumulators
-//               and merge them at the end (split-KV inside the block). Either
-//               way two softmax warps share each scheduler.
+//               half and both consume every tile; the MMA warp alternates
+//               between the halves so that one group's softmax overlaps the
+//               other half's MMAs. With at most 128 rows the groups take
+//               alternate tiles into separate O accumulators and merge them
+//               at the end (split-KV inside the block).
+// The first warpgroup hands registers to the softmax warpgroups
+// (setmaxnreg), which hold a whole 128-column row of S in registers.
+// Tensor memory: S of half w in columns [128w, 128w+128), O of half w in
+// [256 + d*w, 256 + d*w + d). The softmax overwrites S with P (bf16, two per
+// column); the next S of that half is issued after the P V that reads it, and
+// tcgen05 MMAs from one thread run in issue order.
 // Softmax works in the log2 domain with 1/sqrt(d) folded into one FMA; the
 // running max only moves (and O is rescaled in tensor memory) when it grows
-// by more than 2^8, so the result is exact in fp32. P goes to shared memory
-// as bf16 hi + lo parts (p = hi + lo to ~2^-16), which keeps the PV product
-// as accurate as an fp32 one. (Measured on GB300: with P kept in tensor
-// memory instead, the PV MMAs reading it ran at about half rate while the
-// softmax warps loaded S and stored P; from shared memory they run at full rate.)
+// by more than 2^8, so the result is exact in fp32. The EXACT instance (chunks
+// shorter than the plan's p_bf16_min_tokens) splits P into bf16 hi + lo parts
+// (p = hi + lo to ~2^-16), which makes P V as accurate as an fp32 product; the
+// other rounds P once to bf16, whose relative error (2^-8 per weight, random
+// in sign) averages out over a long chunk's many weights. Scores a row may
+// not see (tile edges, bit causal masks) are set to -inf in tensor memory
+// before the row is loaded, which keeps masking out of the hot code.
 #include "dev_common.cuh"
 #include "umma.cuh"
 
 namespace pst {
 namespace dev {
 
-constexpr int kUWarps = 11;      // K producer, MMA, 2 x 4 softmax warps, V producer
-constexpr int kUStages = 3;
+constexpr int kUWarps = 12;      // K producer, MMA, V producer, idle, 2 x 4 softmax warps
 constexpr int kUThreads = kUWarps * 32;
+// Registers per thread: at launch (the __launch_bounds__ cap for 384 threads),
+// then after setmaxnreg in the producer/MMA warpgroup and in the two softmax
+// warpgroups. The split must not exceed the launch total:
+// 128 * 104 + 256 * 200 == 384 * 168.
+constexpr int kURegsLaunch = 168, kURegsLow = 104, kURegsHigh = 200;
+static_assert(128 * kURegsLow + 256 * kURegsHigh <= kUThreads * kURegsLaunch, "register split");
+constexpr int kUT = kTcTileTokens;   // tokens per tile
 constexpr float kLazyRescale = 8.f;
 
 template <int D>
 struct UmmaLayout {
     static constexpr int NSLAB = D / 64;
-    static constexpr uint32_t kSlab = kTileTokens * 128;          // one 64-row slab
-    static constexpr uint32_t kHalf = NSLAB * kSlab;              // K or V of a stage
-    static constexpr uint32_t kStage = 2 * kHalf;
-    static constexpr uint32_t kQSlab = 128 * 128;                 // 128 rows x 128 B
-    static constexpr uint32_t kRing = kUStages * kStage;
-    static constexpr uint32_t kQ = kRing;                         // Q: 2 halves x NSLAB slabs
-    static constexpr uint32_t kP = kQ + 2 * NSLAB * kQSlab;       // P[w][hi|lo]: 128 rows x 64 tokens bf16
-    static constexpr uint32_t kPBuf = 128 * 128;
-    static constexpr uint32_t kXchg = kP + 4 * kPBuf;             // 128 x (m, l) for the split-KV merge
+    static constexpr uint32_t kSlab = kUT * 128;                   // 128 token rows x 128 B
+    static constexpr uint32_t kOp = NSLAB * kSlab;                 // one K or V tile
+    static constexpr int KST = D == 128 ? 3 : 4;                   // K stages
+    static constexpr int VST = D == 128 ? 2 : 4;                   // V stages
+    static constexpr uint32_t kQSlab = 128 * 128;                  // 128 rows x 128 B
+    static constexpr uint32_t kK = 0;
+    static constexpr uint32_t kV = kK + KST * kOp;
+    static constexpr uint32_t kQ = kV + VST * kOp;                 // 2 halves x NSLAB slabs
+    static constexpr uint32_t kXchg = kQ + 2 * NSLAB * kQSlab;     // 128 x (m, l) for the split-KV merge
     static constexpr uint32_t kBars = kXchg + 128 * 8;
-    // k_full[ST], k_empty[ST], v_full[ST], v_empty[ST], q_ready, s_full[2][2], p_full[2][2],
-    // o_done[2], mma_done, tmem slot
-    static constexpr int kNumBars = 4 * kUStages + 12;
+    // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], q_ready, s_full[2], p_full[2], mma_done
+    static constexpr int kNumBars = 2 * KST + 2 * VST + 6;
     static constexpr uint32_t kBytes = kBars + 8 * kNumBars + 16;
     static_assert(kBytes + 1024 <= 232448, "shared memory");
     static constexpr uint32_t kTmemCols = 512;
-    // tensor-memory columns: S[w][b] at 128w + 64b, O[w] at 256 + D*w
-    __device__ static constexpr uint32_t colS(int w, int b) { return 128 * w + 64 * b; }
+    __device__ static constexpr uint32_t colS(int w) { return 128 * w; }
     __device__ static constexpr uint32_t colO(int w) { return 256 + D * w; }
 };
 
@@ -70,28 +84,24 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D>
+template <int D, bool EXACT>
 __global__ void __launch_bounds__(kUThreads, 1)
 pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                 const __nv_bfloat16* __restrict__ Q, int item_off) {
     using L = UmmaLayout<D>;
     constexpr int NSLAB = L::NSLAB;
+    constexpr int KST = L::KST, VST = L::VST;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(base);
-    const uint32_t ring = sbase, sQ = sbase + L::kQ, sP = sbase + L::kP;
+    const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sQ = sbase + L::kQ;
     const uint32_t bars = sbase + L::kBars;
-    // K and V stages have separate barriers: a K stage is refilled once Q K^T
-    // has read it, a V stage once P V has.
-    const uint32_t k_full = bars, k_empty = bars + 8 * kUStages;
-    const uint32_t v_full = bars + 16 * kUStages, v_empty = bars + 24 * kUStages;
-    const uint32_t q_ready = bars + 32 * kUStages;
-    // One p_full per S buffer: a group can then never complete two phases of
-    // the same barrier before the MMA warp has waited for the first.
-    const uint32_t s_full = q_ready + 8;      // [w][b] at s_full + 8*(2w+b)
-    const uint32_t p_full = s_full + 32;      // [w][b] at p_full + 8*(2w+b)
-    const uint32_t o_done = p_full + 32;      // [w]
-    const uint32_t mma_done = o_done + 16;
+    const uint32_t k_full = bars, k_empty = k_full + 8 * KST;
+    const uint32_t v_full = k_empty + 8 * KST, v_empty = v_full + 8 * VST;
+    const uint32_t q_ready = v_empty + 8 * VST;
+    const uint32_t s_full = q_ready + 8;      // [w]
+    const uint32_t p_full = s_full + 16;      // [w]
+    const uint32_t mma_done = p_full + 16;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kBars + 8 * L::kNumBars);
     float2* xchg = reinterpret_cast<float2*>(base + L::kXchg);
 
@@ -106,18 +116,19 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     const bool split_rows = rows_here > 128;   // mode A: groups own row halves; else alternate tiles
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kUStages; ++s) {
+        for (int s = 0; s < KST; ++s) {
             mbar_init(k_full + 8 * s, 1);
             mbar_init(k_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < VST; ++s) {
             mbar_init(v_full + 8 * s, 1);
             mbar_init(v_empty + 8 * s, 1);
         }
         mbar_init(q_ready, 256);
-        for (int i = 0; i < 4; ++i) {
-            mbar_init(s_full + 8 * i, 1);
-            mbar_init(p_full + 8 * i, 128);
+        for (int w = 0; w < 2; ++w) {
+            mbar_init(s_full + 8 * w, 1);
+            mbar_init(p_full + 8 * w, 128);
         }
-        for (int w = 0; w < 2; ++w) mbar_init(o_done + 8 * w, 1);
         mbar_init(mma_done, 1);
         fence_barrier_init();
     }
@@ -129,95 +140,117 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const ChunkGeo geo = chunk_geo(C);
+    const ChunkGeo geo = chunk_geo<kUT>(C);
     const int n = geo.n_tiles;
     // steps of softmax group w: tiles it consumes, in order
     auto n_steps = [&](int w) { return split_rows ? n : (n - w + 1) / 2; };
     auto tile_of = [&](int w, int k) { return split_rows ? k : 2 * k + w; };
 
-    if (warp == 0 || warp == kUWarps - 1) {
+    if (warp < 4) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kURegsLow));
+    if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ TMA producers
-        // warp 0 streams K, the last warp streams V, each at its own pace (two
-        // lanes of one warp would reconverge and tie the two streams together)
+        // warp 0 streams K, warp 2 streams V, each at its own pace (two lanes
+        // of one warp would reconverge and tie the two streams together)
         if (lane == 0) {
-            const bool vee = warp != 0;
-            prefetch_tmap(vee ? &tv : &tk);
-            produce_operand<NSLAB, kUStages, 64>(P, C, head, ring, L::kStage, vee ? v_full : k_full,
-                                                 vee ? v_empty : k_empty, vee ? &tv : &tk, vee);
+            if (warp == 0) {
+                prefetch_tmap(&tk);
+                produce_tiles<NSLAB, kUT, KST>(P, C, head, sK, k_full, k_empty, &tk);
+            } else {
+                prefetch_tmap(&tv);
+                produce_tiles<NSLAB, kUT, VST>(P, C, head, sV, v_full, v_empty, &tv);
+            }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idS = umma::idesc_bf16_f32(128, kTileTokens, 0, 0);
+            constexpr uint32_t idS = umma::idesc_bf16_f32(128, kUT, 0, 0);
             constexpr uint32_t idO = umma::idesc_bf16_f32(128, D, 0, 1);   // V is MN-major
             bool ok = mbar_wait(q_ready, 0, P.status);
             umma::fence_after_sync();
             // Descriptors are built once; an MMA only adds a compile-time byte
-            // offset (>> 4) to the start-address field, which keeps the single
-            // issuing thread far ahead of the tensor pipe. Shared-memory
+            // offset (>> 4) to the start-address field. Shared-memory
             // addresses stay below 2^18, so the field never carries over.
             const uint64_t dq_base[2] = {umma::smem_desc_sw128(sQ, 16, 1024),
                                          umma::smem_desc_sw128(sQ + NSLAB * L::kQSlab, 16, 1024)};
-            const uint64_t dk_base = umma::smem_desc_sw128(ring, 16, 1024);
-            const uint64_t dv_base = umma::smem_desc_sw128(ring + L::kHalf, L::kSlab, 1024);
-            const uint64_t dp_base = umma::smem_desc_sw128(sP, 16, 1024);
-            auto issue_s = [&](int w, int k, int j) {
+            const uint64_t dk_base = umma::smem_desc_sw128(sK, 16, 1024);
+            const uint64_t dv_base = umma::smem_desc_sw128(sV, L::kSlab, 1024);
+            // S of group w for tile j: Q half (mode A) x K tile j
+            auto issue_s = [&](int w, int j) {
                 const uint64_t dq = dq_base[split_rows ? w : 0];
-                const uint64_t dk = dk_base + (uint64_t)(((j % kUStages) * L::kStage) >> 4);
-                const uint32_t dst = tmem + L::colS(w, k & 1);
+                const uint64_t dk = dk_base + (uint64_t)(((j % KST) * L::kOp) >> 4);
+                const uint32_t dst = tmem + L::colS(w);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     umma::mma_bf16_ss(dst, dq + (((kk / 4) * L::kQSlab + (kk % 4) * 32) >> 4),
                                       dk + (((kk / 4) * L::kSlab + (kk % 4) * 32) >> 4), idS, kk > 0 ? 1u : 0u);
-                umma::commit(s_full + 8 * (2 * w + (k & 1)));
+                umma::commit(s_full + 8 * w);
             };
-            // PV of step k of group w (tile j): O[w] += P_hi V + P_lo V
+            // PV of group w for tile j (its step k): O[w] (+)= P V (+ P_lo V)
             auto issue_pv = [&](int w, int k, int j) -> bool {
-                if (!mbar_wait(p_full + 8 * (2 * w + (k & 1)), (k >> 1) & 1, P.status)) return false;
-                if (!mbar_wait(v_full + 8 * (j % kUStages), (j / kUStages) & 1, P.status)) return false;
+                if (!mbar_wait(p_full + 8 * w, k & 1, P.status)) return false;
                 umma::fence_after_sync();
-                const uint64_t dv = dv_base + (uint64_t)(((j % kUStages) * L::kStage) >> 4);
-                const uint64_t dh = dp_base + (uint64_t)((2 * w * L::kPBuf) >> 4);
-                const uint64_t dl = dh + (uint64_t)(L::kPBuf >> 4);
+                const uint64_t dv = dv_base + (uint64_t)(((j % VST) * L::kOp) >> 4);
+                const uint32_t ph = tmem + L::colS(w);
                 const uint32_t dst = tmem + L::colO(w);
                 const uint32_t acc0 = k > 0 ? 1u : 0u;
 #pragma unroll
-                for (int kk = 0; kk < kTileTokens / 16; ++kk) {
-                    umma::mma_bf16_ss(dst, dh + ((kk * 32) >> 4), dv + ((kk * 2048) >> 4), idO, kk > 0 ? 1u : acc0);
-                    umma::mma_bf16_ss(dst, dl + ((kk * 32) >> 4), dv + ((kk * 2048) >> 4), idO, 1u);
+                for (int kk = 0; kk < kUT / 16; ++kk)
+                    umma::mma_bf16_ts(dst, ph + 8 * kk, dv + ((kk * 2048) >> 4), idO, kk > 0 ? 1u : acc0);
+                if (EXACT) {
+#pragma unroll
+                    for (int kk = 0; kk < kUT / 16; ++kk)
+                        umma::mma_bf16_ts(dst, ph + 64 + 8 * kk, dv + ((kk * 2048) >> 4), idO, 1u);
                 }
-                umma::commit(o_done + 8 * w);
                 return true;
             };
-            for (int j = 0; j < n && ok; ++j) {
-                const int s = j % kUStages;
-                if (!mbar_wait(k_full + 8 * s, (j / kUStages) & 1, P.status)) { ok = false; break; }
-                if (split_rows) {
-                    issue_s(0, j, j);
-                    issue_s(1, j, j);
-                } else {
-                    issue_s(j & 1, j >> 1, j);
+            auto wait_v = [&](int j) { return mbar_wait(v_full + 8 * (j % VST), (j / VST) & 1, P.status); };
+            if (split_rows) {
+                // per tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j)
+                for (int j = 0; j < n && ok; ++j) {
+                    if (!mbar_wait(k_full + 8 * (j % KST), (j / KST) & 1, P.status)) { ok = false; break; }
+                    if (j >= 1 && !wait_v(j - 1)) { ok = false; break; }
+                    for (int w = 0; w < 2 && ok; ++w) {
+                        if (j >= 1 && !issue_pv(w, j - 1, j - 1)) { ok = false; break; }
+                        issue_s(w, j);
+                    }
+                    if (!ok) break;
+                    umma::commit(k_empty + 8 * (j % KST));
+                    if (j >= 1) umma::commit(v_empty + 8 * ((j - 1) % VST));
                 }
-                umma::commit(k_empty + 8 * s);     // K stage free once these S MMAs complete
-                if (j >= 1) {
-                    const bool good = split_rows ? (issue_pv(0, j - 1, j - 1) && issue_pv(1, j - 1, j - 1))
-                                                 : issue_pv((j - 1) & 1, (j - 1) >> 1, j - 1);
-                    if (!good) { ok = false; break; }
-                    umma::commit(v_empty + 8 * ((j - 1) % kUStages));
+                if (ok && n >= 1) {
+                    const int j = n - 1;
+                    ok = wait_v(j) && issue_pv(0, j, j) && issue_pv(1, j, j);
+                    if (ok) umma::commit(v_empty + 8 * (j % VST));
+                }
+            } else {
+                // tile j belongs to group j & 1 (its step j >> 1); per tile j:
+                // PV of tile j-2 (same group), then S of tile j
+                for (int j = 0; j < n && ok; ++j) {
+                    const int w = j & 1;
+                    if (!mbar_wait(k_full + 8 * (j % KST), (j / KST) & 1, P.status)) { ok = false; break; }
+                    if (j >= 2) {
+                        if (!(wait_v(j - 2) && issue_pv(w, (j >> 1) - 1, j - 2))) { ok = false; break; }
+                        umma::commit(v_empty + 8 * ((j - 2) % VST));
+                    }
+                    issue_s(w, j);
+                    umma::commit(k_empty + 8 * (j % KST));
+                }
+                for (int j = max(0, n - 2); j < n && ok; ++j) {
+                    ok = wait_v(j) && issue_pv(j & 1, j >> 1, j);
+                    if (ok) umma::commit(v_empty + 8 * (j % VST));
                 }
             }
-            if (ok && n >= 1) {
-                const int j = n - 1;
-                bool good = split_rows ? (issue_pv(0, j, j) && issue_pv(1, j, j)) : issue_pv(j & 1, j >> 1, j);
-                if (good) umma::commit(v_empty + 8 * (j % kUStages));
-            }
-            // every MMA issued above has finished before tensor memory is released
+            // every MMA issued above has finished before tensor memory is read
+            // by the epilogue or released
             umma::commit(mma_done);
             mbar_wait(mma_done, 0, P.status);
         }
+    }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kURegsHigh));
         // ------------------------------------------------------------ softmax warpgroups
-        const int w = (warp - 2) / 4;                // group 0: warps 2-5, group 1: warps 6-9
+        const int w = (warp - 4) / 4;                // group 0: warps 4-7, group 1: warps 8-11
         const int r = 32 * (warp % 4) + lane;        // tensor-memory lane = row within the half
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp % 4)) << 16);
         const int rloc = split_rows ? 128 * w + r : r;   // row within the block
@@ -250,122 +283,147 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         const float sl = P.scale_log2;
         const bool masked_chunk = C.mask_base >= 0;
         const bool zero_v = split_rows ? (w == 0) : true;   // one group zeroes a tile's stray V rows
-        float m_ref = -INFINITY, l = 0.f;                      // raw-score units for m_ref
+        float m_ref = -INFINITY, l = 0.f;                      // m_ref in scaled (log2) units
         bool ok = true;
         const int nk = n_steps(w);
+        const uint32_t s_addr = lane_addr + L::colS(w);
         for (int k = 0; k < nk; ++k) {
             const int j = tile_of(w, k);
-            const int b = k & 1;
-            if (!mbar_wait(s_full + 8 * (2 * w + b), (k >> 1) & 1, P.status)) { ok = false; break; }
+            // tcgen05.ld/st are warp-collective: every decision that guards
+            // them is taken by the whole warp
+            if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * w, k & 1, P.status))) { ok = false; break; }
             umma::fence_after_sync();
-            float x[kTileTokens];
-            {
-                float v[32];
-                umma::ld32(lane_addr + L::colS(w, b), v);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) x[c] = v[c];
-                umma::ld32(lane_addr + L::colS(w, b) + 32, v);
-                umma::wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) x[32 + c] = v[c];
-            }
-            const int tpos = geo.tile0 + j * kTileTokens;
-            const bool edge = tpos < geo.pos_begin || tpos + kTileTokens > geo.pos_end;
-            float mx = -INFINITY;
+            const int tpos = geo.tile0 + j * kUT;
+            const bool edge = tpos < geo.pos_begin || tpos + kUT > geo.pos_end;
             if (edge || masked_chunk) {
+                // Scores this row may not see become -inf in tensor memory, in
+                // 32-column groups, so that the hot code below has no masking.
+                const int c_lo = geo.pos_begin - tpos, c_hi = geo.pos_end - tpos;
+#pragma unroll 1
+                for (int c0 = 0; c0 < kUT; c0 += 32) {
+                    if (!masked_chunk && c0 >= c_lo && c0 + 32 <= c_hi) continue;
+                    float v[32];
+                    umma::ld32(s_addr + c0, v);
+                    umma::wait_ld();
 #pragma unroll
-                for (int c = 0; c < kTileTokens; ++c) {
-                    const int pos = tpos + c;
-                    const int t = pos - geo.pos_begin;
-                    const bool vis = pos >= geo.pos_begin && pos < geo.pos_end && (t >= 64 || ((mask >> (t & 63)) & 1ull));
-                    x[c] = vis ? x[c] : -INFINITY;
-                    mx = fmaxf(mx, x[c]);
+                    for (int c = 0; c < 32; ++c) {
+                        const int t = c0 + c - c_lo;   // token index in the chunk
+                        const bool vis = t >= 0 && c0 + c < c_hi && (t >= kMaskTokens || ((mask >> (t & 63)) & 1ull));
+                        v[c] = vis ? v[c] : -INFINITY;
+                    }
+                    umma::st32(s_addr + c0, v);
                 }
-            } else {
+                umma::wait_st();
+            }
+            float x[kUT];
 #pragma unroll
-                for (int c = 0; c < kTileTokens; ++c) mx = fmaxf(mx, x[c]);
+            for (int q = 0; q < kUT / 32; ++q) {
+                float v[32];
+                umma::ld32(s_addr + 32 * q, v);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[32 * q + c] = v[c];
+            }
+            umma::wait_ld();
+            // four independent chains of three-input maxima
+            float mx;
+            {
+                float acc[4];
+#pragma unroll
+                for (int a = 0; a < 4; ++a) acc[a] = fmaxf(x[a], x[4 + a]);
+#pragma unroll
+                for (int c = 8; c < kUT; c += 8) {
+#pragma unroll
+                    for (int a = 0; a < 4; ++a) acc[a] = fmax3(acc[a], x[c + a], x[c + 4 + a]);
+                }
+                mx = fmaxf(fmax3(acc[0], acc[1], acc[2]), acc[3]);
             }
             const float mxs = mx * sl;   // scale > 0: max commutes with it
             const bool grow = (m_ref == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref + kLazyRescale);
-            bool rescaled = false;
+            float alpha = 1.f;
+            bool rescale = false;
             if (grow) {
-                const float alpha = fast_exp2(m_ref - mxs);   // 0 when nothing was accumulated
-                if (k >= 1 && m_ref != -INFINITY) {
-                    // O is about to be rescaled: the previous PV of this group must be
-                    // done (waited for just below in any case).
-                    if (!mbar_wait(o_done + 8 * w, (k - 1) & 1, P.status)) { ok = false; break; }
-                    umma::fence_after_sync();
-#pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[32];
-                        umma::ld32(lane_addr + L::colO(w) + 32 * c, o);
-                        umma::wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        umma::st32(lane_addr + L::colO(w) + 32 * c, o);
-                    }
-                    rescaled = true;
-                }
+                alpha = fast_exp2(m_ref - mxs);   // 0 when nothing was accumulated
+                rescale = k >= 1 && m_ref != -INFINITY;
                 l *= alpha;
                 m_ref = mxs;
             }
             const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
-            uint32_t hi[32], lo[32];
-            float sum = 0.f;
+            const u64 sl2 = pk2(sl, sl), nmu2 = pk2(nmu, nmu);
+            u64 sum2[4] = {0ull, 0ull, 0ull, 0ull};   // independent add chains
+            if (!EXACT) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const float a = fast_exp2(fmaf(x[2 * c], sl, nmu));
-                const float bb = fast_exp2(fmaf(x[2 * c + 1], sl, nmu));
-                sum += a + bb;
-                const uint32_t h = bf16x2_bits(a, bb);
-                hi[c] = h;
-                lo[c] = bf16x2_bits(a - __uint_as_float(h << 16), bb - __uint_as_float(h & 0xffff0000u));
-            }
-            l += sum;
-            // P's shared-memory buffer is reused every step: the previous PV of
-            // this group must have read it. When S_k has completed, every PV
-            // before step k-1 has too, so o_done is at most one phase behind and
-            // the parity wait is exact.
-            if (k >= 1 && !rescaled) {
-                if (!mbar_wait(o_done + 8 * w, (k - 1) & 1, P.status)) { ok = false; break; }
-            }
-            {
-                // row r of P (64 tokens = 128 bytes), K-major with the 128B swizzle
-                uint8_t* ph = base + L::kP + 2 * w * L::kPBuf;
-                uint8_t* pl = ph + L::kPBuf;
+                for (int q = 0; q < kUT / 32; ++q) {
+                    uint32_t hi[16];
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    *reinterpret_cast<uint4*>(ph + swz(r, ch)) =
-                        make_uint4(hi[4 * ch], hi[4 * ch + 1], hi[4 * ch + 2], hi[4 * ch + 3]);
-                    *reinterpret_cast<uint4*>(pl + swz(r, ch)) =
-                        make_uint4(lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
+                    for (int c = 0; c < 16; ++c) {
+                        float a, b;
+                        upk2(fma2(pk2(x[32 * q + 2 * c], x[32 * q + 2 * c + 1]), sl2, nmu2), a, b);
+                        a = fast_exp2(a);
+                        b = fast_exp2(b);
+                        sum2[c & 3] = add2(sum2[c & 3], pk2(a, b));
+                        hi[c] = bf16x2_bits(a, b);
+                    }
+                    umma::st16(s_addr + 16 * q, hi);
+                }
+            } else {
+#pragma unroll
+                for (int q = 0; q < kUT / 16; ++q) {
+                    uint32_t hi[8], lo[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        float a, b;
+                        upk2(fma2(pk2(x[16 * q + 2 * c], x[16 * q + 2 * c + 1]), sl2, nmu2), a, b);
+                        a = fast_exp2(a);
+                        b = fast_exp2(b);
+                        sum2[c & 3] = add2(sum2[c & 3], pk2(a, b));
+                        hi[c] = bf16x2_bits(a, b);
+                        lo[c] = bf16x2_bits(a - __uint_as_float(hi[c] << 16), b - __uint_as_float(hi[c] & 0xffff0000u));
+                    }
+                    umma::st8(s_addr + 8 * q, hi);
+                    umma::st8(s_addr + 64 + 8 * q, lo);
                 }
             }
-            bool zeroed = false;
+            {
+                float s0, s1;
+                upk2(add2(add2(sum2[0], sum2[1]), add2(sum2[2], sum2[3])), s0, s1);
+                l += s0 + s1;
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+                // O of this group is stable between its S completing (every
+                // earlier MMA of the group had finished) and its p_full arrival.
+                if (!rescale) alpha = 1.f;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    float o[32];
+                    umma::ld32(lane_addr + L::colO(w) + 32 * c, o);
+                    umma::wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    umma::st32(lane_addr + L::colO(w) + 32 * c, o);
+                }
+            }
             if (edge && zero_v) {
                 // V rows outside the chunk may hold stale or non-finite values:
                 // zero them before the PV of this tile multiplies them by P = 0.
-                const int s = j % kUStages;
-                if (!mbar_wait(v_full + 8 * s, (j / kUStages) & 1, P.status)) { ok = false; break; }
-                if (r < kTileTokens * NSLAB) {          // one 128-byte slab row per thread
-                    const int t = r % kTileTokens, sl_i = r / kTileTokens;
-                    const int pos = tpos + t;
-                    if (pos < geo.pos_begin || pos >= geo.pos_end) {
-                        uint8_t* vrow = base + s * L::kStage + L::kHalf + sl_i * L::kSlab + t * 128;
+                const int s = j % VST;
+                if (!__all_sync(0xffffffffu, mbar_wait(v_full + 8 * s, (j / VST) & 1, P.status))) { ok = false; break; }
+                const int pos = tpos + r;                    // thread r owns token row r of the tile
+                if (pos < geo.pos_begin || pos >= geo.pos_end) {
+#pragma unroll
+                    for (int sl_i = 0; sl_i < NSLAB; ++sl_i) {
+                        uint8_t* vrow = base + L::kV + s * L::kOp + sl_i * L::kSlab + r * 128;
 #pragma unroll
                         for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0, 0, 0, 0);
-                        zeroed = true;
                     }
                 }
+                fence_proxy_async_smem();   // zeroed V rows are read by the tensor core
             }
-            if (rescaled) umma::wait_st();
-            (void)zeroed;
-            fence_proxy_async_smem();   // P (and zeroed V rows) are read by the tensor core
+            umma::wait_st();
             umma::fence_before_sync();
-            mbar_arrive(p_full + 8 * (2 * w + b));
+            mbar_arrive(p_full + 8 * w);
         }
         // ---- epilogue: wait for the MMA warp's final commit (every MMA done)
-        bool have = ok && nk >= 1 && mbar_wait(mma_done, 0, P.status);
+        const bool have = __all_sync(0xffffffffu, ok && nk >= 1 && mbar_wait(mma_done, 0, P.status));
         if (have) umma::fence_after_sync();
         if (!split_rows) {
             // split-KV inside the block: group 1 hands (m, l) to group 0, which
@@ -391,7 +449,11 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             const float Lt = l * a0 + l1 * a1;
             const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
             const int64_t prow = (int64_t)C.part_base + (int64_t)qi * Hq + head * G + gh;
-            float* dst = P.part_o + prow * D;
+            // The warp's 32 rows go through shared memory (the K/V rings are
+            // free once every MMA has finished) so that each global store
+            // writes whole 512-byte rows: row-major [32][D] floats, the 16-byte
+            // units of row r permuted by r & 7 against bank conflicts.
+            float* stage = reinterpret_cast<float*>(base + L::kK) + (size_t)(warp - 4) * 32 * D;
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
                 float o[32];
@@ -407,12 +469,24 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= a0;
                 }
-                if (row_ok) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(dst + 32 * c + i) =
-                            make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+                for (int i = 0; i < 32; i += 4) {
+                    const int u = 8 * c + i / 4;
+                    *reinterpret_cast<float4*>(stage + lane * D + 4 * (u ^ (lane & 7))) =
+                        make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
                 }
+            }
+            __syncwarp();
+            constexpr int kUnits = D / 4;            // float4 units per row
+            constexpr int kRowsPerStep = 32 / kUnits;
+            const int64_t my_prow = row_ok ? prow : -1;
+#pragma unroll 4
+            for (int rr = 0; rr < 32; rr += kRowsPerStep) {
+                const int r2 = rr + lane / kUnits, u = lane % kUnits;
+                const int64_t pr = __shfl_sync(0xffffffffu, my_prow, r2);
+                if (pr >= 0)
+                    *reinterpret_cast<float4*>(P.part_o + pr * D + 4 * u) =
+                        *reinterpret_cast<const float4*>(stage + r2 * D + 4 * (u ^ (r2 & 7)));
             }
             if (row_ok) P.part_lse[prow] = Lt > 0.f ? M + __log2f(Lt) : -INFINITY;
         }
@@ -425,28 +499,38 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     }
 }
 
-template <int D>
+template <int D, bool EXACT>
 cudaError_t launch_umma_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
                           int item_off, cudaStream_t st) {
     const size_t smem = 1024 + UmmaLayout<D>::kBytes;
     static bool attr_set = false;  // once per process (single device per process)
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(pac_umma_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        // setmaxnreg.inc waits for registers the other warpgroup released: the
+        // split is only valid for the launch register count it was sized for
+        cudaFuncAttributes fa;
+        cudaError_t e = cudaFuncGetAttributes(&fa, pac_umma_kernel<D, EXACT>);
+        if (e != cudaSuccess) return e;
+        if (fa.numRegs != kURegsLaunch) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(pac_umma_kernel<D, EXACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    pac_umma_kernel<D><<<n_items, kUThreads, smem, st>>>(P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q), item_off);
+    pac_umma_kernel<D, EXACT><<<n_items, kUThreads, smem, st>>>(P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q),
+                                                                item_off);
     return cudaGetLastError();
 }
 
 }  // namespace dev
 
 cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items, int item_off,
-                            cudaStream_t st) {
+                            bool exact_p, cudaStream_t st) {
     const CUtensorMap* k = static_cast<const CUtensorMap*>(tk);
     const CUtensorMap* v = static_cast<const CUtensorMap*>(tv);
-    if (P.d == 128) return dev::launch_umma_t<128>(P, k, v, Q, n_items, item_off, st);
-    return dev::launch_umma_t<64>(P, k, v, Q, n_items, item_off, st);
+    if (P.d == 128)
+        return exact_p ? dev::launch_umma_t<128, true>(P, k, v, Q, n_items, item_off, st)
+                       : dev::launch_umma_t<128, false>(P, k, v, Q, n_items, item_off, st);
+    return exact_p ? dev::launch_umma_t<64, true>(P, k, v, Q, n_items, item_off, st)
+                   : dev::launch_umma_t<64, false>(P, k, v, Q, n_items, item_off, st);
 }
 
 }  // namespace pst

@@ -13,6 +13,7 @@
 // KVMapQ (per node the queries sharing it). DEFT's bit causal mask: one 64-bit
 // word per query records which tokens of a chunk it may see.
 #include <algorithm>
+#include <cstdint>
 #include <chrono>
 #include <memory>
 #include <cmath>
@@ -150,6 +151,7 @@ extern "C" void pst_plan_opts_default(pst_plan_opts* o) {
     o->slots_per_sm = 1;
     o->tc_engine = 0;
     o->tc_block_rows = 256;
+    o->p_bf16_min_tokens = kPBf16MinTokens;
 }
 
 namespace {
@@ -157,13 +159,14 @@ namespace {
 int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
 
 // Chunk boundaries of a node: the node's page-space span [fo, fo+len) is cut
-// at multiples of the tile size so that every chunk starts on a TMA tile.
+// at multiples of the kernel's tile size (`blk` tokens) so that every chunk
+// starts on a TMA tile.
 struct Span {
-    int32_t fo, len, first_block, n_blocks;
+    int32_t fo, len, first_block, n_blocks, blk;
 };
-Span node_span(int32_t fo, int32_t len) {
-    Span s{fo, len, fo / kTileTokens, 0};
-    const int32_t end_block = (fo + len + kTileTokens - 1) / kTileTokens;
+Span node_span(int32_t fo, int32_t len, int32_t blk) {
+    Span s{fo, len, fo / blk, 0, blk};
+    const int32_t end_block = (fo + len + blk - 1) / blk;
     s.n_blocks = std::max(1, end_block - s.first_block);
     return s;
 }
@@ -171,10 +174,15 @@ Span node_span(int32_t fo, int32_t len) {
 void chunk_range(const Span& s, int32_t bk, int32_t k, int32_t* b, int32_t* e) {
     const int64_t blk0 = s.first_block + (int64_t)s.n_blocks * k / bk;
     const int64_t blk1 = s.first_block + (int64_t)s.n_blocks * (k + 1) / bk;
-    int64_t p0 = std::max<int64_t>(blk0 * kTileTokens, s.fo);
-    int64_t p1 = std::min<int64_t>(blk1 * kTileTokens, (int64_t)s.fo + s.len);
+    int64_t p0 = std::max<int64_t>(blk0 * s.blk, s.fo);
+    int64_t p1 = std::min<int64_t>(blk1 * s.blk, (int64_t)s.fo + s.len);
     *b = (int32_t)(p0 - s.fo);
     *e = (int32_t)std::max<int64_t>(p1 - s.fo, p0 - s.fo);
+}
+
+// KV tokens per pipeline tile of the kernel that runs a task of `kind`.
+int32_t tile_tokens(int kind, const pst_plan_opts& o) {
+    return (kind == 1 && o.tc_engine == 0) ? kTcTileTokens : kTileTokens;
 }
 
 int32_t cc_row_tile(int32_t rows) {
@@ -236,7 +244,8 @@ struct Planner {
                     int chunk_id_base) const {
         const int rpb = rows_per_block(t);
         const int n_rb = (t.rows + rpb - 1) / rpb;
-        Span s = t.node >= 0 ? node_span(T.first_offset[t.node], t.n_tok) : Span{0, t.n_tok, 0, 1};
+        Span s = t.node >= 0 ? node_span(T.first_offset[t.node], t.n_tok, tile_tokens(t.kind, P.opts))
+                              : Span{0, t.n_tok, 0, 1, kTileTokens};
         for (int k = 0; k < b; ++k) {
             int32_t tb = 0, te = t.n_tok;
             if (t.node >= 0) chunk_range(s, b, k, &tb, &te);
@@ -414,6 +423,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     if (o.tc_min_rows <= 0) o.tc_min_rows = 16;
     if (o.slots_per_sm <= 0) o.slots_per_sm = 1;
     if (o.tc_block_rows != 128) o.tc_block_rows = 256;
+    if (o.p_bf16_min_tokens == 0) o.p_bf16_min_tokens = kPBf16MinTokens;
     if (o.split_policy == PST_SPLIT_UNIFORM && (o.fixed_chunk <= 0 || o.fixed_chunk % kTileTokens))
         return fail(PST_EINVAL, "plan_create: fixed_chunk must be a positive multiple of 64");
 
@@ -529,7 +539,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
         t.rows = t.n_q * G;
         t.n_tok = T.len[n];
         t.kind = (tc_ok && t.rows >= o.tc_min_rows) ? 1 : 0;
-        t.max_splits = node_span(T.first_offset[n], T.len[n]).n_blocks;
+        t.max_splits = node_span(T.first_offset[n], T.len[n], tile_tokens(t.kind, o)).n_blocks;
         P->tasks.push_back(t);
     }
     for (size_t gi = 0; gi < P->groups.size(); ++gi) {
@@ -576,7 +586,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     for (size_t ti = 0; ti < P->tasks.size(); ++ti) {
         const Task& t = P->tasks[ti];
         if (t.node >= 0) {
-            Span s = node_span(T.first_offset[t.node], t.n_tok);
+            Span s = node_span(T.first_offset[t.node], t.n_tok, tile_tokens(t.kind, o));
             for (int k = 0; k < t.b_k; ++k) {
                 int32_t tb, te;
                 chunk_range(s, t.b_k, k, &tb, &te);
@@ -660,8 +670,18 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     }
     list_schedule(tc, m);
     list_schedule(cc, m);
-    for (const auto& it : tc) P->items.push_back({it.chunk, it.head, it.rb});
+    // tcgen05: items whose chunk multiplies V by P rounded once to bf16 first,
+    // then the exact-P ones (a launch of their own)
+    const int32_t p_single = o.p_bf16_min_tokens < 0 ? INT32_MAX : o.p_bf16_min_tokens;
+    auto exact_item = [&](const ItemCost& it) {
+        return o.tc_engine == 0 && P->chunks[it.chunk].dev.n_tok < p_single;
+    };
+    for (const auto& it : tc)
+        if (!exact_item(it)) P->items.push_back({it.chunk, it.head, it.rb});
+    for (const auto& it : tc)
+        if (exact_item(it)) P->items.push_back({it.chunk, it.head, it.rb});
     P->n_tc_items = (int64_t)tc.size();
+    P->n_tc_exact = (int64_t)std::count_if(tc.begin(), tc.end(), exact_item);
     P->n_cc_items = (int64_t)cc.size();
     // one CUDA-core launch per row tile (8, 4, 2, 1), each in largest-first order
     for (int k = 0; k < 4; ++k) {
@@ -730,7 +750,7 @@ extern "C" int pst_plan_stats_get(const pst_plan* p, pst_plan_stats* s) {
     s->kv_tokens_read = p->kv_tokens_read;
     s->workspace_bytes = p->ws.total;
     s->num_slots = p->num_slots;
-    s->n_launches = (p->n_tc_items > 0) + 1;
+    s->n_launches = (p->n_tc_items - p->n_tc_exact > 0) + (p->n_tc_exact > 0) + 1;
     for (int k = 0; k < 4; ++k) s->n_launches += p->cc_class_cnt[k] > 0;
     return PST_OK;
 }

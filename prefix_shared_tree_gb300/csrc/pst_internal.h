@@ -19,8 +19,12 @@ inline int tc_rows_per_block(const pst_plan_opts& o) {
 }
 // Rows of the CUDA-core PAC per thread block (largest row tile).
 constexpr int kCcRowsPerBlock = 8;
-// KV tokens per pipeline stage of both PAC kernels (4 boxes of 16 rows).
+// KV tokens per pipeline stage of the CUDA-core and mma.sync PAC kernels
+// (4 boxes of 16 rows) and of the tcgen05 PAC (8 boxes).
 constexpr int kTileTokens = 64;
+constexpr int kTcTileTokens = 128;
+// Default of pst_plan_opts::p_bf16_min_tokens.
+constexpr int kPBf16MinTokens = 1024;
 // Rows of one TMA box (page_size must be a multiple).
 constexpr int kBoxRows = 16;
 // Maximum tokens of a chunk that carries a per-query 64-bit mask.
@@ -36,7 +40,7 @@ struct DevChunk {
     int32_t n_q;        // queries grouped with this chunk
     int32_t part_base;  // partial row of (chunk query 0, q-head 0); row = base + qi*Hq + h
     int32_t mask_base;  // -1: every query sees every token; else index into masks[]
-    int32_t r_tile;     // CUDA-core PAC: rows per block (1, 2, 4 or 8); tensor-core: 128
+    int32_t r_tile;     // rows per block: CUDA-core PAC 1, 2, 4 or 8; tensor-core 128 or 256
 };
 static_assert(sizeof(DevChunk) == 32, "DevChunk layout");
 
@@ -78,6 +82,7 @@ struct DevPlan {
     int32_t* status;
     int32_t n_queries, n_q_heads, n_kv_heads, group, d, page_size;
     float scale_log2;  // log2(e) / sqrt(d)
+    int32_t p_bf16_min_tokens;  // tcgen05 PAC: single bf16 rounding of P from this chunk length
 };
 
 // Device status word codes (bit flags).
@@ -159,6 +164,9 @@ struct pst_plan {
     std::vector<int32_t> merge_ptr, merge_row;
     std::vector<pst::DevItem> items;   // tensor-core items first, then CUDA-core
     int64_t n_tc_items = 0, n_cc_items = 0;
+    // the last n_tc_exact tensor-core items split P into bf16 hi + lo (chunks
+    // shorter than opts.p_bf16_min_tokens); they run as their own launch
+    int64_t n_tc_exact = 0;
     // CUDA-core items grouped by row tile 8, 4, 2, 1: offsets into items[] and counts
     int64_t cc_class_off[4] = {0, 0, 0, 0}, cc_class_cnt[4] = {0, 0, 0, 0};
     int64_t n_part_rows = 0;
@@ -170,11 +178,12 @@ struct pst_plan {
     pst::WsLayout ws;
     std::vector<uint8_t> meta_blob;    // staged metadata image [0, meta_end)
     void* d_ws = nullptr;
-    // side stream and fork/join events (cudaStream_t / cudaEvent_t) used to run
-    // the CUDA-core PAC next to the tensor-core PAC; created on first use
-    mutable void* side_stream = nullptr;
+    // side streams and fork/join events (cudaStream_t / cudaEvent_t) that run
+    // the PAC launch groups (tensor-core, tensor-core exact-P, CUDA-core) side
+    // by side; created on first use
+    mutable void* side_stream[2] = {nullptr, nullptr};
     mutable void* ev_fork = nullptr;
-    mutable void* ev_join = nullptr;
+    mutable void* ev_join[2] = {nullptr, nullptr};
     // cached TMA descriptors (built on first decode for a pool pointer)
     mutable const void* tmap_k_ptr = nullptr;
     mutable const void* tmap_v_ptr = nullptr;

@@ -18,12 +18,10 @@
 
 namespace pst {
 
-cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const void* tv, const void* Q,
-                          int r_tile, int n_items, int item_off, cudaStream_t st);
-cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
-                          int item_off, cudaStream_t st);
-cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
-                            int item_off, cudaStream_t st);
+cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
+                            bool exact, cudaStream_t st);
+cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
+                            cudaStream_t st);
 cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, cudaStream_t st);
 int encode_pool_map(const pst_plan* p, const void* pool, unsigned char* out);
 DevPlan dev_plan_at(const pst_plan* p, void* ws);
@@ -90,14 +88,9 @@ extern "C" int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const v
     rc = encode_pool_map(p, V, tv);
     if (rc) return rc;
     const DevPlan dp = dev_plan_at(p, ws);
-    if (p->n_tc_items > 0) {
-        e = p->opts.tc_engine == 1 ? launch_pac_tc(dp, tk, tv, Q, (int)p->n_tc_items, 0, st)
-                                   : launch_pac_umma(dp, tk, tv, Q, (int)p->n_tc_items, 0, st);
-        if (e != cudaSuccess) return fail(PST_ECUDA, std::string("decode_attn_noalloc: PAC launch: ") + cudaGetErrorString(e));
-    }
-    for (int k = 0; k < 4; ++k) {
-        if (p->cc_class_cnt[k] == 0) continue;
-        e = launch_pac_cc(dp, p->dtype, tk, tv, Q, 8 >> k, (int)p->cc_class_cnt[k], (int)p->cc_class_off[k], st);
+    // the launch groups run one after the other on `stream`
+    for (int g = 0; g < 3; ++g) {
+        e = g < 2 ? launch_tc_group(p, dp, tk, tv, Q, g == 1, st) : launch_cc_group(p, dp, tk, tv, Q, st);
         if (e != cudaSuccess) return fail(PST_ECUDA, std::string("decode_attn_noalloc: PAC launch: ") + cudaGetErrorString(e));
     }
     e = launch_por(dp, O, LSE, st);

@@ -21,7 +21,7 @@ ERRORS = {-1: "PST_EINVAL", -2: "PST_ECYCLE", -3: "PST_ERANGE", -4: "PST_EUNSUPP
           -5: "PST_EWORKSPACE", -6: "PST_ECUDA", -7: "PST_EDEVICE", -8: "PST_ENOMEM"}
 DTYPES = {"bf16": 0, "f32": 1}
 SPLIT = {"cost_model": 0, "none": 1, "uniform": 2}
-KERNEL_SLOTS = 3
+KERNEL_SLOTS = 4
 
 
 class PstError(RuntimeError):
@@ -33,7 +33,7 @@ class PstError(RuntimeError):
 class PlanOpts(C.Structure):
     _fields_ = [("split_policy", C.c_int32), ("fixed_chunk", C.c_int32), ("tc_min_rows", C.c_int32),
                 ("pack_masks", C.c_int32), ("num_sms", C.c_int32), ("slots_per_sm", C.c_int32),
-                ("tc_engine", C.c_int32), ("tc_block_rows", C.c_int32)]
+                ("tc_engine", C.c_int32), ("tc_block_rows", C.c_int32), ("p_bf16_min_tokens", C.c_int32)]
 
 
 class PlanStats(C.Structure):
@@ -206,7 +206,8 @@ class Plan:
 def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int, dtype: str = "bf16",
                 split_policy: str = "cost_model", fixed_chunk: int | None = None,
                 tc_min_rows: int | None = None, pack_masks: bool | None = None, num_sms: int = 0,
-                slots_per_sm: int = 0, tc_engine: str = "tcgen05", tc_block_rows: int = 256) -> Plan:
+                slots_per_sm: int = 0, tc_engine: str = "tcgen05", tc_block_rows: int = 256,
+                p_bf16_min_tokens: int = 0) -> Plan:
     o = plan_opts_default()
     o.split_policy = SPLIT[split_policy]
     if fixed_chunk is not None:
@@ -219,6 +220,7 @@ def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int,
     o.slots_per_sm = slots_per_sm
     o.tc_engine = {"tcgen05": 0, "mma_sync": 1}[tc_engine]
     o.tc_block_rows = tc_block_rows
+    o.p_bf16_min_tokens = p_bf16_min_tokens
     qn, qnp = _arr(query_node, np.int32)
     h = C.c_void_p()
     _check(lib().pst_plan_create(tree._h, len(qn), qnp, n_q_heads, n_kv_heads, d, DTYPES[dtype],

@@ -133,3 +133,34 @@ def test_flat_control_matches_shared(lib):
     assert np.array_equal(Qf, Q)
     assert np.abs(Of - O).max() <= 2 * ABS_TOL and np.abs(Lf - L).max() <= 2 * LSE_TOL
     assert_matches(fl, Of, Lf, Kf, Vf, Qf, queries=[0, 31, 63])
+
+
+def _boosted_prefix(prefix, n_req, boost_from):
+    """A document-QA tree whose root tokens from `boost_from` on carry a large
+    key component that only the even-numbered queries see: their running max
+    jumps by ~33 (log2 units) in the middle of the root chunk while the odd
+    queries' does not, so the lazy O rescale runs on some rows of a warp and
+    not on the others."""
+    wl = synth.document_qa(prefix=prefix, n_req=n_req)
+    K, V = wl.kv_pools()
+    Q = wl.q()
+    lids = wl.row_lids().reshape(wl.num_pages, wl.page_size)
+    boosted = np.isin(lids, wl.lid[wl.lid_ptr[0] + boost_from:wl.lid_ptr[1]])
+    bf16_16 = 0x4180                       # 16.0 in bf16
+    k0 = K[..., 0]
+    k0[np.broadcast_to(boosted[:, None, :], k0.shape)] = bf16_16
+    Q[0::2, :, 0] = bf16_16                # score += 16 * 16 / sqrt(128) on boosted tokens
+    return wl, K, V, Q
+
+
+@pytest.mark.parametrize("prefix,n_req,boost,opts", [
+    (2048, 64, 1024, {"split_policy": "none"}),   # 256 rows in two halves, P rounded once
+    (2048, 16, 1024, {"split_policy": "none"}),   # 64 rows, alternate tiles per softmax group
+    (768, 64, 384, {"split_policy": "none"}),     # short chunk: P split into hi + lo
+    (2048, 64, 1024, {}),
+])
+def test_lazy_rescale_on_some_rows(lib, prefix, n_req, boost, opts):
+    wl, K, V, Q = _boosted_prefix(prefix, n_req, boost)
+    O, L, _, att = run_gpu(lib, wl, pools=(K, V), Q=Q, **opts)
+    assert att.plan.stats()["n_tc_items"] > 0
+    assert_matches(wl, O, L, K, V, Q, queries=range(0, n_req, 3))
