@@ -310,7 +310,11 @@ def run_ours(args, rank, world):
     # tensor-core chunks shorter than p_bf16_min_tokens run in the exact-P launch (tcgen05 engine)
     thr = int(plan_opts.get("p_bf16_min_tokens", 0)) or 1024
     thr = np.inf if thr < 0 else thr
-    exact = (kinds == 1) & (ntok < thr) & (plan_opts.get("tc_engine", "tcgen05") == "tcgen05")
+    tok_ptr = ex["chunk_tok_ptr"]
+    node_tokens = np.array([wl.node_len[ex["chunk_tok_node"][tok_ptr[c]:tok_ptr[c + 1]]].max()
+                            if len(set(ex["chunk_tok_node"][tok_ptr[c]:tok_ptr[c + 1]].tolist())) == 1 else 0
+                            for c in range(len(ntok))])
+    exact = (kinds == 1) & (node_tokens < thr) & (plan_opts.get("tc_engine", "tcgen05") == "tcgen05")
     alg = {"pac_tc": int(ntok[(kinds == 1) & ~exact].sum()) * per_tok,
            "pac_tc_exact": int(ntok[exact].sum()) * per_tok,
            "pac_cc": int(ntok[kinds == 0].sum()) * per_tok,

@@ -71,9 +71,10 @@ typedef struct {
                                1 legacy mma.sync (kept for comparison)               */
     int32_t tc_block_rows;  /* tcgen05 PAC rows per thread block: 256 (default; two
                                128-row halves share each K/V tile) or 128            */
-    int32_t p_bf16_min_tokens; /* tcgen05 PAC: chunks of at least this many tokens
-                               multiply V by the softmax weights P rounded once to
-                               bf16; shorter chunks split P into bf16 hi + lo parts,
+    int32_t p_bf16_min_tokens; /* tcgen05 PAC: chunks of nodes of at least this many
+                               tokens multiply V by the softmax weights P rounded
+                               once to bf16; chunks of shorter nodes (and packed
+                               draft subtrees) split P into bf16 hi + lo parts,
                                which keeps P V as accurate as an fp32 product.
                                0: default (1024); -1: always split               */
 } pst_plan_opts;

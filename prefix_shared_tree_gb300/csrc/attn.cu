@@ -25,7 +25,7 @@
 namespace pst {
 
 cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const void* tv, const void* Q,
-                          int r_tile, int n_items, int item_off, cudaStream_t st);
+                          int r_tile, int n_items, int item_off, int counter, cudaStream_t st);
 cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
                           int item_off, cudaStream_t st);
 cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
@@ -48,7 +48,7 @@ cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk
     for (int k = 0; k < 4; ++k) {
         if (p->cc_class_cnt[k] == 0) continue;
         cudaError_t e = launch_pac_cc(dp, p->dtype, tk, tv, Q, 8 >> k, (int)p->cc_class_cnt[k],
-                                      (int)p->cc_class_off[k], st);
+                                      (int)p->cc_class_off[k], k, st);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -61,6 +61,8 @@ constexpr int kPorWarps = 8;
 template <int D>
 __global__ void __launch_bounds__(kPorWarps * 32) por_kernel(DevPlan P, float* __restrict__ O, float* __restrict__ LSE) {
     constexpr int EPL = D / 32;
+    // every PAC launch of this call has finished: rearm their work queues
+    if (blockIdx.x == 0 && threadIdx.x < kNumCounters) P.counters[threadIdx.x] = 0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int64_t w = (int64_t)blockIdx.x * kPorWarps + warp;
     const int Hq = P.n_q_heads;
@@ -186,6 +188,7 @@ DevPlan dev_plan_at(const pst_plan* p, void* ws) {
     d.part_o = reinterpret_cast<float*>(b + p->ws.part_o);
     d.part_lse = reinterpret_cast<float*>(b + p->ws.part_lse);
     d.status = reinterpret_cast<int32_t*>(b + p->ws.status);
+    d.counters = d.status + 4;
     d.n_queries = p->n_queries;
     d.n_q_heads = p->hq;
     d.n_kv_heads = p->hkv;
@@ -193,7 +196,6 @@ DevPlan dev_plan_at(const pst_plan* p, void* ws) {
     d.d = p->d;
     d.page_size = p->page_size;
     d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->d));
-    d.p_bf16_min_tokens = p->opts.p_bf16_min_tokens < 0 ? INT32_MAX : p->opts.p_bf16_min_tokens;
     return d;
 }
 

@@ -140,19 +140,22 @@ __device__ __forceinline__ ChunkGeo chunk_geo(const DevChunk& c) {
 // TMA producer (one elected thread): streams every tile of the chunk through
 // a ring of `STAGES` stages. Stage s holds K then V, each NSLAB slabs of
 // kTileTokens rows x 128 bytes. Boxes entirely outside the chunk are skipped.
+// `tbase` tiles went through the ring before this chunk (stage and phase
+// continue from there).
 template <int NSLAB, int STAGES, int ELEMS_PER_SLAB>
 __device__ void produce_chunk(const DevPlan& P, const DevChunk& C, int head, uint32_t ring,
                               uint32_t bar_full, uint32_t bar_empty, const CUtensorMap* tk,
-                              const CUtensorMap* tv) {
+                              const CUtensorMap* tv, int tbase = 0) {
     constexpr uint32_t kSlabBytes = kTileTokens * 128;
     constexpr uint32_t kHalf = NSLAB * kSlabBytes;  // K (or V) part of a stage
     const ChunkGeo g = chunk_geo(C);
     const int ps = P.page_size;
     const int n_list = (g.pos_end - 1) / ps + 1;  // page list entries the chunk reaches
     for (int i = 0; i < g.n_tiles; ++i) {
-        const int s = i % STAGES;
-        if (i >= STAGES) {
-            if (!mbar_wait(bar_empty + 8 * s, ((i / STAGES) - 1) & 1, P.status)) return;
+        const int I = tbase + i;
+        const int s = I % STAGES;
+        if (I >= STAGES) {
+            if (!mbar_wait(bar_empty + 8 * s, ((I / STAGES) - 1) & 1, P.status)) return;
         }
         const int tpos = g.tile0 + i * kTileTokens;
         uint32_t nbox = 0;

@@ -17,6 +17,8 @@
 // the group with a transposing butterfly, so each lane ends up holding the
 // score of one row; every group keeps its own running (m, l, O) and the
 // groups, then the warps, are merged with the same rescaling rule at the end.
+#include <algorithm>
+
 #include "dev_common.cuh"
 
 namespace pst {
@@ -98,11 +100,12 @@ __device__ __forceinline__ constexpr int owner_shift() {
 }
 static_assert(owner_shift<8, 8>() == 0, "owner shift");
 
-// One chunk x kv head x row block on the compute warps.
+// One chunk x kv head x row block on the compute warps; `tbase` tiles went
+// through the ring before it. Returns false if a wait gave up.
 template <typename T, int D, int LPT, int RT>
-__device__ __forceinline__ void cc_consume(const DevPlan& P, const DevChunk& C, int head, int rb, const T* __restrict__ Q,
+__device__ __forceinline__ bool cc_consume(const DevPlan& P, const DevChunk& C, int head, int rb, const T* __restrict__ Q,
                            uint32_t ring, const uint8_t* ring_ptr, uint32_t bar_full, uint32_t bar_empty,
-                           float* scratch) {
+                           float* scratch, int tbase) {
     constexpr int EB = ElemTraits<T>::kBytes;
     constexpr int ROWB = D * EB;            // bytes per K/V row
     constexpr int NSLAB = ROWB / 128;
@@ -174,8 +177,8 @@ __device__ __forceinline__ void cc_consume(const DevPlan& P, const DevChunk& C, 
         }
     bool ok = true;
     for (int i = 0; i < g.n_tiles; ++i) {
-        const int s = i % kCcStages;
-        if (!mbar_wait(bar_full + 8 * s, (i / kCcStages) & 1, P.status)) { ok = false; break; }
+        const int s = (tbase + i) % kCcStages;
+        if (!mbar_wait(bar_full + 8 * s, ((tbase + i) / kCcStages) & 1, P.status)) { ok = false; break; }
         const uint8_t* kb = ring_ptr + s * 2 * kHalf;
         const uint8_t* vb = kb + kHalf;
         const int tpos = g.tile0 + i * kTileTokens;
@@ -303,8 +306,7 @@ __device__ __forceinline__ void cc_consume(const DevPlan& P, const DevChunk& C, 
         so[RT * D + RT + lane] = lr[lane];
     }
     asm volatile("bar.sync 1, %0;" ::"r"(kCcWarps * 32) : "memory");
-    if (!ok) return;
-    for (int r = warp; r < RT; r += kCcWarps) {
+    for (int r = warp; r < RT && ok; r += kCcWarps) {
         const int row = rb * RT + r;
         if (row >= rows_total) continue;
         float M = -INFINITY;
@@ -329,12 +331,19 @@ __device__ __forceinline__ void cc_consume(const DevPlan& P, const DevChunk& C, 
         }
         if (lane == 0) P.part_lse[prow] = L > 0.f ? M + __log2f(L) : -INFINITY;
     }
+    // the next item reuses the scratch
+    asm volatile("bar.sync 1, %0;" ::"r"(kCcWarps * 32) : "memory");
+    return ok;
 }
 
+// Persistent: each block takes items (largest first) from a work queue, so
+// blocks that start late, when tensor-core blocks leave their SMs, still
+// share the work evenly. The producer warp claims the next item and hands
+// its index to the compute warps through a 2-deep queue in shared memory.
 template <typename T, int D, int RT>
 __global__ void __launch_bounds__((kCcWarps + 1) * 32)
 pac_cc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-              const T* __restrict__ Q, int item_off) {
+              const T* __restrict__ Q, int item_off, int n_items, int counter) {
     constexpr int EB = ElemTraits<T>::kBytes;
     constexpr int NSLAB = D * EB / 128;
     constexpr uint32_t kStage = 2 * NSLAB * kTileTokens * 128;
@@ -344,23 +353,39 @@ pac_cc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
     float* scratch = reinterpret_cast<float*>(base + kCcStages * kStage);
     uint64_t* bars = reinterpret_cast<uint64_t*>(base + kCcStages * kStage + kCcWarps * RT * (D + 2) * 4);
     const uint32_t bar_full = smem_u32(bars), bar_empty = smem_u32(bars + kCcStages);
+    const uint32_t item_full = smem_u32(bars + 2 * kCcStages), item_empty = item_full + 16;
+    volatile int* item_idx = reinterpret_cast<volatile int*>(bars + 2 * kCcStages + 4);
 
-    const DevItem it = P.items[item_off + blockIdx.x];
-    const DevChunk C = P.chunks[it.chunk];
     if (threadIdx.x == 0) {
         for (int s = 0; s < kCcStages; ++s) {
             mbar_init(bar_full + 8 * s, 1);
             mbar_init(bar_empty + 8 * s, kCcWarps);
         }
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(item_full + 8 * q, 1);
+            mbar_init(item_empty + 8 * q, kCcWarps);
+        }
         fence_barrier_init();
     }
     __syncthreads();
-    const int warp = threadIdx.x / 32;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     if (warp == kCcWarps) {
-        if ((threadIdx.x & 31) == 0) {
+        if (lane == 0) {
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
-            produce_chunk<NSLAB, kCcStages, 128 / EB>(P, C, it.kv_head, ring, bar_full, bar_empty, &tk, &tv);
+            int tbase = 0;
+            for (int q = 0;; ++q) {
+                const int slot = q & 1;
+                if (q >= 2 && !mbar_wait(item_empty + 8 * slot, ((q >> 1) - 1) & 1, P.status)) break;
+                const int idx = atomicAdd(P.counters + counter, 1);
+                item_idx[slot] = idx < n_items ? idx : -1;
+                mbar_arrive(item_full + 8 * slot);   // release: the index store is visible to the waiters
+                if (idx >= n_items) break;
+                const DevItem it = P.items[item_off + idx];
+                const DevChunk C = P.chunks[it.chunk];
+                produce_chunk<NSLAB, kCcStages, 128 / EB>(P, C, it.kv_head, ring, bar_full, bar_empty, &tk, &tv, tbase);
+                tbase += chunk_geo(C).n_tiles;
+            }
         }
         return;
     }
@@ -369,53 +394,74 @@ pac_cc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
     constexpr int CH = D * EB / 16;
     constexpr int LW = RT == 1 ? 8 : RT <= 4 ? 16 : 32;
     constexpr int LPT = CH < LW ? CH : LW;
-    cc_consume<T, D, LPT, RT>(P, C, it.kv_head, it.row_block, Q, ring, base, bar_full, bar_empty, scratch);
+    int tbase = 0;
+    for (int q = 0;; ++q) {
+        const int slot = q & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(item_full + 8 * slot, (q >> 1) & 1, P.status))) break;
+        const int idx = item_idx[slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(item_empty + 8 * slot);
+        if (idx < 0) break;
+        const DevItem it = P.items[item_off + idx];
+        const DevChunk C = P.chunks[it.chunk];
+        if (!cc_consume<T, D, LPT, RT>(P, C, it.kv_head, it.row_block, Q, ring, base, bar_full, bar_empty, scratch,
+                                       tbase))
+            break;
+        tbase += chunk_geo(C).n_tiles;
+    }
 }
 
 template <typename T, int D, int RT>
 size_t cc_smem_bytes() {
     constexpr int EB = ElemTraits<T>::kBytes;
     constexpr int NSLAB = D * EB / 128;
-    return 1024 + kCcStages * 2 * NSLAB * kTileTokens * 128 + kCcWarps * RT * (D + 2) * 4 + 2 * kCcStages * 8;
+    return 1024 + kCcStages * 2 * NSLAB * kTileTokens * 128 + kCcWarps * RT * (D + 2) * 4 + 2 * kCcStages * 8 + 48;
 }
 
 template <typename T, int D, int RT>
 cudaError_t launch_cc_rt(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q,
-                         int n_items, int item_off, cudaStream_t st) {
+                         int n_items, int item_off, int counter, cudaStream_t st) {
     const size_t smem = cc_smem_bytes<T, D, RT>();
-    static bool attr_set = false;  // once per process (single device per process)
-    if (!attr_set) {
+    static int resident = 0;  // blocks that fit on the GPU at once (single device per process)
+    if (!resident) {
         cudaError_t e = cudaFuncSetAttribute(pac_cc_kernel<T, D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        int per_sm = 0, dev = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pac_cc_kernel<T, D, RT>, (kCcWarps + 1) * 32, smem);
+        if (e == cudaSuccess) e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        resident = std::max(1, per_sm) * std::max(1, sms);
     }
-    pac_cc_kernel<T, D, RT><<<n_items, (kCcWarps + 1) * 32, smem, st>>>(P, *tk, *tv, static_cast<const T*>(Q), item_off);
+    const int grid = std::min(n_items, resident);
+    pac_cc_kernel<T, D, RT><<<grid, (kCcWarps + 1) * 32, smem, st>>>(P, *tk, *tv, static_cast<const T*>(Q), item_off,
+                                                                    n_items, counter);
     return cudaGetLastError();
 }
 
 template <typename T, int D>
 cudaError_t launch_cc_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int r_tile,
-                        int n_items, int item_off, cudaStream_t st) {
+                        int n_items, int item_off, int counter, cudaStream_t st) {
     switch (r_tile) {
-        case 1: return launch_cc_rt<T, D, 1>(P, tk, tv, Q, n_items, item_off, st);
-        case 2: return launch_cc_rt<T, D, 2>(P, tk, tv, Q, n_items, item_off, st);
-        case 4: return launch_cc_rt<T, D, 4>(P, tk, tv, Q, n_items, item_off, st);
-        default: return launch_cc_rt<T, D, 8>(P, tk, tv, Q, n_items, item_off, st);
+        case 1: return launch_cc_rt<T, D, 1>(P, tk, tv, Q, n_items, item_off, counter, st);
+        case 2: return launch_cc_rt<T, D, 2>(P, tk, tv, Q, n_items, item_off, counter, st);
+        case 4: return launch_cc_rt<T, D, 4>(P, tk, tv, Q, n_items, item_off, counter, st);
+        default: return launch_cc_rt<T, D, 8>(P, tk, tv, Q, n_items, item_off, counter, st);
     }
 }
 
 }  // namespace dev
 
 cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const void* tv, const void* Q,
-                          int r_tile, int n_items, int item_off, cudaStream_t st) {
+                          int r_tile, int n_items, int item_off, int counter, cudaStream_t st) {
     const CUtensorMap* k = static_cast<const CUtensorMap*>(tk);
     const CUtensorMap* v = static_cast<const CUtensorMap*>(tv);
     if (dt == PST_BF16) {
-        if (P.d == 128) return dev::launch_cc_t<__nv_bfloat16, 128>(P, k, v, Q, r_tile, n_items, item_off, st);
-        return dev::launch_cc_t<__nv_bfloat16, 64>(P, k, v, Q, r_tile, n_items, item_off, st);
+        if (P.d == 128) return dev::launch_cc_t<__nv_bfloat16, 128>(P, k, v, Q, r_tile, n_items, item_off, counter, st);
+        return dev::launch_cc_t<__nv_bfloat16, 64>(P, k, v, Q, r_tile, n_items, item_off, counter, st);
     }
-    if (P.d == 128) return dev::launch_cc_t<float, 128>(P, k, v, Q, r_tile, n_items, item_off, st);
-    return dev::launch_cc_t<float, 64>(P, k, v, Q, r_tile, n_items, item_off, st);
+    if (P.d == 128) return dev::launch_cc_t<float, 128>(P, k, v, Q, r_tile, n_items, item_off, counter, st);
+    return dev::launch_cc_t<float, 64>(P, k, v, Q, r_tile, n_items, item_off, counter, st);
 }
 
 }  // namespace pst

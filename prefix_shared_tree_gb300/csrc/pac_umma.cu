@@ -34,10 +34,10 @@
 // Softmax works in the log2 domain with 1/sqrt(d) folded into one FMA; the
 // running max only moves (and O is rescaled in tensor memory) when it grows
 // by more than 2^8, so the result is exact in fp32. The EXACT instance (chunks
-// shorter than the plan's p_bf16_min_tokens) splits P into bf16 hi + lo parts
+// of nodes shorter than the plan's p_bf16_min_tokens) splits P into bf16 hi + lo parts
 // (p = hi + lo to ~2^-16), which makes P V as accurate as an fp32 product; the
 // other rounds P once to bf16, whose relative error (2^-8 per weight, random
-// in sign) averages out over a long chunk's many weights. Scores a row may
+// in sign) averages out over a long node's many weights. Scores a row may
 // not see (tile edges, bit causal masks) are set to -inf in tensor memory
 // before the row is loaded, which keeps masking out of the hot code.
 #include "dev_common.cuh"
@@ -62,8 +62,8 @@ struct UmmaLayout {
     static constexpr int NSLAB = D / 64;
     static constexpr uint32_t kSlab = kUT * 128;                   // 128 token rows x 128 B
     static constexpr uint32_t kOp = NSLAB * kSlab;                 // one K or V tile
-    static constexpr int KST = D == 128 ? 3 : 4;                   // K stages
-    static constexpr int VST = D == 128 ? 2 : 4;                   // V stages
+    static constexpr int KST = D == 128 ? 2 : 4;                   // K stages
+    static constexpr int VST = D == 128 ? 3 : 4;                   // V stages (a V stage is held longer)
     static constexpr uint32_t kQSlab = 128 * 128;                  // 128 rows x 128 B
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = kK + KST * kOp;

@@ -670,11 +670,13 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     }
     list_schedule(tc, m);
     list_schedule(cc, m);
-    // tcgen05: items whose chunk multiplies V by P rounded once to bf16 first,
-    // then the exact-P ones (a launch of their own)
+    // tcgen05: items that multiply V by P rounded once to bf16 first, then the
+    // exact-P ones (a launch of their own). The rounding errors of a node's
+    // chunks average out in POR like those inside one chunk, so the node's
+    // length decides.
     const int32_t p_single = o.p_bf16_min_tokens < 0 ? INT32_MAX : o.p_bf16_min_tokens;
     auto exact_item = [&](const ItemCost& it) {
-        return o.tc_engine == 0 && P->chunks[it.chunk].dev.n_tok < p_single;
+        return o.tc_engine == 0 && P->tasks[P->chunks[it.chunk].task].n_tok < p_single;
     };
     for (const auto& it : tc)
         if (!exact_item(it)) P->items.push_back({it.chunk, it.head, it.rb});

@@ -54,7 +54,7 @@ static_assert(sizeof(DevItem) == 8, "DevItem layout");
 
 // Byte offsets of the workspace sections (all 256-aligned).
 struct WsLayout {
-    int64_t status = 0;      // int32 device status word (+ padding)
+    int64_t status = 0;      // int32 device status word, then kNumCounters work counters
     int64_t items = 0;
     int64_t chunks = 0;
     int64_t pages = 0;
@@ -80,10 +80,13 @@ struct DevPlan {
     float* part_o;
     float* part_lse;
     int32_t* status;
+    int32_t* counters;  // work-queue counters of the persistent PAC launches (zeroed by POR)
     int32_t n_queries, n_q_heads, n_kv_heads, group, d, page_size;
     float scale_log2;  // log2(e) / sqrt(d)
-    int32_t p_bf16_min_tokens;  // tcgen05 PAC: single bf16 rounding of P from this chunk length
 };
+
+// Work-queue counters after the status word (one per persistent launch).
+constexpr int kNumCounters = 8;
 
 // Device status word codes (bit flags).
 enum : int32_t {
