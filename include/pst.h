@@ -281,11 +281,18 @@ int pst_plan_export_sizes(const pst_plan* p, pst_export_sizes* s);
 int pst_plan_export(const pst_plan* p, pst_export* e);
 
 /* Cost model C_est(rows, tokens) in microseconds for one PAC thread block
- * (CoDec "profile-based cost estimation"). pst_cost_set_table installs a
- * table measured on the device: n_r row grid points x n_n token grid points,
- * values row-major [n_r][n_n], kind 0 = CUDA-core PAC, 1 = tensor-core PAC;
- * between grid points the estimate is bilinear in (log rows, log tokens).
- * Process-wide; plans created afterwards use it. */
+ * with every SM busy (CoDec "profile-based cost estimation"), per PAC kind:
+ * 0 = CUDA-core PAC, 1 = tcgen05 PAC with P rounded once to bf16, 2 = tcgen05
+ * PAC with exact (hi + lo) P. Tables measured on a GB300 are built in (see
+ * the package's cost_fit.py); pst_cost_set_table replaces the table of one
+ * kind: n_r row grid points x n_n token grid points, values row-major
+ * [n_r][n_n]; n_r == 0 selects the analytic model for that kind and n_r < 0
+ * restores the built-in table. Between grid
+ * points the estimate is bilinear in (log rows, log tokens), past the last
+ * token point it grows linearly with tokens. The tables cover d = 128 bf16;
+ * other shapes and the mma.sync engine use the analytic model. Process-wide;
+ * plans created afterwards use it. pst_cost_estimate returns -1 for an
+ * unknown kind. */
 int pst_cost_set_table(int32_t kind, int32_t n_r, const float* rows, int32_t n_n,
                        const float* tokens, const float* us);
 double pst_cost_estimate(int32_t kind, double rows, double tokens);

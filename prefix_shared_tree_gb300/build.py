@@ -36,7 +36,7 @@ def _cuda_home() -> str:
 def _sources():
     cu = sorted(f for f in os.listdir(CSRC) if f.endswith(".cu"))
     cpp = sorted(f for f in os.listdir(CSRC) if f.endswith(".cpp"))
-    hdr = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    hdr = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh", ".inc"))]
     hdr.append(os.path.join(INCLUDE, "pst.h"))
     return cu, cpp, hdr
 

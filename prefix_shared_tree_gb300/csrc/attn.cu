@@ -69,34 +69,40 @@ __global__ void __launch_bounds__(kPorWarps * 32) por_kernel(DevPlan P, float* _
     if (w >= (int64_t)P.n_queries * Hq) return;
     const int q = (int)(w / Hq), h = (int)(w % Hq);
     const int e0 = P.merge_ptr[q], e1 = P.merge_ptr[q + 1];
-    // the query's partials, 32 at a time: lane i holds entry i's row and weight
-    float M = -INFINITY;
-    for (int e = e0 + lane; e < e1; e += 32) M = fmaxf(M, P.part_lse[P.merge_row[e] + h]);
-#pragma unroll
-    for (int off = 16; off; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float Mu = M == -INFINITY ? 0.f : M;
+    // One pass over the query's partials, 32 at a time: lane i holds entry
+    // i's row and log-sum-exp; the running max M rescales what was summed.
+    float M = -INFINITY, W = 0.f;
     float acc[EPL];
 #pragma unroll
     for (int k = 0; k < EPL; ++k) acc[k] = 0.f;
-    float W = 0.f;
     for (int b = e0; b < e1; b += 32) {
         const int cnt = min(32, e1 - b);
         int64_t my_row = 0;
-        float my_w = 0.f;
+        float my_lse = -INFINITY;
         if (lane < cnt) {
             my_row = (int64_t)P.merge_row[b + lane] + h;
-            my_w = fast_exp2(P.part_lse[my_row] - Mu);
+            my_lse = P.part_lse[my_row];
         }
+        float m = my_lse;
+#pragma unroll
+        for (int off = 16; off; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+        const float M2 = fmaxf(M, m);
+        const float Mu = M2 == -INFINITY ? 0.f : M2;
+        const float a = fast_exp2(M - Mu);   // rescales the earlier sum (0 when empty)
+        const float my_w = lane < cnt ? fast_exp2(my_lse - Mu) : 0.f;
         float ws = my_w;
 #pragma unroll
         for (int off = 16; off; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
-        W += ws;
-        // four partial rows in flight at a time
-        for (int i = 0; i < cnt; i += 4) {
-            float v[4][EPL];
-            float wt[4];
+        W = W * a + ws;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
+        for (int k = 0; k < EPL; ++k) acc[k] *= a;
+        M = M2;
+        // eight partial rows in flight at a time
+        for (int i = 0; i < cnt; i += 8) {
+            float v[8][EPL];
+            float wt[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
                 const int src_lane = min(i + u, cnt - 1);
                 const int64_t row = __shfl_sync(0xffffffffu, my_row, src_lane);
                 wt[u] = i + u < cnt ? __shfl_sync(0xffffffffu, my_w, src_lane) : 0.f;
@@ -110,7 +116,7 @@ __global__ void __launch_bounds__(kPorWarps * 32) por_kernel(DevPlan P, float* _
                 }
             }
 #pragma unroll
-            for (int u = 0; u < 4; ++u)
+            for (int u = 0; u < 8; ++u)
 #pragma unroll
                 for (int k = 0; k < EPL; ++k) acc[k] = fmaf(wt[u], v[u][k], acc[k]);
         }

@@ -32,15 +32,38 @@ int device_sm_count(int* out);  // attn.cu
 
 // ------------------------------------------------------------------ cost model
 // Profile-based estimator C_est(rows, tokens) (CoDec "profile-based cost
-// estimation"): a measured table per PAC kind, bilinear in (log rows, log
-// tokens); an analytic model stands in until a table is installed.
+// estimation"): a measured table per PAC kind (CUDA core, tensor core with P
+// rounded once, tensor core with exact P), bilinear in (log rows, log tokens)
+// and linear in tokens past the last grid point. The tables measured on a
+// GB300 are built in; an analytic model stands in for shapes they do not
+// cover (d != 128, fp32, the mma.sync engine).
 namespace {
 struct CostTable {
     bool set = false;
     std::vector<double> lr, ln, us;  // log rows, log tokens, values [n_r][n_n]
 };
 std::mutex g_cost_mu;
-CostTable g_cost[2];
+CostTable g_cost[kCostKinds];
+
+// The built-in tables (written by the package's cost_fit.py).
+#include "cost_table_gb300.inc"
+
+CostTable builtin_table(int k) {
+    CostTable T;
+    const BuiltinCostTable& b = kBuiltinCost[k];
+    if (b.n_r == 0) return T;
+    for (int i = 0; i < b.n_r; ++i) T.lr.push_back(std::log(b.rows[i]));
+    for (int j = 0; j < b.n_n; ++j) T.ln.push_back(std::log(b.tokens[j]));
+    T.us.assign(b.us, b.us + b.n_r * b.n_n);
+    T.set = true;
+    return T;
+}
+
+struct BuiltinInstaller {
+    BuiltinInstaller() {
+        for (int k = 0; k < kCostKinds; ++k) g_cost[k] = builtin_table(k);
+    }
+} g_builtin_installer;
 
 double interp(const std::vector<double>& g, double x, int* i0) {
     // returns the fractional position of x between g[i0] and g[i0+1], clamped
@@ -81,18 +104,21 @@ static double analytic_cost(int kind, double rows, double tokens, double bytes_p
 }
 
 double cost_estimate(int kind, double rows, double tokens) {
-    return analytic_cost(kind, rows, tokens, 512.0, 128, 152);
+    return analytic_cost(kind ? 1 : 0, rows, tokens, 512.0, 128, 152);
 }
 
+// kind: 0 CUDA core, 1 tensor core (P rounded once), 2 tensor core (exact P)
 static double cost_us(int kind, double rows, double tokens, double bytes_per_tok, int d,
                       int num_sms) {
     {
         std::lock_guard<std::mutex> lk(g_cost_mu);
-        const CostTable& T = g_cost[kind ? 1 : 0];
+        const CostTable& T = g_cost[kind];
         if (T.set && d == 128 && bytes_per_tok == 512.0) {
+            const double t_max = std::exp(T.ln.back());
+            const double scale = tokens > t_max ? tokens / t_max : 1.0;   // linear past the grid
             int i, j;
             double fr = interp(T.lr, std::log(std::max(1.0, rows)), &i);
-            double ft = interp(T.ln, std::log(std::max(1.0, tokens)), &j);
+            double ft = interp(T.ln, std::log(std::max(1.0, std::min(tokens, t_max))), &j);
             const int nn = (int)T.ln.size();
             auto at = [&](int a, int b) {
                 a = std::min(a, (int)T.lr.size() - 1);
@@ -101,10 +127,10 @@ static double cost_us(int kind, double rows, double tokens, double bytes_per_tok
             };
             double v0 = at(i, j) * (1 - ft) + at(i, j + 1) * ft;
             double v1 = at(i + 1, j) * (1 - ft) + at(i + 1, j + 1) * ft;
-            return v0 * (1 - fr) + v1 * fr;
+            return (v0 * (1 - fr) + v1 * fr) * scale;
         }
     }
-    return analytic_cost(kind, rows, tokens, bytes_per_tok, d, num_sms);
+    return analytic_cost(kind ? 1 : 0, rows, tokens, bytes_per_tok, d, num_sms);
 }
 
 }  // namespace pst
@@ -113,11 +139,15 @@ using namespace pst;
 
 extern "C" int pst_cost_set_table(int32_t kind, int32_t n_r, const float* rows, int32_t n_n,
                                   const float* tokens, const float* us) {
-    if (kind != 0 && kind != 1) return fail(PST_EINVAL, "cost_set_table: kind must be 0 or 1");
+    if (kind < 0 || kind >= kCostKinds) return fail(PST_EINVAL, "cost_set_table: kind must be 0, 1 or 2");
     std::lock_guard<std::mutex> lk(g_cost_mu);
     CostTable& T = g_cost[kind];
-    if (n_r <= 0 || n_n <= 0 || !rows || !tokens || !us) {
-        T = CostTable();  // clearing reverts to the analytic model
+    if (n_r < 0) {
+        T = builtin_table(kind);  // back to the built-in table
+        return PST_OK;
+    }
+    if (n_r == 0 || n_n <= 0 || !rows || !tokens || !us) {
+        T = CostTable();  // the analytic model
         return PST_OK;
     }
     CostTable nt;
@@ -138,7 +168,8 @@ extern "C" int pst_cost_set_table(int32_t kind, int32_t n_r, const float* rows, 
 }
 
 extern "C" double pst_cost_estimate(int32_t kind, double rows, double tokens) {
-    return cost_us(kind ? 1 : 0, rows, tokens, 512.0, 128, 152);
+    if (kind < 0 || kind >= kCostKinds) return -1.0;
+    return cost_us(kind, rows, tokens, 512.0, 128, 152);
 }
 
 extern "C" void pst_plan_opts_default(pst_plan_opts* o) {
@@ -231,8 +262,18 @@ struct Planner {
 
     Planner(const Tree& t, pst_plan& p) : T(t), P(p) {}
 
-    double item_cost(int kind, int rows_blk, int tokens) const {
-        return cost_us(kind, rows_blk, std::max(1, tokens), bytes_per_tok, P.d, num_sms);
+    // cost kind of a task: 0 CUDA core, 1 tensor core with P rounded once,
+    // 2 tensor core with exact P (a node shorter than p_bf16_min_tokens)
+    int cost_kind(const Task& t) const {
+        if (t.kind == 0) return 0;
+        const int32_t p_single = P.opts.p_bf16_min_tokens < 0 ? INT32_MAX : P.opts.p_bf16_min_tokens;
+        return t.n_tok < p_single ? 2 : 1;
+    }
+
+    double item_cost(const Task& t, int rows_blk, int tokens) const {
+        if (t.kind == 1 && P.opts.tc_engine == 1)   // the tables are for the tcgen05 engine
+            return analytic_cost(1, rows_blk, std::max(1, tokens), bytes_per_tok, P.d, num_sms);
+        return cost_us(cost_kind(t), rows_blk, std::max(1, tokens), bytes_per_tok, P.d, num_sms);
     }
 
     int rows_per_block(const Task& t) const {
@@ -251,7 +292,7 @@ struct Planner {
             if (t.node >= 0) chunk_range(s, b, k, &tb, &te);
             for (int rb = 0; rb < n_rb; ++rb) {
                 const int rows_blk = std::min(rpb, t.rows - rb * rpb);
-                const double c = item_cost(t.kind, rows_blk, te - tb);
+                const double c = item_cost(t, rows_blk, te - tb);
                 if (total) *total += c * P.hkv;
                 if (out)
                     for (int h = 0; h < P.hkv; ++h)
@@ -276,7 +317,7 @@ struct Planner {
         auto& tasks = P.tasks;
         const size_t nt = tasks.size();
         std::vector<double> c_full(nt);
-        for (size_t i = 0; i < nt; ++i) c_full[i] = item_cost(tasks[i].kind, rows_per_block(tasks[i]), tasks[i].n_tok);
+        for (size_t i = 0; i < nt; ++i) c_full[i] = item_cost(tasks[i], rows_per_block(tasks[i]), tasks[i].n_tok);
         auto b_of = [&](size_t i, double Tc, int cap) {
             if (Tc <= 0) return cap;
             int b = (int)std::ceil(c_full[i] / Tc - 1e-9);
@@ -291,7 +332,7 @@ struct Planner {
         double hi = 0, lo = 1e30;
         for (size_t i = 0; i < nt; ++i) {
             hi = std::max(hi, c_full[i]);
-            lo = std::min(lo, item_cost(tasks[i].kind, rows_per_block(tasks[i]), std::min(tasks[i].n_tok, kTileTokens)));
+            lo = std::min(lo, item_cost(tasks[i], rows_per_block(tasks[i]), std::min(tasks[i].n_tok, kTileTokens)));
         }
         double cost_l;
         const double avg_hi = avg_at(hi);
@@ -663,7 +704,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
         const int n_rb = (t.rows + rpb - 1) / rpb;
         for (int rb = 0; rb < n_rb; ++rb) {
             const int rows_blk = std::min(rpb, t.rows - rb * rpb);
-            const double cst = pl.item_cost(t.kind, rows_blk, c.dev.n_tok);
+            const double cst = pl.item_cost(t, rows_blk, c.dev.n_tok);
             for (int h = 0; h < n_kv_heads; ++h)
                 (t.kind == 1 ? tc : cc).push_back({cst, (int32_t)ci, (int16_t)h, (int16_t)rb});
         }

@@ -85,6 +85,10 @@ struct DevPlan {
     float scale_log2;  // log2(e) / sqrt(d)
 };
 
+// PAC kinds of the cost model: CUDA core, tensor core with P rounded once to
+// bf16, tensor core with exact (hi + lo) P.
+constexpr int kCostKinds = 3;
+
 // Work-queue counters after the status word (one per persistent launch).
 constexpr int kNumCounters = 8;
 

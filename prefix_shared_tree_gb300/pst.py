@@ -271,6 +271,12 @@ def decode_attn_timed(plan: Plan, q: int, k_pool: int, v_pool: int, o: int, lse:
 
 
 def cost_set_table(kind: int, rows, tokens, us):
+    """Install a measured table for PAC kind 0 (CUDA core), 1 (tcgen05, P
+    rounded once) or 2 (tcgen05, exact P); rows=None selects the analytic
+    model, rows="builtin" restores the built-in table."""
+    if isinstance(rows, str) and rows == "builtin":
+        _check(lib().pst_cost_set_table(kind, -1, None, 0, None, None))
+        return
     if rows is None:
         _check(lib().pst_cost_set_table(kind, 0, None, 0, None, None))
         return

@@ -191,6 +191,13 @@ def test_cost_table_interpolation(lib):
         assert abs(lib.cost_estimate(1, 4, 1024) - 3.0) < 1e-5
         mid = lib.cost_estimate(1, 8, 1024)       # halfway in log rows
         assert abs(mid - 3.5) < 1e-4
-        assert abs(lib.cost_estimate(1, 1000, 1e6) - 80) < 1e-4   # clamped
+        assert abs(lib.cost_estimate(1, 1000, 16384) - 80) < 1e-4     # rows clamped to the grid
+        assert abs(lib.cost_estimate(1, 256, 32768) - 160) < 1e-3     # linear in tokens past the grid
+        assert abs(lib.cost_estimate(1, 1, 10) - 1.0) < 1e-5          # clamped below the grid
+        lib.cost_set_table(2, rows, toks, us * 2)
+        assert abs(lib.cost_estimate(2, 16, 1024) - 8.0) < 1e-5       # kinds are independent
+        assert abs(lib.cost_estimate(1, 16, 1024) - 4.0) < 1e-5
+        assert lib.cost_estimate(3, 16, 1024) == -1.0
     finally:
-        lib.cost_set_table(1, None, None, None)
+        lib.cost_set_table(1, "builtin", None, None)
+        lib.cost_set_table(2, "builtin", None, None)
