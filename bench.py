@@ -206,6 +206,23 @@ print(json.dumps({{"queries": done, "seconds": el}}))
                       f"in {d['seconds']:.1f} s, scaled to the full batch"}
 
 
+def rotating_copies(U):
+    """Device copies of the inputs the timed loop rotates over (their total exceeds L2)."""
+    return max(2, math.ceil(3 * L2_BYTES / max(U, 1)))
+
+
+def bench_config(args, wl, world):
+    """The `config` object of a bench line (shared by both arms)."""
+    U = wl.unique_kv_bytes()
+    copies = rotating_copies(U)
+    return {
+        "workload": args.workload + (": " + DESCRIPTIONS[args.workload] if args.workload in DESCRIPTIONS else ""),
+        "n_queries": wl.n_queries, "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "d": wl.d,
+        "unique_kv_bytes": U, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
+        "l2": f"inputs rotate over {copies} device copies ({copies * U / 2**20:.0f} MiB > L2 129 MiB)",
+    }
+
+
 # ------------------------------------------------------------------ arms
 
 def run_ours(args, rank, world):
@@ -224,7 +241,7 @@ def run_ours(args, rank, world):
     K_np, V_np = wl.kv_pools()
     Q_np = wl.q()
     U = wl.unique_kv_bytes()
-    copies = max(2, math.ceil(3 * L2_BYTES / max(U, 1)))
+    copies = rotating_copies(U)
     Kd = [to_device(K_np, wl.dtype, dev)]
     Vd = [to_device(V_np, wl.dtype, dev)]
     Qd = [to_device(Q_np, wl.dtype, dev)]
@@ -340,12 +357,7 @@ def run_ours(args, rank, world):
         "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic (seeded N(0,1) K/V/Q, shapes of the CoDec/DEFT workloads)",
-        "config": {
-            "workload": args.workload + (": " + DESCRIPTIONS[args.workload] if args.workload in DESCRIPTIONS else ""),
-            "n_queries": wl.n_queries, "n_q_heads": wl.n_q_heads, "n_kv_heads": wl.n_kv_heads, "d": wl.d,
-            "unique_kv_bytes": U, "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-            "l2": f"inputs rotate over {copies} device copies ({copies * U / 2**20:.0f} MiB > L2 129 MiB)",
-        },
+        "config": bench_config(args, wl, world),
         "achieved_unique_kv_gbs": round(achieved_gbs, 1),
         "frac_of_8tbs": round(achieved_gbs / NOMINAL_HBM_GBS, 4),
         "frac_of_measured_hbm": round(achieved_gbs / peak, 4),
@@ -408,7 +420,7 @@ def run_reference(args, rank):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": args.workload, "unique_kv_bytes": wl.unique_kv_bytes()},
+        "config": bench_config(args, wl, 1),
         "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": ncpu, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
