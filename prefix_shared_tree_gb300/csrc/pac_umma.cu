@@ -18,13 +18,16 @@
 //               from one thread: S = Q K^T (M=128, N=128, Q and K from shared
 //               memory) and O += P V (M=128, N=d, P from tensor memory, V
 //               MN-major from shared memory);
-//   warps 4-11  two softmax warpgroups, one thread per row (tensor-memory
-//               lane). With more than 128 rows each group owns one 128-row
-//               half and both consume every tile; the MMA warp alternates
-//               between the halves so that one group's softmax overlaps the
-//               other half's MMAs. With at most 128 rows the groups take
-//               alternate tiles into separate O accumulators and merge them
-//               at the end (split-KV inside the block).
+//   warps 4-11  two softmax warpgroups, one thread per tensor-memory lane.
+//               With more than 128 rows the MMA warp alternates between the
+//               two 128-row halves (P V and S of half 0, then of half 1) and
+//               both groups work on each half as soon as its S is ready: group
+//               w takes S columns [64w, 64w + 64), the row max is the larger of
+//               the two groups' maxima (exchanged through shared memory), so a
+//               half's softmax takes half as long and overlaps the other
+//               half's MMAs. With at most 128 rows the groups take alternate
+//               tiles into separate S buffers and O accumulators and merge at
+//               the end (split-KV inside the block).
 // The first warpgroup hands registers to the softmax warpgroups
 // (setmaxnreg), which hold a whole 128-column row of S in registers.
 // Tensor memory: S of half w in columns [128w, 128w+128), O of half w in
@@ -63,15 +66,17 @@ struct UmmaLayout {
     static constexpr uint32_t kSlab = kUT * 128;                   // 128 token rows x 128 B
     static constexpr uint32_t kOp = NSLAB * kSlab;                 // one K or V tile
     static constexpr int KST = D == 128 ? 2 : 4;                   // K stages
-    static constexpr int VST = D == 128 ? 3 : 4;                   // V stages (a V stage is held longer)
+    static constexpr int VST = D == 128 ? 2 : 4;                   // V stages
     static constexpr uint32_t kQSlab = 128 * 128;                  // 128 rows x 128 B
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = kK + KST * kOp;
     static constexpr uint32_t kQ = kV + VST * kOp;                 // 2 halves x NSLAB slabs
     static constexpr uint32_t kXchg = kQ + 2 * NSLAB * kQSlab;     // 128 x (m, l) for the split-KV merge
-    static constexpr uint32_t kBars = kXchg + 128 * 8;
-    // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], q_ready, s_full[2], p_full[2], mma_done
-    static constexpr int kNumBars = 2 * KST + 2 * VST + 6;
+    static constexpr uint32_t kRed = kXchg + 128 * 8;              // [2][2][128] row maxima, then [2][128] sums
+    static constexpr uint32_t kBars = kRed + 768 * 4;
+    // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], q_ready, s_full[2], p_full[2], mma_done,
+    // xchg[2], lfin
+    static constexpr int kNumBars = 2 * KST + 2 * VST + 9;
     static constexpr uint32_t kBytes = kBars + 8 * kNumBars + 16;
     static_assert(kBytes + 1024 <= 232448, "shared memory");
     static constexpr uint32_t kTmemCols = 512;
@@ -82,6 +87,139 @@ struct UmmaLayout {
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ---- softmax pieces (one thread = one tensor-memory lane = one row)
+
+// NC columns of this lane from tensor memory into registers.
+template <int NC>
+__device__ __forceinline__ void ld_cols(uint32_t taddr, float (&x)[NC]) {
+#pragma unroll
+    for (int q = 0; q < NC / 32; ++q) {
+        float v[32];
+        umma::ld32(taddr + 32 * q, v);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) x[32 * q + c] = v[c];
+    }
+    umma::wait_ld();
+}
+
+// Max of NC values: four independent chains of three-input maxima.
+template <int NC>
+__device__ __forceinline__ float row_max(const float (&x)[NC]) {
+    float acc[4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) acc[a] = fmaxf(x[a], x[4 + a]);
+#pragma unroll
+    for (int c = 8; c < NC; c += 8) {
+#pragma unroll
+        for (int a = 0; a < 4; ++a) acc[a] = fmax3(acc[a], x[c + a], x[c + 4 + a]);
+    }
+    return fmaxf(fmax3(acc[0], acc[1], acc[2]), acc[3]);
+}
+
+// Scores this row may not see become -inf in tensor memory, 32 columns at a
+// time, over the NC columns starting at col0 of the tile. [c_lo, c_hi) is the
+// chunk's token range in tile columns; in a masked chunk, bit t of `mask` is
+// chunk token t.
+template <int NC>
+__device__ __forceinline__ void mask_in_tmem(uint32_t s_addr, int col0, int c_lo, int c_hi, uint64_t mask,
+                                             bool masked_chunk) {
+#pragma unroll 1
+    for (int c0 = col0; c0 < col0 + NC; c0 += 32) {
+        if (!masked_chunk && c0 >= c_lo && c0 + 32 <= c_hi) continue;
+        float v[32];
+        umma::ld32(s_addr + c0, v);
+        umma::wait_ld();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const int t = c0 + c - c_lo;   // token index in the chunk
+            const bool vis = t >= 0 && c0 + c < c_hi && (t >= kMaskTokens || ((mask >> (t & 63)) & 1ull));
+            v[c] = vis ? v[c] : -INFINITY;
+        }
+        umma::st32(s_addr + c0, v);
+    }
+    umma::wait_st();
+}
+
+// P = 2^(x*sl - m) for NC scores into tensor memory as bf16 pairs (P[2i],
+// P[2i+1] in one column): at p_hi, and with EXACT the remainder p - hi at
+// p_lo. Returns the row sum of the unrounded weights.
+template <int NC, bool EXACT>
+__device__ __forceinline__ float softmax_p(const float (&x)[NC], float sl, float nmu, uint32_t p_hi, uint32_t p_lo) {
+    const u64 sl2 = pk2(sl, sl), nmu2 = pk2(nmu, nmu);
+    u64 sum2[4] = {0ull, 0ull, 0ull, 0ull};   // independent add chains
+    if (!EXACT) {
+#pragma unroll
+        for (int q = 0; q < NC / 32; ++q) {
+            uint32_t hi[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                float a, b;
+                upk2(fma2(pk2(x[32 * q + 2 * c], x[32 * q + 2 * c + 1]), sl2, nmu2), a, b);
+                a = fast_exp2(a);
+                b = fast_exp2(b);
+                sum2[c & 3] = add2(sum2[c & 3], pk2(a, b));
+                hi[c] = bf16x2_bits(a, b);
+            }
+            umma::st16(p_hi + 16 * q, hi);
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < NC / 16; ++q) {
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                float a, b;
+                upk2(fma2(pk2(x[16 * q + 2 * c], x[16 * q + 2 * c + 1]), sl2, nmu2), a, b);
+                a = fast_exp2(a);
+                b = fast_exp2(b);
+                sum2[c & 3] = add2(sum2[c & 3], pk2(a, b));
+                hi[c] = bf16x2_bits(a, b);
+                lo[c] = bf16x2_bits(a - __uint_as_float(hi[c] << 16), b - __uint_as_float(hi[c] & 0xffff0000u));
+            }
+            umma::st8(p_hi + 8 * q, hi);
+            umma::st8(p_lo + 8 * q, lo);
+        }
+    }
+    float s0, s1;
+    upk2(add2(add2(sum2[0], sum2[1]), add2(sum2[2], sum2[3])), s0, s1);
+    return s0 + s1;
+}
+
+// O columns [taddr, taddr + NC) of this row *= alpha (whole warp).
+template <int NC>
+__device__ __forceinline__ void scale_o(uint32_t taddr, float alpha) {
+#pragma unroll 1
+    for (int c = 0; c < NC; c += 32) {
+        float o[32];
+        umma::ld32(taddr + c, o);
+        umma::wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+        umma::st32(taddr + c, o);
+    }
+}
+
+// V rows outside the chunk may hold stale or non-finite values: zero them
+// (thread r owns token row r of tile j) before P V multiplies them by P = 0.
+// False if the wait for the tile gave up.
+template <typename L>
+__device__ __forceinline__ bool zero_stray_v(const DevPlan& P, uint8_t* base, const ChunkGeo& geo, int tpos, int j, int r,
+                                             uint32_t v_full) {
+    const int s = j % L::VST;
+    if (!mbar_wait(v_full + 8 * s, (j / L::VST) & 1, P.status)) return false;
+    const int pos = tpos + r;
+    if (pos < geo.pos_begin || pos >= geo.pos_end) {
+#pragma unroll
+        for (int sl_i = 0; sl_i < L::NSLAB; ++sl_i) {
+            uint8_t* vrow = base + L::kV + s * L::kOp + sl_i * L::kSlab + r * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    fence_proxy_async_smem();   // zeroed V rows are read by the tensor core
+    return true;
 }
 
 template <int D, bool EXACT>
@@ -102,6 +240,8 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     const uint32_t s_full = q_ready + 8;      // [w]
     const uint32_t p_full = s_full + 16;      // [w]
     const uint32_t mma_done = p_full + 16;
+    const uint32_t xchg_bar = mma_done + 8;   // [half]: both groups' row maxima of a half are in
+    const uint32_t lfin_bar = xchg_bar + 16;  // both groups' row sums are in
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kBars + 8 * L::kNumBars);
     float2* xchg = reinterpret_cast<float2*>(base + L::kXchg);
 
@@ -127,9 +267,11 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         mbar_init(q_ready, 256);
         for (int w = 0; w < 2; ++w) {
             mbar_init(s_full + 8 * w, 1);
-            mbar_init(p_full + 8 * w, 128);
+            mbar_init(p_full + 8 * w, split_rows ? 256 : 128);   // both groups work on a half above 128 rows
+            mbar_init(xchg_bar + 8 * w, 256);
         }
         mbar_init(mma_done, 1);
+        mbar_init(lfin_bar, 256);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -282,171 +424,139 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
 
         const float sl = P.scale_log2;
         const bool masked_chunk = C.mask_base >= 0;
-        const bool zero_v = split_rows ? (w == 0) : true;   // one group zeroes a tile's stray V rows
-        float m_ref = -INFINITY, l = 0.f;                      // m_ref in scaled (log2) units
         bool ok = true;
-        const int nk = n_steps(w);
-        const uint32_t s_addr = lane_addr + L::colS(w);
-        for (int k = 0; k < nk; ++k) {
-            const int j = tile_of(w, k);
-            // tcgen05.ld/st are warp-collective: every decision that guards
-            // them is taken by the whole warp
-            if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * w, k & 1, P.status))) { ok = false; break; }
-            umma::fence_after_sync();
-            const int tpos = geo.tile0 + j * kUT;
-            const bool edge = tpos < geo.pos_begin || tpos + kUT > geo.pos_end;
-            if (edge || masked_chunk) {
-                // Scores this row may not see become -inf in tensor memory, in
-                // 32-column groups, so that the hot code below has no masking.
-                const int c_lo = geo.pos_begin - tpos, c_hi = geo.pos_end - tpos;
-#pragma unroll 1
-                for (int c0 = 0; c0 < kUT; c0 += 32) {
-                    if (!masked_chunk && c0 >= c_lo && c0 + 32 <= c_hi) continue;
-                    float v[32];
-                    umma::ld32(s_addr + c0, v);
-                    umma::wait_ld();
+        // the row this thread writes out: its running max (log2 units) and sum
+        float m_fin = -INFINITY, l_fin = 0.f;
+        int nk;   // steps this thread took part in
+        if (split_rows) {
+            // ---- more than 128 rows: both groups work on both row halves of
+            // every tile; group w owns S columns [64w, 64w + 64) of each half.
+            // The row max is the larger of the two groups' halves, exchanged
+            // through shared memory; one half's softmax then takes half the
+            // time and fits in the MMAs of the other half.
+            nk = n;
+            float* red = reinterpret_cast<float*>(base + L::kRed);   // [half][group][128]
+            float m_ref[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
+            uint64_t mask_h[2] = {~0ull, ~0ull};
+            if (masked_chunk) {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int t = c0 + c - c_lo;   // token index in the chunk
-                        const bool vis = t >= 0 && c0 + c < c_hi && (t >= kMaskTokens || ((mask >> (t & 63)) & 1ull));
-                        v[c] = vis ? v[c] : -INFINITY;
+                for (int h = 0; h < 2; ++h)
+                    if (128 * h + r < rows_here) mask_h[h] = P.masks[C.mask_base + (row0 + 128 * h + r) / G];
+            }
+            const int col0 = 64 * w;
+            for (int k = 0; k < n && ok; ++k) {
+                const int tpos = geo.tile0 + k * kUT;
+                const bool edge = tpos < geo.pos_begin || tpos + kUT > geo.pos_end;
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    // tcgen05.ld/st are warp-collective: every decision that
+                    // guards them is taken by the whole warp
+                    if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * h, k & 1, P.status))) { ok = false; break; }
+                    umma::fence_after_sync();
+                    const uint32_t s_addr = lane_addr + L::colS(h);
+                    if (edge || masked_chunk) mask_in_tmem<64>(s_addr, col0, geo.pos_begin - tpos, geo.pos_end - tpos,
+                                                              mask_h[h], masked_chunk);
+                    float x[64];
+                    ld_cols<64>(s_addr + col0, x);
+                    const float mxp = row_max(x);
+                    red[(2 * h + w) * 128 + r] = mxp;
+                    mbar_arrive(xchg_bar + 8 * h);
+                    if (!__all_sync(0xffffffffu, mbar_wait(xchg_bar + 8 * h, k & 1, P.status))) { ok = false; break; }
+                    const float mx = fmaxf(mxp, red[(2 * h + 1 - w) * 128 + r]);
+                    const float mxs = mx * sl;   // scale > 0: max commutes with it
+                    const bool grow = (m_ref[h] == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref[h] + kLazyRescale);
+                    float alpha = 1.f;
+                    bool rescale = false;
+                    if (grow) {
+                        alpha = fast_exp2(m_ref[h] - mxs);   // 0 when nothing was accumulated
+                        rescale = k >= 1 && m_ref[h] != -INFINITY;
+                        lsum[h] *= alpha;
+                        m_ref[h] = mxs;
                     }
-                    umma::st32(s_addr + c0, v);
+                    // both groups' S is in registers (exchange above): P may
+                    // now go anywhere in the half's columns
+                    lsum[h] += softmax_p<64, EXACT>(x, sl, m_ref[h] == -INFINITY ? 0.f : -m_ref[h], s_addr + 32 * w,
+                                                    s_addr + 64 + 32 * w);
+                    if (__any_sync(0xffffffffu, rescale))
+                        scale_o<D / 2>(lane_addr + L::colO(h) + (D / 2) * w, rescale ? alpha : 1.f);
+                    if (edge && w == 0 && h == 0) {
+                        if (!__all_sync(0xffffffffu, zero_stray_v<L>(P, base, geo, tpos, k, r, v_full))) { ok = false; break; }
+                    }
+                    umma::wait_st();
+                    umma::fence_before_sync();
+                    mbar_arrive(p_full + 8 * h);
+                }
+            }
+            // each group writes out one half: it needs the other group's sums
+            // of those rows (the K ring is free only later, so a small buffer)
+            float* lx = red + 512;   // [half][128]
+            lx[(1 - w) * 128 + r] = lsum[1 - w];
+            mbar_arrive(lfin_bar);
+            if (!__all_sync(0xffffffffu, mbar_wait(lfin_bar, 0, P.status))) ok = false;
+            m_fin = m_ref[w];
+            l_fin = lsum[w] + lx[w * 128 + r];
+        } else {
+            // ---- at most 128 rows: the groups take alternate tiles into their
+            // own S buffer and O accumulator (split-KV inside the block)
+            nk = n_steps(w);
+            float m_ref = -INFINITY, l = 0.f;
+            const uint32_t s_addr = lane_addr + L::colS(w);
+            for (int k = 0; k < nk; ++k) {
+                const int j = tile_of(w, k);
+                if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * w, k & 1, P.status))) { ok = false; break; }
+                umma::fence_after_sync();
+                const int tpos = geo.tile0 + j * kUT;
+                const bool edge = tpos < geo.pos_begin || tpos + kUT > geo.pos_end;
+                if (edge || masked_chunk) mask_in_tmem<kUT>(s_addr, 0, geo.pos_begin - tpos, geo.pos_end - tpos, mask,
+                                                           masked_chunk);
+                float x[kUT];
+                ld_cols<kUT>(s_addr, x);
+                const float mx = row_max(x);
+                const float mxs = mx * sl;
+                const bool grow = (m_ref == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref + kLazyRescale);
+                float alpha = 1.f;
+                bool rescale = false;
+                if (grow) {
+                    alpha = fast_exp2(m_ref - mxs);
+                    rescale = k >= 1 && m_ref != -INFINITY;
+                    l *= alpha;
+                    m_ref = mxs;
+                }
+                l += softmax_p<kUT, EXACT>(x, sl, m_ref == -INFINITY ? 0.f : -m_ref, s_addr, s_addr + 64);
+                if (__any_sync(0xffffffffu, rescale)) scale_o<D>(lane_addr + L::colO(w), rescale ? alpha : 1.f);
+                if (edge) {
+                    if (!__all_sync(0xffffffffu, zero_stray_v<L>(P, base, geo, tpos, j, r, v_full))) { ok = false; break; }
                 }
                 umma::wait_st();
+                umma::fence_before_sync();
+                mbar_arrive(p_full + 8 * w);
             }
-            float x[kUT];
-#pragma unroll
-            for (int q = 0; q < kUT / 32; ++q) {
-                float v[32];
-                umma::ld32(s_addr + 32 * q, v);
-#pragma unroll
-                for (int c = 0; c < 32; ++c) x[32 * q + c] = v[c];
-            }
-            umma::wait_ld();
-            // four independent chains of three-input maxima
-            float mx;
-            {
-                float acc[4];
-#pragma unroll
-                for (int a = 0; a < 4; ++a) acc[a] = fmaxf(x[a], x[4 + a]);
-#pragma unroll
-                for (int c = 8; c < kUT; c += 8) {
-#pragma unroll
-                    for (int a = 0; a < 4; ++a) acc[a] = fmax3(acc[a], x[c + a], x[c + 4 + a]);
-                }
-                mx = fmaxf(fmax3(acc[0], acc[1], acc[2]), acc[3]);
-            }
-            const float mxs = mx * sl;   // scale > 0: max commutes with it
-            const bool grow = (m_ref == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref + kLazyRescale);
-            float alpha = 1.f;
-            bool rescale = false;
-            if (grow) {
-                alpha = fast_exp2(m_ref - mxs);   // 0 when nothing was accumulated
-                rescale = k >= 1 && m_ref != -INFINITY;
-                l *= alpha;
-                m_ref = mxs;
-            }
-            const float nmu = m_ref == -INFINITY ? 0.f : -m_ref;
-            const u64 sl2 = pk2(sl, sl), nmu2 = pk2(nmu, nmu);
-            u64 sum2[4] = {0ull, 0ull, 0ull, 0ull};   // independent add chains
-            if (!EXACT) {
-#pragma unroll
-                for (int q = 0; q < kUT / 32; ++q) {
-                    uint32_t hi[16];
-#pragma unroll
-                    for (int c = 0; c < 16; ++c) {
-                        float a, b;
-                        upk2(fma2(pk2(x[32 * q + 2 * c], x[32 * q + 2 * c + 1]), sl2, nmu2), a, b);
-                        a = fast_exp2(a);
-                        b = fast_exp2(b);
-                        sum2[c & 3] = add2(sum2[c & 3], pk2(a, b));
-                        hi[c] = bf16x2_bits(a, b);
-                    }
-                    umma::st16(s_addr + 16 * q, hi);
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < kUT / 16; ++q) {
-                    uint32_t hi[8], lo[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        float a, b;
-                        upk2(fma2(pk2(x[16 * q + 2 * c], x[16 * q + 2 * c + 1]), sl2, nmu2), a, b);
-                        a = fast_exp2(a);
-                        b = fast_exp2(b);
-                        sum2[c & 3] = add2(sum2[c & 3], pk2(a, b));
-                        hi[c] = bf16x2_bits(a, b);
-                        lo[c] = bf16x2_bits(a - __uint_as_float(hi[c] << 16), b - __uint_as_float(hi[c] & 0xffff0000u));
-                    }
-                    umma::st8(s_addr + 8 * q, hi);
-                    umma::st8(s_addr + 64 + 8 * q, lo);
-                }
-            }
-            {
-                float s0, s1;
-                upk2(add2(add2(sum2[0], sum2[1]), add2(sum2[2], sum2[3])), s0, s1);
-                l += s0 + s1;
-            }
-            if (__any_sync(0xffffffffu, rescale)) {
-                // O of this group is stable between its S completing (every
-                // earlier MMA of the group had finished) and its p_full arrival.
-                if (!rescale) alpha = 1.f;
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[32];
-                    umma::ld32(lane_addr + L::colO(w) + 32 * c, o);
-                    umma::wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    umma::st32(lane_addr + L::colO(w) + 32 * c, o);
-                }
-            }
-            if (edge && zero_v) {
-                // V rows outside the chunk may hold stale or non-finite values:
-                // zero them before the PV of this tile multiplies them by P = 0.
-                const int s = j % VST;
-                if (!__all_sync(0xffffffffu, mbar_wait(v_full + 8 * s, (j / VST) & 1, P.status))) { ok = false; break; }
-                const int pos = tpos + r;                    // thread r owns token row r of the tile
-                if (pos < geo.pos_begin || pos >= geo.pos_end) {
-#pragma unroll
-                    for (int sl_i = 0; sl_i < NSLAB; ++sl_i) {
-                        uint8_t* vrow = base + L::kV + s * L::kOp + sl_i * L::kSlab + r * 128;
-#pragma unroll
-                        for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-                fence_proxy_async_smem();   // zeroed V rows are read by the tensor core
-            }
-            umma::wait_st();
-            umma::fence_before_sync();
-            mbar_arrive(p_full + 8 * w);
+            m_fin = m_ref;
+            l_fin = l;
         }
         // ---- epilogue: wait for the MMA warp's final commit (every MMA done)
         const bool have = __all_sync(0xffffffffu, ok && nk >= 1 && mbar_wait(mma_done, 0, P.status));
         if (have) umma::fence_after_sync();
+        float m1 = -INFINITY, l1 = 0.f;
         if (!split_rows) {
             // split-KV inside the block: group 1 hands (m, l) to group 0, which
             // reads both O accumulators (same lanes) and merges them
             if (w == 1) {
-                xchg[r] = make_float2(have ? m_ref : -INFINITY, have ? l : 0.f);
+                xchg[r] = make_float2(have ? m_fin : -INFINITY, have ? l_fin : 0.f);
                 asm volatile("bar.arrive 1, 256;" ::: "memory");
             } else {
                 asm volatile("bar.sync 1, 256;" ::: "memory");
-            }
-        }
-        if (have && (split_rows || w == 0)) {
-            float m1 = -INFINITY, l1 = 0.f;
-            if (!split_rows) {
                 const float2 ml = xchg[r];
                 m1 = ml.x;
                 l1 = ml.y;
             }
+        }
+        if (have && (split_rows || w == 0)) {
             const bool use1 = !split_rows && n >= 2;   // group 1's accumulator is complete (mma_done)
-            const float M = fmaxf(m_ref, m1);
+            const float M = fmaxf(m_fin, m1);
             const float Mu = M == -INFINITY ? 0.f : M;
-            const float a0 = fast_exp2(m_ref - Mu), a1 = fast_exp2(m1 - Mu);
-            const float Lt = l * a0 + l1 * a1;
+            const float a0 = fast_exp2(m_fin - Mu), a1 = fast_exp2(m1 - Mu);
+            const float Lt = l_fin * a0 + l1 * a1;
             const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
             const int64_t prow = (int64_t)C.part_base + (int64_t)qi * Hq + head * G + gh;
             // The warp's 32 rows go through shared memory (the K/V rings are
