@@ -11,7 +11,9 @@ them, times the PAC launch with the library's timer and reports
     C_est = (launch time) x (number of SMs) / (number of blocks),
 
 the time one block holds one of the planner's per-SM slots with every SM
-busy. Inputs are random bf16, d = 128, one KV head (blocks are per KV head).
+busy (CUDA-core blocks, several waves). Tensor-core blocks hold a whole SM;
+they are timed as one wave on two thirds of the SMs, where C_est is the launch
+time. Inputs are random bf16, d = 128, one KV head (blocks are per KV head).
 
 Writes ``cost_table_gb300.json`` and the C++ include ``cost_table_gb300.inc``
 that libpst compiles in as its built-in tables:
@@ -42,11 +44,15 @@ def measure_point(kind: int, rows: int, tokens: int, num_sms: int, seed: int, re
     from . import pst
     from .torch_api import TreeDecodeAttention
 
-    # blocks: a few waves, more when blocks are short so launch cost amortises
-    waves = 4 if kind == 0 else 2
-    n = waves * num_sms
-    n = max(n, min(16 * num_sms, (1 << 21) // max(tokens, 1)))
-    n = min(n, max(num_sms, (6 << 20) // tokens))        # <= ~3 GiB per pool
+    # CUDA-core blocks: a few waves, more when blocks are short so launch cost
+    # amortises. Tensor-core blocks (one per SM): a single wave on about two
+    # thirds of the SMs, the share they usually get beside CUDA-core work.
+    if kind == 0:
+        n = 4 * num_sms
+        n = max(n, min(16 * num_sms, (1 << 21) // max(tokens, 1)))
+        n = min(n, max(num_sms, (6 << 20) // tokens))    # <= ~3 GiB per pool
+    else:
+        n = (2 * num_sms) // 3
     pages_per_node = (tokens + PAGE - 1) // PAGE
     num_pages = n * pages_per_node
     rng = np.random.default_rng(seed)
@@ -82,8 +88,9 @@ def measure_point(kind: int, rows: int, tokens: int, num_sms: int, seed: int, re
     t_us = ms[SLOT[kind]] * 1e3 / calls
     del K, V, Q, O, L, att
     torch.cuda.empty_cache()
-    return {"kind": kind, "rows": rows, "tokens": tokens, "blocks": n, "launch_us": t_us,
-            "us": t_us * num_sms / n}
+    # per slot: a wave of n blocks on n SMs holds each for the launch time
+    per_slot = t_us * num_sms / n if kind == 0 else t_us
+    return {"kind": kind, "rows": rows, "tokens": tokens, "blocks": n, "launch_us": t_us, "us": per_slot}
 
 
 def write_inc(tables: dict, path: str, note: str):

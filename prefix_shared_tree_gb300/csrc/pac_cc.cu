@@ -418,25 +418,51 @@ size_t cc_smem_bytes() {
     return 1024 + kCcStages * 2 * NSLAB * kTileTokens * 128 + kCcWarps * RT * (D + 2) * 4 + 2 * kCcStages * 8 + 48;
 }
 
+// Blocks that fit on the GPU at once (single device per process); sets the
+// kernel's shared-memory limit on first use. 0 if the runtime cannot say.
+template <typename T, int D, int RT>
+int cc_resident_blocks(int* per_sm_out = nullptr) {
+    static int per_sm = 0, resident = 0;
+    if (!resident) {
+        const size_t smem = cc_smem_bytes<T, D, RT>();
+        if (cudaFuncSetAttribute(pac_cc_kernel<T, D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess)
+            return 0;
+        int n = 0, dev = 0, sms = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pac_cc_kernel<T, D, RT>, (kCcWarps + 1) * 32, smem) !=
+                cudaSuccess ||
+            cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        per_sm = std::max(1, n);
+        resident = per_sm * std::max(1, sms);
+    }
+    if (per_sm_out) *per_sm_out = per_sm;
+    return resident;
+}
+
 template <typename T, int D, int RT>
 cudaError_t launch_cc_rt(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q,
                          int n_items, int item_off, int counter, cudaStream_t st) {
     const size_t smem = cc_smem_bytes<T, D, RT>();
-    static int resident = 0;  // blocks that fit on the GPU at once (single device per process)
-    if (!resident) {
-        cudaError_t e = cudaFuncSetAttribute(pac_cc_kernel<T, D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        int per_sm = 0, dev = 0, sms = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, pac_cc_kernel<T, D, RT>, (kCcWarps + 1) * 32, smem);
-        if (e == cudaSuccess) e = cudaGetDevice(&dev);
-        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        resident = std::max(1, per_sm) * std::max(1, sms);
-    }
+    const int resident = cc_resident_blocks<T, D, RT>();
+    if (!resident) return cudaErrorInvalidConfiguration;
     const int grid = std::min(n_items, resident);
     pac_cc_kernel<T, D, RT><<<grid, (kCcWarps + 1) * 32, smem, st>>>(P, *tk, *tv, static_cast<const T*>(Q), item_off,
                                                                     n_items, counter);
     return cudaGetLastError();
+}
+
+template <typename T, int D>
+int cc_per_sm_t(int r_tile) {
+    int n = 0;
+    switch (r_tile) {
+        case 1: cc_resident_blocks<T, D, 1>(&n); break;
+        case 2: cc_resident_blocks<T, D, 2>(&n); break;
+        case 4: cc_resident_blocks<T, D, 4>(&n); break;
+        default: cc_resident_blocks<T, D, 8>(&n); break;
+    }
+    return n > 0 ? n : -1;
 }
 
 template <typename T, int D>
@@ -451,6 +477,16 @@ cudaError_t launch_cc_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorM
 }
 
 }  // namespace dev
+
+int cc_blocks_per_sm(pst_dtype dt, int d, int r_tile) {
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess || count == 0) {
+        cudaGetLastError();   // leave no sticky error behind
+        return -1;
+    }
+    if (dt == PST_BF16) return d == 128 ? dev::cc_per_sm_t<__nv_bfloat16, 128>(r_tile) : dev::cc_per_sm_t<__nv_bfloat16, 64>(r_tile);
+    return d == 128 ? dev::cc_per_sm_t<float, 128>(r_tile) : dev::cc_per_sm_t<float, 64>(r_tile);
+}
 
 cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const void* tv, const void* Q,
                           int r_tile, int n_items, int item_off, int counter, cudaStream_t st) {

@@ -227,6 +227,7 @@ struct ItemCost {
     double cost;
     int32_t chunk;
     int16_t head, rb;
+    int8_t klass;   // launch: 0 tensor core, 1 tensor core exact P, 2 + k CUDA core row tile 8 >> k
 };
 
 // Graham list scheduling (largest first) of item costs onto m slots: returns
@@ -252,13 +253,70 @@ double list_schedule(std::vector<ItemCost>& v, int m) {
     return mk;
 }
 
+// The block dispatcher's view of one decode call, used to score a partition:
+// the tensor-core launches come first and hold an SM per block (largest
+// first, the exact-P launch after the other); the CUDA-core launches run one
+// after the other on their own stream with `cc_per_sm[k]` blocks per SM, a
+// block taking cc_per_sm[k] x C_est of wall time (C_est is per-SM-slot
+// throughput), on the SMs the tensor-core blocks leave and, once those
+// retire, on theirs. Returns the time the last block ends.
+double simulate_call(std::vector<ItemCost> v, int num_sms, const int (&cc_per_sm)[4]) {
+    std::sort(v.begin(), v.end(), [](const ItemCost& a, const ItemCost& b) {
+        if (a.klass != b.klass) return a.klass < b.klass;
+        if (a.cost != b.cost) return a.cost > b.cost;
+        if (a.chunk != b.chunk) return a.chunk < b.chunk;
+        if (a.head != b.head) return a.head < b.head;
+        return a.rb < b.rb;
+    });
+    using Slot = std::pair<double, int>;
+    std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> sm;
+    for (int i = 0; i < num_sms; ++i) sm.push({0.0, i});
+    std::vector<double> sm_free(num_sms, 0.0);
+    size_t i = 0;
+    double end = 0;
+    for (; i < v.size() && v[i].klass < 2; ++i) {
+        Slot x = sm.top();
+        sm.pop();
+        x.first += v[i].cost;
+        sm_free[x.second] = x.first;
+        end = std::max(end, x.first);
+        sm.push(x);
+    }
+    double start = 0;   // a CUDA-core launch starts when the previous one has ended
+    while (i < v.size()) {
+        const int k = v[i].klass - 2;
+        const int per = std::max(1, cc_per_sm[k]);
+        std::priority_queue<double, std::vector<double>, std::greater<double>> slots;
+        for (int s2 = 0; s2 < num_sms; ++s2)
+            for (int b = 0; b < per; ++b) slots.push(std::max(start, sm_free[s2]));
+        double cls_end = start;
+        for (; i < v.size() && v[i].klass - 2 == k; ++i) {
+            double t = slots.top();
+            slots.pop();
+            t += per * v[i].cost;
+            cls_end = std::max(cls_end, t);
+            slots.push(t);
+        }
+        start = cls_end;
+        end = std::max(end, cls_end);
+    }
+    return end;
+}
+
 }  // namespace
+
+namespace pst {
+// CUDA-core PAC blocks that fit on one SM for a row tile (pac_cc.cu); -1 if
+// no device can be asked.
+int cc_blocks_per_sm(pst_dtype dt, int d, int r_tile);
+}  // namespace pst
 
 struct Planner {
     const Tree& T;
     pst_plan& P;
     int num_sms = 152;
     double bytes_per_tok = 0;
+    int cc_per_sm[4] = {1, 3, 3, 3};   // row tiles 8, 4, 2, 1
 
     Planner(const Tree& t, pst_plan& p) : T(t), P(p) {}
 
@@ -296,19 +354,27 @@ struct Planner {
                 if (total) *total += c * P.hkv;
                 if (out)
                     for (int h = 0; h < P.hkv; ++h)
-                        out->push_back({c, chunk_id_base + k, (int16_t)h, (int16_t)rb});
+                        out->push_back({c, chunk_id_base + k, (int16_t)h, (int16_t)rb, item_class(t)});
             }
         }
     }
 
     double makespan(const std::vector<int>& b, int m) const {
+        (void)m;
         std::vector<ItemCost> v;
         int cid = 0;
         for (size_t i = 0; i < P.tasks.size(); ++i) {
             task_items(P.tasks[i], b[i], &v, nullptr, cid);
             cid += b[i];
         }
-        return list_schedule(v, m);
+        return simulate_call(std::move(v), num_sms, cc_per_sm);
+    }
+
+    // launch class of a task's items (see ItemCost::klass)
+    int8_t item_class(const Task& t) const {
+        if (t.kind == 1) return (int8_t)((P.opts.tc_engine == 0 && cost_kind(t) == 2) ? 1 : 0);
+        const int rt = cc_row_tile(t.rows);
+        return (int8_t)(2 + (rt == 8 ? 0 : rt == 4 ? 1 : rt == 2 ? 2 : 3));
     }
 
     // CoDec's heuristic solver: binary search for cost_l, bound b_k, then a
@@ -605,6 +671,10 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
         pl.num_sms = sms;
     }
     pl.bytes_per_tok = 2.0 * d * (dtype == PST_BF16 ? 2 : 4);
+    for (int k = 0; k < 4; ++k) {
+        const int n = pst::cc_blocks_per_sm(dtype, d, 8 >> k);
+        if (n > 0) pl.cc_per_sm[k] = n;
+    }
     const int m = pl.num_sms * o.slots_per_sm;
     P->num_slots = m;
     if (o.split_policy == PST_SPLIT_NONE) {
@@ -706,7 +776,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
             const int rows_blk = std::min(rpb, t.rows - rb * rpb);
             const double cst = pl.item_cost(t, rows_blk, c.dev.n_tok);
             for (int h = 0; h < n_kv_heads; ++h)
-                (t.kind == 1 ? tc : cc).push_back({cst, (int32_t)ci, (int16_t)h, (int16_t)rb});
+                (t.kind == 1 ? tc : cc).push_back({cst, (int32_t)ci, (int16_t)h, (int16_t)rb, pl.item_class(t)});
         }
     }
     list_schedule(tc, m);
