@@ -12,6 +12,7 @@
 // (query, q-head) merges all of the query's partials at once.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <chrono>
 #include <cstdint>
 #include <cmath>
@@ -29,18 +30,19 @@ cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const 
 cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
                           int item_off, cudaStream_t st);
 cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
-                            int item_off, bool exact_p, cudaStream_t st);
+                            int item_off, bool exact_p, bool split_rows, cudaStream_t st);
 
-// Tensor-core PAC items of one launch group: those that round P once to bf16
-// (`exact` false; every item of the mma.sync engine) or the exact-P ones.
+// Tensor-core PAC launch group g (pst_plan::tc_group_cnt): P rounded once
+// (g < 2) or exact, more than 128 rows per block (even g) or at most 128.
+// The mma.sync engine has all its items in group 1.
 cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
-                            bool exact, cudaStream_t st) {
-    const int64_t n_fast = p->n_tc_items - p->n_tc_exact;
-    const int n = (int)(exact ? p->n_tc_exact : n_fast);
-    const int off = exact ? (int)n_fast : 0;
+                            int g, cudaStream_t st) {
+    int64_t off = 0;
+    for (int k = 0; k < g; ++k) off += p->tc_group_cnt[k];
+    const int n = (int)p->tc_group_cnt[g];
     if (n == 0) return cudaSuccess;
-    if (p->opts.tc_engine == 1) return launch_pac_tc(dp, tk, tv, Q, n, off, st);
-    return launch_pac_umma(dp, tk, tv, Q, n, off, exact, st);
+    if (p->opts.tc_engine == 1) return launch_pac_tc(dp, tk, tv, Q, n, (int)off, st);
+    return launch_pac_umma(dp, tk, tv, Q, n, (int)off, g >= 2, (g & 1) == 0, st);
 }
 
 cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
@@ -217,16 +219,16 @@ cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, cudaStream_t st)
 
 }  // namespace pst
 
-// Per recorded call, events: [0] start, [1] end of the tensor-core PAC,
-// [2] end of the exact-P tensor-core PAC, [3] end of the CUDA-core PAC (each on
-// the stream that ran it), [4] POR start (after the join), [5] POR end. The PAC
-// slots report time from the call's start to the end of their group (the
-// groups run side by side); the POR slot reports POR alone.
+// Per recorded call, events: [0] start, [1..5] end of each PAC launch group
+// (tensor core P once / two row-block modes, exact P / two modes, CUDA core;
+// each on the stream that ran it), [6] POR start (after the join), [7] POR
+// end. The PAC slots report time from the call's start to the end of their
+// groups (the groups run side by side); the POR slot reports POR alone.
 struct pst_timer {
     int32_t max_calls = 0;
     int32_t calls = 0;
     std::vector<cudaEvent_t> ev;         // max_calls x kEvents
-    static constexpr int kEvents = 6;
+    static constexpr int kEvents = 8;
 };
 
 using namespace pst;
@@ -275,15 +277,18 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
         cudaEventRecord(ev[0], st);
     }
     cudaError_t e;
-    // The three PAC launch groups write disjoint partial rows. The first
-    // non-empty one runs on `st`, the others on side streams forked from it,
-    // so their blocks fill the SMs the first group's blocks leave idle; POR
-    // waits on the joins.
-    const bool has[3] = {p->n_tc_items - p->n_tc_exact > 0, p->n_tc_exact > 0, p->n_cc_items > 0};
-    cudaStream_t gst[3] = {st, st, st};
+    // The PAC launch groups (four tensor-core ones, the CUDA-core one) write
+    // disjoint partial rows. The first non-empty one runs on `st`, the others
+    // on side streams forked from it, so their blocks fill the SMs the other
+    // groups' blocks leave idle; POR waits on the joins.
+    constexpr int kGroups = 5;
+    bool has[kGroups];
+    for (int g = 0; g < 4; ++g) has[g] = p->tc_group_cnt[g] > 0;
+    has[4] = p->n_cc_items > 0;
+    cudaStream_t gst[kGroups] = {st, st, st, st, st};
     int n_side = 0;
     bool first = true;
-    for (int g = 0; g < 3; ++g) {
+    for (int g = 0; g < kGroups; ++g) {
         if (!has[g]) continue;
         if (first) { first = false; continue; }
         if (!p->side_stream[n_side]) {
@@ -309,11 +314,11 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
         for (int k = 0; k < n_side; ++k)
             cudaStreamWaitEvent(static_cast<cudaStream_t>(p->side_stream[k]), static_cast<cudaEvent_t>(p->ev_fork), 0);
     }
-    for (int g = 0; g < 3; ++g) {
+    for (int g = 0; g < kGroups; ++g) {
         if (has[g]) {
-            e = g < 2 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g == 1, gst[g])
+            e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g, gst[g])
                       : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, gst[g]);
-            if (e != cudaSuccess) return cuda_fail(g < 2 ? "decode_attn: PAC (tensor core) launch"
+            if (e != cudaSuccess) return cuda_fail(g < 4 ? "decode_attn: PAC (tensor core) launch"
                                                          : "decode_attn: PAC (CUDA core) launch", e);
         }
         if (ev) cudaEventRecord(ev[1 + g], gst[g]);
@@ -322,11 +327,11 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
         cudaEventRecord(static_cast<cudaEvent_t>(p->ev_join[k]), static_cast<cudaStream_t>(p->side_stream[k]));
         cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(p->ev_join[k]), 0);
     }
-    if (ev) cudaEventRecord(ev[4], st);
+    if (ev) cudaEventRecord(ev[6], st);
     e = launch_por(dp, O, LSE, st);
     if (e != cudaSuccess) return cuda_fail("decode_attn: POR launch", e);
     if (ev) {
-        cudaEventRecord(ev[5], st);
+        cudaEventRecord(ev[7], st);
         timer->calls++;
     }
     return PST_OK;
@@ -334,7 +339,7 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
 
 namespace pst {
 void release_plan_streams(pst_plan* p) {
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < 4; ++k) {
         if (p->side_stream[k]) cudaStreamDestroy(static_cast<cudaStream_t>(p->side_stream[k]));
         if (p->ev_join[k]) cudaEventDestroy(static_cast<cudaEvent_t>(p->ev_join[k]));
         p->side_stream[k] = p->ev_join[k] = nullptr;
@@ -401,14 +406,16 @@ extern "C" int pst_timer_read(pst_timer* t, float* ms, int32_t n, int32_t* calls
         cudaError_t e = cudaEventSynchronize(t->ev[(size_t)(t->calls - 1) * stride + stride - 1]);
         if (e != cudaSuccess) return cuda_fail("timer_read: cudaEventSynchronize", e);
     }
-    // slot k: (from, to) events
-    static const int from[4] = {0, 0, 0, 4}, to[4] = {1, 2, 3, 5};
+    // slot k: from event, the later of two end events
+    static const int from[4] = {0, 0, 0, 6}, to_a[4] = {1, 3, 5, 7}, to_b[4] = {2, 4, 5, 7};
     for (int c = 0; c < t->calls; ++c) {
+        const cudaEvent_t* e0 = t->ev.data() + (size_t)c * stride;
         for (int k = 0; k < 4 && k < n; ++k) {
-            float x = 0.f;
-            cudaError_t e = cudaEventElapsedTime(&x, t->ev[(size_t)c * stride + from[k]], t->ev[(size_t)c * stride + to[k]]);
+            float xa = 0.f, xb = 0.f;
+            cudaError_t e = cudaEventElapsedTime(&xa, e0[from[k]], e0[to_a[k]]);
+            if (e == cudaSuccess) e = cudaEventElapsedTime(&xb, e0[from[k]], e0[to_b[k]]);
             if (e != cudaSuccess) return cuda_fail("timer_read: cudaEventElapsedTime", e);
-            ms[k] += x;
+            ms[k] += std::max(xa, xb);
         }
     }
     if (calls) *calls = t->calls;

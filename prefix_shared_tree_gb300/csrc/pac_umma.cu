@@ -49,14 +49,22 @@
 namespace pst {
 namespace dev {
 
-constexpr int kUWarps = 12;      // K producer, MMA, V producer, idle, 2 x 4 softmax warps
-constexpr int kUThreads = kUWarps * 32;
-// Registers per thread: at launch (the __launch_bounds__ cap for 384 threads),
-// then after setmaxnreg in the producer/MMA warpgroup and in the two softmax
-// warpgroups. The split must not exceed the launch total:
-// 128 * 104 + 256 * 200 == 384 * 168.
-constexpr int kURegsLaunch = 168, kURegsLow = 104, kURegsHigh = 200;
-static_assert(128 * kURegsLow + 256 * kURegsHigh <= kUThreads * kURegsLaunch, "register split");
+// Warps: the producer/MMA warpgroup (K producer, MMA, V producer, idle), then
+// the softmax warpgroups: four above 128 rows (each takes 32 columns of a row
+// half, so a half's softmax runs on four warps per scheduler), two at most.
+// Registers per thread: at launch (the __launch_bounds__ cap), then after
+// setmaxnreg in the producer/MMA warpgroup and in the softmax warpgroups; a
+// split never exceeds the launch total.
+template <bool SPLIT>
+struct UWarps {
+    static constexpr int kGroups = SPLIT ? 4 : 2;
+    static constexpr int kWarps = 4 + 4 * kGroups;
+    static constexpr int kThreads = kWarps * 32;
+    static constexpr int kRegsLaunch = SPLIT ? 96 : 168;
+    static constexpr int kRegsMma = SPLIT ? 160 : 104;       // producer/MMA warpgroup
+    static constexpr int kRegsSoftmax = SPLIT ? 80 : 200;    // each softmax warpgroup
+    static_assert(128 * kRegsMma + 128 * kGroups * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
+};
 constexpr int kUT = kTcTileTokens;   // tokens per tile
 constexpr float kLazyRescale = 8.f;
 
@@ -72,8 +80,8 @@ struct UmmaLayout {
     static constexpr uint32_t kV = kK + KST * kOp;
     static constexpr uint32_t kQ = kV + VST * kOp;                 // 2 halves x NSLAB slabs
     static constexpr uint32_t kXchg = kQ + 2 * NSLAB * kQSlab;     // 128 x (m, l) for the split-KV merge
-    static constexpr uint32_t kRed = kXchg + 128 * 8;              // [2][2][128] row maxima, then [2][128] sums
-    static constexpr uint32_t kBars = kRed + 768 * 4;
+    static constexpr uint32_t kRed = kXchg + 128 * 8;              // [2][4][128] row maxima, then [2][4][128] sums
+    static constexpr uint32_t kBars = kRed + 2048 * 4;
     // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], q_ready, s_full[2], p_full[2], mma_done,
     // xchg[2], lfin
     static constexpr int kNumBars = 2 * KST + 2 * VST + 9;
@@ -190,14 +198,27 @@ __device__ __forceinline__ float softmax_p(const float (&x)[NC], float sl, float
 // O columns [taddr, taddr + NC) of this row *= alpha (whole warp).
 template <int NC>
 __device__ __forceinline__ void scale_o(uint32_t taddr, float alpha) {
+    static_assert(NC % 16 == 0, "O column block");
+    if constexpr (NC % 32 == 0) {
 #pragma unroll 1
-    for (int c = 0; c < NC; c += 32) {
-        float o[32];
-        umma::ld32(taddr + c, o);
-        umma::wait_ld();
+        for (int c = 0; c < NC; c += 32) {
+            float o[32];
+            umma::ld32(taddr + c, o);
+            umma::wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-        umma::st32(taddr + c, o);
+            for (int i = 0; i < 32; ++i) o[i] *= alpha;
+            umma::st32(taddr + c, o);
+        }
+    } else {
+#pragma unroll 1
+        for (int c = 0; c < NC; c += 16) {
+            uint32_t o[16];
+            umma::ld16(taddr + c, o);
+            umma::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            umma::st16(taddr + c, o);
+        }
     }
 }
 
@@ -222,8 +243,8 @@ __device__ __forceinline__ bool zero_stray_v(const DevPlan& P, uint8_t* base, co
     return true;
 }
 
-template <int D, bool EXACT>
-__global__ void __launch_bounds__(kUThreads, 1)
+template <int D, bool EXACT, bool SPLIT>
+__global__ void __launch_bounds__(UWarps<SPLIT>::kThreads, 1)
 pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                 const __nv_bfloat16* __restrict__ Q, int item_off) {
     using L = UmmaLayout<D>;
@@ -253,7 +274,14 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     const int rows_total = C.n_q * G;
     const int row0 = rb * C.r_tile;                 // C.r_tile: 256 or 128 rows per block
     const int rows_here = min(C.r_tile, rows_total - row0);
-    const bool split_rows = rows_here > 128;   // mode A: groups own row halves; else alternate tiles
+    // SPLIT instance: more than 128 rows in the block (both groups on both row
+    // halves); otherwise the groups alternate tiles. The plan launches each
+    // item with the instance its row count needs.
+    constexpr bool split_rows = SPLIT;
+    if ((rows_here > 128) != SPLIT) {
+        if (threadIdx.x == 0) atomicOr(P.status, kStatusBadIndex);
+        return;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < KST; ++s) {
@@ -264,14 +292,15 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             mbar_init(v_full + 8 * s, 1);
             mbar_init(v_empty + 8 * s, 1);
         }
-        mbar_init(q_ready, 256);
+        mbar_init(q_ready, 128 * UWarps<SPLIT>::kGroups);
         for (int w = 0; w < 2; ++w) {
             mbar_init(s_full + 8 * w, 1);
-            mbar_init(p_full + 8 * w, split_rows ? 256 : 128);   // both groups work on a half above 128 rows
-            mbar_init(xchg_bar + 8 * w, 256);
+            // above 128 rows every group works on each half
+            mbar_init(p_full + 8 * w, split_rows ? 128 * UWarps<SPLIT>::kGroups : 128);
+            mbar_init(xchg_bar + 8 * w, 128 * UWarps<SPLIT>::kGroups);
         }
         mbar_init(mma_done, 1);
-        mbar_init(lfin_bar, 256);
+        mbar_init(lfin_bar, 128 * UWarps<SPLIT>::kGroups);
         fence_barrier_init();
     }
     if (warp == 1) {
@@ -289,7 +318,10 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     auto tile_of = [&](int w, int k) { return split_rows ? k : 2 * k + w; };
 
     if (warp < 4) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kURegsLow));
+        if (UWarps<SPLIT>::kRegsMma < UWarps<SPLIT>::kRegsLaunch)
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(UWarps<SPLIT>::kRegsMma));
+        else
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(UWarps<SPLIT>::kRegsMma));
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------------------ TMA producers
         // warp 0 streams K, warp 2 streams V, each at its own pace (two lanes
@@ -390,12 +422,17 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         }
     }
     } else {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kURegsHigh));
+        if (UWarps<SPLIT>::kRegsSoftmax > UWarps<SPLIT>::kRegsLaunch)
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(UWarps<SPLIT>::kRegsSoftmax));
+        else
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(UWarps<SPLIT>::kRegsSoftmax));
         // ------------------------------------------------------------ softmax warpgroups
-        const int w = (warp - 4) / 4;                // group 0: warps 4-7, group 1: warps 8-11
+        constexpr int NG = UWarps<SPLIT>::kGroups;
+        const int w = (warp - 4) / 4;                // group w: warps 4 + 4w .. 7 + 4w
         const int r = 32 * (warp % 4) + lane;        // tensor-memory lane = row within the half
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * (warp % 4)) << 16);
-        const int rloc = split_rows ? 128 * w + r : r;   // row within the block
+        // above 128 rows, groups 0 and 1 write out (and stage Q for) row halves 0 and 1
+        const int rloc = split_rows ? 128 * (w & 1) + r : r;   // row within the block
         const bool row_ok = rloc < rows_here;
         int qi = 0, gh = 0;
         uint64_t mask = ~0ull;
@@ -404,7 +441,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             gh = (row0 + rloc) % G;
             if (C.mask_base >= 0) mask = P.masks[C.mask_base + qi];
         }
-        if (split_rows || w == 0) {
+        if (split_rows ? w < 2 : w == 0) {
             uint8_t* qdst = base + L::kQ + (split_rows ? w : 0) * NSLAB * L::kQSlab;
             if (row_ok) {
                 const int qid = P.chunk_q[C.q_base + qi];
@@ -428,12 +465,13 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         // the row this thread writes out: its running max (log2 units) and sum
         float m_fin = -INFINITY, l_fin = 0.f;
         int nk;   // steps this thread took part in
-        if (split_rows) {
-            // ---- more than 128 rows: both groups work on both row halves of
-            // every tile; group w owns S columns [64w, 64w + 64) of each half.
-            // The row max is the larger of the two groups' halves, exchanged
-            // through shared memory; one half's softmax then takes half the
-            // time and fits in the MMAs of the other half.
+        if constexpr (SPLIT) {
+            // ---- more than 128 rows: every group works on both row halves of
+            // every tile; group w owns S columns [kCols w, kCols (w + 1)) of
+            // each half. The row max is the largest of the groups' maxima,
+            // exchanged through shared memory; a half's softmax then runs on
+            // all groups and overlaps the MMAs of the other half.
+            constexpr int kCols = 128 / NG;
             nk = n;
             float* red = reinterpret_cast<float*>(base + L::kRed);   // [half][group][128]
             float m_ref[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
@@ -443,7 +481,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 for (int h = 0; h < 2; ++h)
                     if (128 * h + r < rows_here) mask_h[h] = P.masks[C.mask_base + (row0 + 128 * h + r) / G];
             }
-            const int col0 = 64 * w;
+            const int col0 = kCols * w;
             for (int k = 0; k < n && ok; ++k) {
                 const int tpos = geo.tile0 + k * kUT;
                 const bool edge = tpos < geo.pos_begin || tpos + kUT > geo.pos_end;
@@ -454,15 +492,16 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                     if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * h, k & 1, P.status))) { ok = false; break; }
                     umma::fence_after_sync();
                     const uint32_t s_addr = lane_addr + L::colS(h);
-                    if (edge || masked_chunk) mask_in_tmem<64>(s_addr, col0, geo.pos_begin - tpos, geo.pos_end - tpos,
-                                                              mask_h[h], masked_chunk);
-                    float x[64];
-                    ld_cols<64>(s_addr + col0, x);
-                    const float mxp = row_max(x);
-                    red[(2 * h + w) * 128 + r] = mxp;
+                    if (edge || masked_chunk) mask_in_tmem<kCols>(s_addr, col0, geo.pos_begin - tpos,
+                                                                 geo.pos_end - tpos, mask_h[h], masked_chunk);
+                    float x[kCols];
+                    ld_cols<kCols>(s_addr + col0, x);
+                    red[(NG * h + w) * 128 + r] = row_max(x);
                     mbar_arrive(xchg_bar + 8 * h);
                     if (!__all_sync(0xffffffffu, mbar_wait(xchg_bar + 8 * h, k & 1, P.status))) { ok = false; break; }
-                    const float mx = fmaxf(mxp, red[(2 * h + 1 - w) * 128 + r]);
+                    float mx = red[(NG * h) * 128 + r];
+#pragma unroll
+                    for (int g = 1; g < NG; ++g) mx = fmaxf(mx, red[(NG * h + g) * 128 + r]);
                     const float mxs = mx * sl;   // scale > 0: max commutes with it
                     const bool grow = (m_ref[h] == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref[h] + kLazyRescale);
                     float alpha = 1.f;
@@ -473,12 +512,12 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                         lsum[h] *= alpha;
                         m_ref[h] = mxs;
                     }
-                    // both groups' S is in registers (exchange above): P may
+                    // every group's S is in registers (exchange above): P may
                     // now go anywhere in the half's columns
-                    lsum[h] += softmax_p<64, EXACT>(x, sl, m_ref[h] == -INFINITY ? 0.f : -m_ref[h], s_addr + 32 * w,
-                                                    s_addr + 64 + 32 * w);
+                    lsum[h] += softmax_p<kCols, EXACT>(x, sl, m_ref[h] == -INFINITY ? 0.f : -m_ref[h],
+                                                       s_addr + (kCols / 2) * w, s_addr + 64 + (kCols / 2) * w);
                     if (__any_sync(0xffffffffu, rescale))
-                        scale_o<D / 2>(lane_addr + L::colO(h) + (D / 2) * w, rescale ? alpha : 1.f);
+                        scale_o<D / NG>(lane_addr + L::colO(h) + (D / NG) * w, rescale ? alpha : 1.f);
                     if (edge && w == 0 && h == 0) {
                         if (!__all_sync(0xffffffffu, zero_stray_v<L>(P, base, geo, tpos, k, r, v_full))) { ok = false; break; }
                     }
@@ -487,14 +526,19 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                     mbar_arrive(p_full + 8 * h);
                 }
             }
-            // each group writes out one half: it needs the other group's sums
-            // of those rows (the K ring is free only later, so a small buffer)
-            float* lx = red + 512;   // [half][128]
-            lx[(1 - w) * 128 + r] = lsum[1 - w];
+            // groups 0 and 1 write out halves 0 and 1 and need every group's
+            // sums of their rows (the K ring is free only later)
+            float* lx = red + 2 * NG * 128;   // [half][group][128]
+            lx[w * 128 + r] = lsum[0];
+            lx[(NG + w) * 128 + r] = lsum[1];
             mbar_arrive(lfin_bar);
             if (!__all_sync(0xffffffffu, mbar_wait(lfin_bar, 0, P.status))) ok = false;
-            m_fin = m_ref[w];
-            l_fin = lsum[w] + lx[w * 128 + r];
+            if (w < 2) {
+                m_fin = m_ref[w];
+                l_fin = 0.f;
+#pragma unroll
+                for (int g = 0; g < NG; ++g) l_fin += lx[(NG * w + g) * 128 + r];
+            }
         } else {
             // ---- at most 128 rows: the groups take alternate tiles into their
             // own S buffer and O accumulator (split-KV inside the block)
@@ -551,7 +595,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 l1 = ml.y;
             }
         }
-        if (have && (split_rows || w == 0)) {
+        if (have && (split_rows ? w < 2 : w == 0)) {
             const bool use1 = !split_rows && n >= 2;   // group 1's accumulator is complete (mma_done)
             const float M = fmaxf(m_fin, m1);
             const float Mu = M == -INFINITY ? 0.f : M;
@@ -609,38 +653,46 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     }
 }
 
-template <int D, bool EXACT>
+template <int D, bool EXACT, bool SPLIT>
 cudaError_t launch_umma_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
                           int item_off, cudaStream_t st) {
     const size_t smem = 1024 + UmmaLayout<D>::kBytes;
     static bool attr_set = false;  // once per process (single device per process)
     if (!attr_set) {
-        // setmaxnreg.inc waits for registers the other warpgroup released: the
+        // setmaxnreg.inc waits for registers another warpgroup released: the
         // split is only valid for the launch register count it was sized for
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, pac_umma_kernel<D, EXACT>);
+        cudaError_t e = cudaFuncGetAttributes(&fa, pac_umma_kernel<D, EXACT, SPLIT>);
         if (e != cudaSuccess) return e;
-        if (fa.numRegs != kURegsLaunch) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(pac_umma_kernel<D, EXACT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (fa.numRegs != UWarps<SPLIT>::kRegsLaunch) return cudaErrorInvalidConfiguration;
+        e = cudaFuncSetAttribute(pac_umma_kernel<D, EXACT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    pac_umma_kernel<D, EXACT><<<n_items, kUThreads, smem, st>>>(P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q),
-                                                                item_off);
+    pac_umma_kernel<D, EXACT, SPLIT><<<n_items, UWarps<SPLIT>::kThreads, smem, st>>>(P, *tk, *tv,
+                                                                       static_cast<const __nv_bfloat16*>(Q), item_off);
     return cudaGetLastError();
+}
+
+template <int D, bool EXACT>
+cudaError_t launch_umma_m(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
+                          int item_off, bool split_rows, cudaStream_t st) {
+    return split_rows ? launch_umma_t<D, EXACT, true>(P, tk, tv, Q, n_items, item_off, st)
+                      : launch_umma_t<D, EXACT, false>(P, tk, tv, Q, n_items, item_off, st);
 }
 
 }  // namespace dev
 
 cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items, int item_off,
-                            bool exact_p, cudaStream_t st) {
+                            bool exact_p, bool split_rows, cudaStream_t st) {
     const CUtensorMap* k = static_cast<const CUtensorMap*>(tk);
     const CUtensorMap* v = static_cast<const CUtensorMap*>(tv);
     if (P.d == 128)
-        return exact_p ? dev::launch_umma_t<128, true>(P, k, v, Q, n_items, item_off, st)
-                       : dev::launch_umma_t<128, false>(P, k, v, Q, n_items, item_off, st);
-    return exact_p ? dev::launch_umma_t<64, true>(P, k, v, Q, n_items, item_off, st)
-                   : dev::launch_umma_t<64, false>(P, k, v, Q, n_items, item_off, st);
+        return exact_p ? dev::launch_umma_m<128, true>(P, k, v, Q, n_items, item_off, split_rows, st)
+                       : dev::launch_umma_m<128, false>(P, k, v, Q, n_items, item_off, split_rows, st);
+    return exact_p ? dev::launch_umma_m<64, true>(P, k, v, Q, n_items, item_off, split_rows, st)
+                   : dev::launch_umma_m<64, false>(P, k, v, Q, n_items, item_off, split_rows, st);
 }
 
 }  // namespace pst

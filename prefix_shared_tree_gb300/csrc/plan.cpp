@@ -781,20 +781,25 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     }
     list_schedule(tc, m);
     list_schedule(cc, m);
-    // tcgen05: items that multiply V by P rounded once to bf16 first, then the
-    // exact-P ones (a launch of their own). The rounding errors of a node's
-    // chunks average out in POR like those inside one chunk, so the node's
-    // length decides.
+    // tensor-core launch groups (see pst_plan::tc_group_cnt): precision, then
+    // row-block mode. The rounding errors of a node's chunks average out in
+    // POR like those inside one chunk, so the node's length decides the
+    // precision.
     const int32_t p_single = o.p_bf16_min_tokens < 0 ? INT32_MAX : o.p_bf16_min_tokens;
-    auto exact_item = [&](const ItemCost& it) {
-        return o.tc_engine == 0 && P->tasks[P->chunks[it.chunk].task].n_tok < p_single;
+    auto tc_group = [&](const ItemCost& it) {
+        const HostChunk& hc = P->chunks[it.chunk];
+        const bool exact = o.tc_engine == 0 && P->tasks[hc.task].n_tok < p_single;
+        const int rows_total = hc.dev.n_q * G;
+        const bool split = o.tc_engine == 0 && std::min(hc.dev.r_tile, rows_total - it.rb * hc.dev.r_tile) > 128;
+        return (exact ? 2 : 0) + (split ? 0 : 1);
     };
-    for (const auto& it : tc)
-        if (!exact_item(it)) P->items.push_back({it.chunk, it.head, it.rb});
-    for (const auto& it : tc)
-        if (exact_item(it)) P->items.push_back({it.chunk, it.head, it.rb});
+    for (int g = 0; g < 4; ++g) {
+        const size_t before = P->items.size();
+        for (const auto& it : tc)
+            if (tc_group(it) == g) P->items.push_back({it.chunk, it.head, it.rb});
+        P->tc_group_cnt[g] = (int64_t)(P->items.size() - before);
+    }
     P->n_tc_items = (int64_t)tc.size();
-    P->n_tc_exact = (int64_t)std::count_if(tc.begin(), tc.end(), exact_item);
     P->n_cc_items = (int64_t)cc.size();
     // one CUDA-core launch per row tile (8, 4, 2, 1), each in largest-first order
     for (int k = 0; k < 4; ++k) {
@@ -863,7 +868,8 @@ extern "C" int pst_plan_stats_get(const pst_plan* p, pst_plan_stats* s) {
     s->kv_tokens_read = p->kv_tokens_read;
     s->workspace_bytes = p->ws.total;
     s->num_slots = p->num_slots;
-    s->n_launches = (p->n_tc_items - p->n_tc_exact > 0) + (p->n_tc_exact > 0) + 1;
+    s->n_launches = 1;
+    for (int g = 0; g < 4; ++g) s->n_launches += p->tc_group_cnt[g] > 0;
     for (int k = 0; k < 4; ++k) s->n_launches += p->cc_class_cnt[k] > 0;
     return PST_OK;
 }

@@ -171,9 +171,11 @@ struct pst_plan {
     std::vector<int32_t> merge_ptr, merge_row;
     std::vector<pst::DevItem> items;   // tensor-core items first, then CUDA-core
     int64_t n_tc_items = 0, n_cc_items = 0;
-    // the last n_tc_exact tensor-core items split P into bf16 hi + lo (chunks
-    // shorter than opts.p_bf16_min_tokens); they run as their own launch
-    int64_t n_tc_exact = 0;
+    // Tensor-core items come in four launch groups, in this order: P rounded
+    // once with more than 128 rows per block (both row halves), P once with at
+    // most 128, exact P (nodes shorter than opts.p_bf16_min_tokens) with more
+    // than 128, exact P with at most 128. Counts per group.
+    int64_t tc_group_cnt[4] = {0, 0, 0, 0};
     // CUDA-core items grouped by row tile 8, 4, 2, 1: offsets into items[] and counts
     int64_t cc_class_off[4] = {0, 0, 0, 0}, cc_class_cnt[4] = {0, 0, 0, 0};
     int64_t n_part_rows = 0;
@@ -188,9 +190,9 @@ struct pst_plan {
     // side streams and fork/join events (cudaStream_t / cudaEvent_t) that run
     // the PAC launch groups (tensor-core, tensor-core exact-P, CUDA-core) side
     // by side; created on first use
-    mutable void* side_stream[2] = {nullptr, nullptr};
+    mutable void* side_stream[4] = {nullptr, nullptr, nullptr, nullptr};
     mutable void* ev_fork = nullptr;
-    mutable void* ev_join[2] = {nullptr, nullptr};
+    mutable void* ev_join[4] = {nullptr, nullptr, nullptr, nullptr};
     // cached TMA descriptors (built on first decode for a pool pointer)
     mutable const void* tmap_k_ptr = nullptr;
     mutable const void* tmap_v_ptr = nullptr;

@@ -19,7 +19,7 @@
 namespace pst {
 
 cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
-                            bool exact, cudaStream_t st);
+                            int g, cudaStream_t st);
 cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
                             cudaStream_t st);
 cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, cudaStream_t st);
@@ -89,8 +89,8 @@ extern "C" int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const v
     if (rc) return rc;
     const DevPlan dp = dev_plan_at(p, ws);
     // the launch groups run one after the other on `stream`
-    for (int g = 0; g < 3; ++g) {
-        e = g < 2 ? launch_tc_group(p, dp, tk, tv, Q, g == 1, st) : launch_cc_group(p, dp, tk, tv, Q, st);
+    for (int g = 0; g < 5; ++g) {
+        e = g < 4 ? launch_tc_group(p, dp, tk, tv, Q, g, st) : launch_cc_group(p, dp, tk, tv, Q, st);
         if (e != cudaSuccess) return fail(PST_ECUDA, std::string("decode_attn_noalloc: PAC launch: ") + cudaGetErrorString(e));
     }
     e = launch_por(dp, O, LSE, st);

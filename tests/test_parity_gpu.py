@@ -164,3 +164,16 @@ def test_lazy_rescale_on_some_rows(lib, prefix, n_req, boost, opts):
     O, L, _, att = run_gpu(lib, wl, pools=(K, V), Q=Q, **opts)
     assert att.plan.stats()["n_tc_items"] > 0
     assert_matches(wl, O, L, K, V, Q, queries=range(0, n_req, 3))
+
+
+@pytest.mark.parametrize("seed", range(4))
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("p_bf16_min_tokens", [0, 1], ids=["default_precision", "p_rounded_once"])
+def test_random_trees_many_rows(lib, seed, d, p_bf16_min_tokens):
+    """Up to 96 queries x G=4 per node: row blocks of 256 (both softmax row
+    halves) and of fewer than 128 rows side by side, both P precisions."""
+    wl = synth.random_tree(9500 + seed, max_nodes=8, max_len=400, heads=(8, 2), d=d, dtype="bf16",
+                           n_queries=96)
+    O, L, (K, V, Q), att = run_gpu(lib, wl, tc_min_rows=16, p_bf16_min_tokens=p_bf16_min_tokens)
+    assert att.plan.stats()["n_tc_items"] > 0
+    assert_matches(wl, O, L, K, V, Q)
