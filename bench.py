@@ -334,12 +334,12 @@ def run_ours(args, rank, world):
     exact = (kinds == 1) & (node_tokens < thr) & (plan_opts.get("tc_engine", "tcgen05") == "tcgen05")
     alg = {"pac_tc": int(ntok[(kinds == 1) & ~exact].sum()) * per_tok,
            "pac_tc_exact": int(ntok[exact].sum()) * per_tok,
-           "pac_cc": int(ntok[kinds == 0].sum()) * per_tok,
+           "pac_thin": int(ntok[kinds == 0].sum()) * per_tok,
            "por": int(st["n_partial_rows"]) * (wl.d * 4 + 4) + wl.n_queries * wl.n_q_heads * (wl.d * 4 + 4)}
     shares = {k: v / max(1e-9, sum(kern_ms.values())) for k, v in kern_ms.items()}
     # the PAC launch groups start together; each group's time runs from the
     # call's start to its end. The dominant kernel is the one with the most bytes.
-    dom = max(("pac_tc", "pac_tc_exact", "pac_cc"), key=lambda k: alg[k])
+    dom = max(("pac_tc", "pac_tc_exact", "pac_thin"), key=lambda k: alg[k])
     dom_ms = kern_ms[dom] / max(1, kern_calls)
     dom_achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
     traffic = recorded_traffic(dom, args.workload)

@@ -77,6 +77,11 @@ typedef struct {
                                draft subtrees) split P into bf16 hi + lo parts,
                                which keeps P V as accurate as an fp32 product.
                                0: default (1024); -1: always split               */
+    int32_t thin_engine;    /* chunks below tc_min_rows rows ("thin" chunks): 0
+                               (default) the tcgen05 thin PAC, tokens on the MMA's
+                               M side and query rows (at most 16 per block) on N;
+                               bf16 with d = 128 only, other shapes take the
+                               CUDA-core PAC; 1 the CUDA-core PAC always         */
 } pst_plan_opts;
 
 /* Fill `o` with the defaults above. */
@@ -181,7 +186,8 @@ int pst_plan_check_status(const pst_plan* p, void* stream, int32_t* code);
  *   0 "pac_tc"        tensor-core PAC that rounds P once to bf16 (every
  *                     tensor-core item of the mma.sync engine)
  *   1 "pac_tc_exact"  tensor-core PAC with P split into bf16 hi + lo
- *   2 "pac_cc"        CUDA-core PAC (all row-tile launches)
+ *   2 "pac_thin"      PAC of the thin chunks (below tc_min_rows rows): the
+ *                     tcgen05 thin PAC, or every CUDA-core row-tile launch
  *   3 "por"           partial-output reduction
  * The PAC groups run side by side on forked streams, so slots 0-2 give the
  * time from the call's start to the end of that group; slot 3 is POR alone.
@@ -254,7 +260,7 @@ int pst_plan_stats_get(const pst_plan* p, pst_plan_stats* s);
  *           the chunk has no mask)
  *   chunk_tok_node / chunk_tok_t: per chunk, the (node, token) it covers in
  *           chunk order
- *   chunk_kind: 0 CUDA-core PAC, 1 tensor-core PAC
+ *   chunk_kind: 0 thin chunk (tcgen05 thin PAC or CUDA-core PAC), 1 tensor-core PAC
  *   merge: per query, the partial-row bases merged by POR */
 typedef struct {
     int64_t n_queries, n_nodes, n_chunks;
@@ -283,14 +289,15 @@ int pst_plan_export(const pst_plan* p, pst_export* e);
 /* Cost model C_est(rows, tokens) in microseconds for one PAC thread block
  * with every SM busy (CoDec "profile-based cost estimation"), per PAC kind:
  * 0 = CUDA-core PAC, 1 = tcgen05 PAC with P rounded once to bf16, 2 = tcgen05
- * PAC with exact (hi + lo) P. Tables measured on a GB300 are built in (see
+ * PAC with exact (hi + lo) P, 3 = tcgen05 thin PAC. Tables measured on a GB300 are built in (see
  * the package's cost_fit.py); pst_cost_set_table replaces the table of one
  * kind: n_r row grid points x n_n token grid points, values row-major
  * [n_r][n_n]; n_r == 0 selects the analytic model for that kind and n_r < 0
  * restores the built-in table. Between grid
  * points the estimate is bilinear in (log rows, log tokens), past the last
  * token point it grows linearly with tokens. The tables cover d = 128 bf16;
- * other shapes and the mma.sync engine use the analytic model. Process-wide;
+ * other shapes and the mma.sync engine use the analytic model. For the thin
+ * PAC (one block per SM) C_est is the block's wall time. Process-wide;
  * plans created afterwards use it. pst_cost_estimate returns -1 for an
  * unknown kind. */
 int pst_cost_set_table(int32_t kind, int32_t n_r, const float* rows, int32_t n_n,

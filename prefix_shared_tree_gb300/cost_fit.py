@@ -2,18 +2,21 @@
 
 CoDec, "profile-based cost estimation": the partitioner needs the time of one
 PAC thread block as a function of its aggregated query rows and KV tokens.
-This script measures it for the three PAC kinds (0: CUDA-core PAC, 1: tcgen05
-PAC with P rounded once to bf16, 2: tcgen05 PAC with exact P) on a grid of
-(rows, tokens): for each point it builds a forest of identical independent
-nodes (one thread block each, no KV split), fills the GPU with a few waves of
-them, times the PAC launch with the library's timer and reports
+This script measures it for the four PAC kinds (0: CUDA-core PAC, 1: tcgen05
+PAC with P rounded once to bf16, 2: tcgen05 PAC with exact P, 3: tcgen05 thin
+PAC) on a grid of (rows, tokens): for each point it builds a forest of
+identical independent nodes (one thread block each, no KV split), fills the
+GPU with a few waves of them, times the PAC launch with the library's timer
+and reports
 
     C_est = (launch time) x (number of SMs) / (number of blocks),
 
 the time one block holds one of the planner's per-SM slots with every SM
-busy (CUDA-core blocks, several waves). Tensor-core blocks hold a whole SM;
-they are timed as one wave on two thirds of the SMs, where C_est is the launch
-time. Inputs are random bf16, d = 128, one KV head (blocks are per KV head).
+busy (CUDA-core and thin-PAC blocks, several waves). Tensor-core blocks hold
+a whole SM; they are timed as one wave on two thirds of the SMs, where C_est
+is the launch time. Inputs are random bf16, d = 128, one KV head (blocks are
+per KV head), eight for the thin PAC (a thin block covers eight kv heads;
+rows are per head).
 
 Writes ``cost_table_gb300.json`` and the C++ include ``cost_table_gb300.inc``
 that libpst compiles in as its built-in tables:
@@ -33,8 +36,9 @@ GRID = {
     0: ([1, 2, 4, 8], [64, 128, 256, 512, 1024, 2048, 4096, 8192]),
     1: ([16, 32, 64, 128, 256], [128, 256, 512, 1024, 2048, 4096, 8192]),
     2: ([16, 32, 64, 128, 256], [64, 128, 256, 512, 1024, 2048, 4096]),
+    3: ([1, 2, 4, 8], [16, 32, 64, 128, 256, 512, 1024, 2048, 4096]),
 }
-SLOT = {0: "pac_cc", 1: "pac_tc", 2: "pac_tc_exact"}
+SLOT = {0: "pac_thin", 1: "pac_tc", 2: "pac_tc_exact", 3: "pac_thin"}
 PAGE = 16
 D = 128
 
@@ -47,10 +51,11 @@ def measure_point(kind: int, rows: int, tokens: int, num_sms: int, seed: int, re
     # CUDA-core blocks: a few waves, more when blocks are short so launch cost
     # amortises. Tensor-core blocks (one per SM): a single wave on about two
     # thirds of the SMs, the share they usually get beside CUDA-core work.
-    if kind == 0:
+    hkv = 8 if kind == 3 else 1
+    if kind in (0, 3):
         n = 4 * num_sms
         n = max(n, min(16 * num_sms, (1 << 21) // max(tokens, 1)))
-        n = min(n, max(num_sms, (6 << 20) // tokens))    # <= ~3 GiB per pool
+        n = min(n, max(num_sms, (6 << 20) // (tokens * hkv)))    # <= ~3 GiB per pool
     else:
         n = (2 * num_sms) // 3
     pages_per_node = (tokens + PAGE - 1) // PAGE
@@ -62,21 +67,25 @@ def measure_point(kind: int, rows: int, tokens: int, num_sms: int, seed: int, re
     page_ptr = np.arange(n + 1, dtype=np.int64) * pages_per_node
     query_node = np.repeat(np.arange(n, dtype=np.int32), rows)       # G = 1: rows = queries
     opts = dict(split_policy="none", num_sms=num_sms)
-    if kind == 1:
+    if kind == 0:
+        opts["thin_engine"] = "cuda_core"
+    elif kind == 3:
+        opts["tc_min_rows"] = 1 << 20
+    elif kind == 1:
         opts["p_bf16_min_tokens"] = 1
     elif kind == 2:
         opts["p_bf16_min_tokens"] = -1
     att = TreeDecodeAttention(node_len, parent, page_ptr, perm, None, PAGE, num_pages, query_node,
-                              1, 1, D, "bf16", **opts)
+                              hkv, hkv, D, "bf16", **opts)
     st = att.plan.stats()
-    blocks = st["n_tc_items"] if kind else st["n_cc_items"]
+    blocks = st["n_tc_items"] if kind in (1, 2) else st["n_cc_items"]
     assert blocks == n, (kind, rows, tokens, blocks, n)
     g = torch.Generator(device="cuda").manual_seed(seed)
-    K = torch.randn((num_pages, 1, PAGE, D), generator=g, device="cuda").to(torch.bfloat16)
-    V = torch.randn((num_pages, 1, PAGE, D), generator=g, device="cuda").to(torch.bfloat16)
-    Q = torch.randn((len(query_node), 1, D), generator=g, device="cuda").to(torch.bfloat16)
-    O = torch.empty((len(query_node), 1, D), dtype=torch.float32, device="cuda")
-    L = torch.empty((len(query_node), 1), dtype=torch.float32, device="cuda")
+    K = torch.randn((num_pages, hkv, PAGE, D), generator=g, device="cuda").to(torch.bfloat16)
+    V = torch.randn((num_pages, hkv, PAGE, D), generator=g, device="cuda").to(torch.bfloat16)
+    Q = torch.randn((len(query_node), hkv, D), generator=g, device="cuda").to(torch.bfloat16)
+    O = torch.empty((len(query_node), hkv, D), dtype=torch.float32, device="cuda")
+    L = torch.empty((len(query_node), hkv), dtype=torch.float32, device="cuda")
     for _ in range(3):
         att(Q, K, V, O, L)
     timer = pst.Timer(reps)
@@ -89,7 +98,7 @@ def measure_point(kind: int, rows: int, tokens: int, num_sms: int, seed: int, re
     del K, V, Q, O, L, att
     torch.cuda.empty_cache()
     # per slot: a wave of n blocks on n SMs holds each for the launch time
-    per_slot = t_us * num_sms / n if kind == 0 else t_us
+    per_slot = t_us * num_sms / n if kind in (0, 3) else t_us
     return {"kind": kind, "rows": rows, "tokens": tokens, "blocks": n, "launch_us": t_us, "us": per_slot}
 
 
@@ -100,7 +109,7 @@ def write_inc(tables: dict, path: str, note: str):
              "struct BuiltinCostTable {", "    int n_r, n_n;", "    const double* rows;",
              "    const double* tokens;", "    const double* us;", "};"]
     entries = []
-    for k in range(3):
+    for k in range(4):
         t = tables.get(k)
         if not t:
             entries.append("{0, 0, nullptr, nullptr, nullptr}")
@@ -119,13 +128,21 @@ def write_inc(tables: dict, path: str, note: str):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=os.path.dirname(os.path.abspath(__file__)))
-    ap.add_argument("--kinds", default="0,1,2")
+    ap.add_argument("--kinds", default="0,1,2,3")
     args = ap.parse_args()
     import torch
     props = torch.cuda.get_device_properties(0)
     num_sms = props.multi_processor_count
+    # kinds not measured now keep the tables of the previous run in --out
     tables, points = {}, []
+    prev = os.path.join(args.out, "cost_table_gb300.json")
+    if os.path.exists(prev):
+        with open(prev) as f:
+            old = json.load(f)
+        tables = {int(k): v for k, v in old.get("tables", {}).items()}
+        points = old.get("points", [])
     t0 = time.time()
+    new_points = []
     for kind in [int(k) for k in args.kinds.split(",")]:
         rows_g, tok_g = GRID[kind]
         us = [[0.0] * len(tok_g) for _ in rows_g]
@@ -133,12 +150,14 @@ def main():
             for j, t in enumerate(tok_g):
                 p = measure_point(kind, r, t, num_sms, seed=1000 * kind + 10 * i + j)
                 us[i][j] = p["us"]
-                points.append(p)
+                new_points.append(p)
                 print(json.dumps(p), flush=True)
+        points = [p for p in points if p["kind"] != kind] + [p for p in new_points if p["kind"] == kind]
         tables[kind] = {"rows": rows_g, "tokens": tok_g, "us": us}
     note = f"{props.name}, {num_sms} SMs, measured in {time.time() - t0:.0f} s"
     with open(os.path.join(args.out, "cost_table_gb300.json"), "w") as f:
-        json.dump({"device": props.name, "num_sms": num_sms, "tables": tables, "points": points}, f, indent=1)
+        json.dump({"device": props.name, "num_sms": num_sms, "tables": {str(k): v for k, v in sorted(tables.items())},
+                   "points": points}, f, indent=1)
     write_inc(tables, os.path.join(args.out, "cost_table_gb300.inc"), note)
     print("wrote", args.out)
 

@@ -31,6 +31,8 @@ cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, cons
                           int item_off, cudaStream_t st);
 cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
                             int item_off, bool exact_p, bool split_rows, cudaStream_t st);
+cudaError_t launch_pac_thin(const DevPlan& P, const void* tk5, const void* tv5, const void* Q, int rows_per_head,
+                            int n_items, int item_off, int counter, cudaStream_t st);
 
 // Tensor-core PAC launch group g (pst_plan::tc_group_cnt): P rounded once
 // (g < 2) or exact, more than 128 rows per block (even g) or at most 128.
@@ -45,8 +47,20 @@ cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk
     return launch_pac_umma(dp, tk, tv, Q, n, (int)off, g >= 2, (g & 1) == 0, st);
 }
 
+// Thin chunks: tcgen05 thin PAC launches for row blocks of 8 and of 4 (work
+// counters 4, 5; the pools' 5-D maps follow their 3-D maps), or one CUDA-core
+// launch per row tile (counters 0-3).
 cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
                             cudaStream_t st) {
+    if (p->thin) {
+        for (int k = 0; k < 2; ++k) {
+            cudaError_t e = launch_pac_thin(dp, static_cast<const unsigned char*>(tk) + 128,
+                                            static_cast<const unsigned char*>(tv) + 128, Q, k == 0 ? 8 : 4,
+                                            (int)p->cc_class_cnt[k], (int)p->cc_class_off[k], 4 + k, st);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
     for (int k = 0; k < 4; ++k) {
         if (p->cc_class_cnt[k] == 0) continue;
         cudaError_t e = launch_pac_cc(dp, p->dtype, tk, tv, Q, 8 >> k, (int)p->cc_class_cnt[k],
@@ -160,9 +174,11 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// TMA descriptor over a pool [num_pages][Hkv][page_size][d] viewed as 3-D
-// (d, page row, page*Hkv + head); boxes of one 128-byte slab x 16 rows with the
-// 128B swizzle.
+// TMA descriptors over a pool [num_pages][Hkv][page_size][d], 128B swizzle:
+// out[0, 128): 3-D (d, page row, page*Hkv + head), boxes of one 128-byte slab
+// x 16 rows; for thin plans out[128, 256): 5-D (64 channels, page row, head,
+// slab, page) with the slab stride 128 bytes, boxes of 16 rows x 8 heads x 2
+// slabs, which land in shared memory as [slab][head][row].
 static int make_pool_map(const pst_plan* p, const void* pool, unsigned char* out) {
     auto fn = encode_fn();
     if (!fn) return fail(PST_ECUDA, "decode_attn: cuTensorMapEncodeTiled is unavailable");
@@ -176,6 +192,18 @@ static int make_pool_map(const pst_plan* p, const void* pool, unsigned char* out
                     const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PST_ECUDA, "decode_attn: cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    if (p->thin) {
+        cuuint64_t d5[5] = {64, (cuuint64_t)p->page_size, (cuuint64_t)p->hkv, 2, (cuuint64_t)p->num_pages};
+        cuuint64_t s5[4] = {(cuuint64_t)p->d * eb, (cuuint64_t)p->page_size * p->d * eb, 128,
+                            (cuuint64_t)p->hkv * p->page_size * p->d * eb};
+        cuuint32_t b5[5] = {64, (cuuint32_t)kBoxRows, (cuuint32_t)kThinHeads, 2, 1};
+        cuuint32_t e5[5] = {1, 1, 1, 1, 1};
+        r = fn(reinterpret_cast<CUtensorMap*>(out + 128), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool), d5,
+               s5, b5, e5, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS)
+            return fail(PST_ECUDA, "decode_attn: cuTensorMapEncodeTiled (5-D) failed (" + std::to_string((int)r) + ")");
+    }
     return PST_OK;
 }
 
@@ -319,7 +347,7 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
             e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g, gst[g])
                       : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, gst[g]);
             if (e != cudaSuccess) return cuda_fail(g < 4 ? "decode_attn: PAC (tensor core) launch"
-                                                         : "decode_attn: PAC (CUDA core) launch", e);
+                                                         : "decode_attn: PAC (thin chunks) launch", e);
         }
         if (ev) cudaEventRecord(ev[1 + g], gst[g]);
     }
@@ -427,7 +455,7 @@ extern "C" const char* pst_timer_kernel_name(int32_t slot) {
     switch (slot) {
         case 0: return "pac_tc";
         case 1: return "pac_tc_exact";
-        case 2: return "pac_cc";
+        case 2: return "pac_thin";
         case 3: return "por";
         default: return "";
     }

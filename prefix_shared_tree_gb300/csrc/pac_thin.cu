@@ -1,0 +1,577 @@
+// Tensor-core partial attention computation (PAC) for thin chunks: fewer
+// aggregated query rows (queries x GQA group) per kv head than the
+// tensor-core PAC's threshold; bf16, d = 128, Hkv a multiple of 8.
+//
+// CoDec, "intra-block primitives": each K/V tile of the chunk is loaded into
+// shared memory once for all of the chunk's query rows and the PAC emits a
+// partial output with its softmax statistics for the POR merge. CoDec, "KV
+// cache management": node-local stabilisation with a running max and sum.
+// DEFT's bit causal mask gives per-row visibility inside packed chunks.
+//
+// Layout of the work. A thin chunk has too few rows to fill the 128-row M
+// side of a tcgen05 MMA, so the roles are swapped: the M side holds keys, and
+// a block takes 8 kv heads at once, so one 16-token page row-box of all 8
+// heads fills it (lane 16 h + t = token t of head h). One TMA instruction then
+// moves a whole 32 KB K (or V) tile: the per-instruction cost of the TMA unit,
+// not the bytes, limits paged loads of single-head 2 KB boxes on GB300. Per
+// tile of 16 tokens x 8 heads:
+//     S^T   = K Q^T        M = 128 (head, token), N = 8 R (head, row), K = d;
+//                          only the blocks with matching heads are used
+//     O^T_h += V_h^T P_h^T  per head h: M = d, N = 16 (R rows used), K = the
+//                          head's 16 tokens (V read MN-major, P^T from shared memory)
+// R = 4 or 8 rows per head. Each head's 16 tokens sit in one half-warp, so a
+// row's tile maximum is a 16-lane shuffle reduction. P^T goes to shared memory
+// in bf16 as hi + lo parts (p = hi + lo to ~2^-16), so P V is as accurate as
+// an fp32 product. The running max only moves (and O^T is rescaled in tensor
+// memory, after a block-wide vote) when it grows by more than 2^8.
+//
+// Persistent blocks, one per SM, take items (largest first) from a work queue:
+//   warp 0      claims an item, stages its Q rows in shared memory, then
+//               streams the chunk's K and V tiles with TMA into two rings;
+//   warp 1      allocates tensor memory and issues every MMA (one thread):
+//               S^T of tile g, then the P V products of tile g - 1;
+//   warps 4-7   softmax, one thread per tensor-memory lane, and the epilogue.
+#include <algorithm>
+
+#include "dev_common.cuh"
+#include "umma.cuh"
+
+namespace pst {
+namespace dev {
+
+constexpr int kThinTT = kBoxRows;                // tokens per tile (one page row-box)
+constexpr int kThinThreads = 256;
+constexpr float kThinLazy = 8.f;
+
+template <int R>
+struct ThinLayout {
+    static constexpr int D = 128;
+    static constexpr int NS = kThinHeads * R;                // S^T columns = staged Q rows
+    static constexpr int NSLAB = D / 64;
+    static constexpr uint32_t kSlab = 128 * 128;             // 128 (head, token) rows x 128 B
+    static constexpr uint32_t kOp = NSLAB * kSlab;           // one K or V tile (32 KB)
+    static constexpr int KST = 3, VST = R == 4 ? 3 : 2;
+    static constexpr uint32_t kQSlab = NS * 128;             // NS rows x 128 B
+    static constexpr uint32_t kQBuf = NSLAB * kQSlab;
+    static constexpr uint32_t kPSlab = 16 * 128;             // P^T: 16 rows x 64 lanes (bf16)
+    static constexpr uint32_t kPBuf = 2 * kPSlab;            // 16 rows x 128 lanes
+    static constexpr uint32_t kK = 0;
+    static constexpr uint32_t kV = kK + KST * kOp;
+    static constexpr uint32_t kQ = kV + VST * kOp;           // 2 slots (item parity)
+    static constexpr uint32_t kP = kQ + 2 * kQBuf;           // [tile parity][hi, lo]
+    static constexpr uint32_t kVote = kP + 4 * kPBuf;        // [tile parity][head]: grew flag, R alphas
+    static constexpr uint32_t kSum = kVote + 2 * kThinHeads * (R + 1) * 4;   // [item parity][2][head][R] sums, maxima
+    static constexpr uint32_t kIdx = kSum + 2 * 2 * kThinHeads * R * 4;       // item index, 2 slots
+    static constexpr uint32_t kBars = (kIdx + 8 + 7) & ~7u;
+    // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], item_full[2], item_empty[2], q_empty[2],
+    // s_full[2], p_full[2], vote_bar[2], pv_done, o_full, fin, lsum_bar
+    static constexpr int kNumBars = 2 * KST + 2 * VST + 12 + 4;
+    static constexpr uint32_t kTslot = kBars + 8 * kNumBars;
+    static constexpr uint32_t kBytes = kTslot + 16;
+    static_assert(kBytes + 1024 <= 232448, "shared memory");
+    static_assert(kQ % 1024 == 0 && kP % 1024 == 0 && kQSlab % 1024 == 0, "SW128 operand alignment");
+    static constexpr uint32_t kTmemCols = 256;               // S^T x 2 (NS each), O^T (8 heads x 16)
+    __device__ static constexpr uint32_t colS(int b) { return NS * b; }
+    static constexpr uint32_t kColO = 2 * NS;
+    static_assert(2 * NS + 16 * kThinHeads <= kTmemCols, "tensor memory columns");
+};
+
+// R per-lane values reduced over the 16 lanes of a half-warp (max or sum):
+// each butterfly stage with more than one live value sends half of them to
+// the partner lane and keeps the other half; afterwards lane l of the half
+// holds the result for value index (l & 15) >> (4 - log2 R), in a[0].
+template <int OFF, int NV, bool MAX>
+struct HRed {
+    template <int R>
+    __device__ __forceinline__ static void run(float (&a)[R], int lane) {
+        if constexpr (OFF >= 1) {
+            if constexpr (NV > 1) {
+                constexpr int H = NV / 2;
+                const bool up = (lane & OFF) != 0;
+#pragma unroll
+                for (int i = 0; i < H; ++i) {
+                    const float send = up ? a[i] : a[i + H];
+                    const float keep = up ? a[i + H] : a[i];
+                    const float got = __shfl_xor_sync(0xffffffffu, send, OFF);
+                    a[i] = MAX ? fmaxf(keep, got) : keep + got;
+                }
+                HRed<OFF / 2, H, MAX>::run(a, lane);
+            } else {
+                const float got = __shfl_xor_sync(0xffffffffu, a[0], OFF);
+                a[0] = MAX ? fmaxf(a[0], got) : a[0] + got;
+                HRed<OFF / 2, 1, MAX>::run(a, lane);
+            }
+        }
+    }
+};
+
+// 5-D tiled TMA load (channel, page row, head, slab, page) into shared memory.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
+// TMA producer (one thread): every 16-token tile of the chunk for the block's
+// 8 heads, K into the K ring and V into the V ring (one 32 KB box each: both
+// 64-channel slabs x 8 heads x 16 rows, landing as [slab][head][row]). Tile i
+// is global tile g = gbase + i of this block. False if a wait gave up.
+template <int R>
+__device__ bool thin_produce(const DevPlan& P, const DevChunk& C, int head0, uint32_t sK, uint32_t sV,
+                             uint32_t k_full, uint32_t k_empty, uint32_t v_full, uint32_t v_empty,
+                             const CUtensorMap* tk, const CUtensorMap* tv, int gbase) {
+    using L = ThinLayout<R>;
+    const ChunkGeo geo = chunk_geo<kThinTT>(C);
+    const int ps = P.page_size;
+    for (int i = 0; i < geo.n_tiles; ++i) {
+        const int g = gbase + i;
+        const int tpos = geo.tile0 + i * kThinTT;
+        const int page = P.pages[C.page_base + tpos / ps];
+        const int row0 = tpos % ps;
+        {
+            const int s = g % L::KST;
+            if (g >= L::KST && !mbar_wait(k_empty + 8 * s, ((g / L::KST) - 1) & 1, P.status)) return false;
+            mbar_arrive_expect_tx(k_full + 8 * s, L::kOp);
+            tma_load_5d(sK + s * L::kOp, tk, 0, row0, head0, 0, page, k_full + 8 * s);
+        }
+        {
+            const int s = g % L::VST;
+            if (g >= L::VST && !mbar_wait(v_empty + 8 * s, ((g / L::VST) - 1) & 1, P.status)) return false;
+            mbar_arrive_expect_tx(v_full + 8 * s, L::kOp);
+            tma_load_5d(sV + s * L::kOp, tv, 0, row0, head0, 0, page, v_full + 8 * s);
+        }
+    }
+    return true;
+}
+
+// tcgen05.ld of 2R columns (32 lanes x 32 bit) without the wait.
+template <int R>
+__device__ __forceinline__ void ld_2r(uint32_t taddr, uint32_t (&v)[2 * R]) {
+    if constexpr (R == 4) {
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+                     : "r"(taddr)
+                     : "memory");
+    } else {
+        umma::ld16(taddr, v);
+    }
+}
+
+template <int R>
+__global__ void __launch_bounds__(kThinThreads, 1)
+pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
+                const __nv_bfloat16* __restrict__ Q, int item_off, int n_items, int counter) {
+    using L = ThinLayout<R>;
+    constexpr int NS = L::NS, D = L::D, KST = L::KST, VST = L::VST, HB = kThinHeads;
+    constexpr int kSh = R == 4 ? 2 : 1;   // half-warp lane l holds row (l & 15) >> kSh after a reduction
+    static_assert(R == 4 || R == 8, "rows per head");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(base);
+    const uint32_t bars = sbase + L::kBars;
+    const uint32_t k_full = bars, k_empty = k_full + 8 * KST;
+    const uint32_t v_full = k_empty + 8 * KST, v_empty = v_full + 8 * VST;
+    const uint32_t item_full = v_empty + 8 * VST, item_empty = item_full + 16, q_empty = item_empty + 16;
+    const uint32_t s_full = q_empty + 16, p_full = s_full + 16;
+    const uint32_t vote_bar = p_full + 16;    // [tile parity]: every head's growth flag is in
+    const uint32_t pv_done = vote_bar + 16, o_full = pv_done + 8, fin = o_full + 8;
+    const uint32_t lsum_bar = fin + 8;        // every head's row sums are in
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kTslot);
+    volatile int* item_idx = reinterpret_cast<volatile int*>(base + L::kIdx);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int G = P.group, Hq = P.n_q_heads;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < KST; ++s) {
+            mbar_init(k_full + 8 * s, 1);
+            mbar_init(k_empty + 8 * s, 1);
+        }
+        for (int s = 0; s < VST; ++s) {
+            mbar_init(v_full + 8 * s, 1);
+            mbar_init(v_empty + 8 * s, 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(item_full + 8 * b, 32);       // every lane of the producer warp (its Q stores)
+            mbar_init(item_empty + 8 * b, 1 + 4);   // the MMA thread and the four softmax warps
+            mbar_init(q_empty + 8 * b, 1);
+            mbar_init(s_full + 8 * b, 1);
+            mbar_init(p_full + 8 * b, 128);
+            mbar_init(vote_bar + 8 * b, 128);
+        }
+        mbar_init(pv_done, 1);
+        mbar_init(o_full, 1);
+        mbar_init(fin, 1);
+        mbar_init(lsum_bar, 128);
+        fence_barrier_init();
+    }
+    // P^T rows R..15 of every head block stay zero (the P V MMAs read 16 rows)
+    for (uint32_t i = threadIdx.x; i < 4 * L::kPBuf / 16; i += kThinThreads)
+        *reinterpret_cast<uint4*>(base + L::kP + 16 * i) = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
+    if (warp == 1) {
+        umma::tmem_alloc(smem_u32(tmem_slot), L::kTmemCols);
+        umma::tmem_relinquish();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ items, Q and TMA
+        if (lane == 0) {
+            prefetch_tmap(&tk);
+            prefetch_tmap(&tv);
+        }
+        int gbase = 0;
+        for (int q = 0;; ++q) {
+            const int slot = q & 1;
+            if (q >= 2) {
+                // the slot's index was read and the MMAs reading its Q are done
+                bool w = true;
+                if (lane == 0)
+                    w = mbar_wait(item_empty + 8 * slot, ((q >> 1) - 1) & 1, P.status) &&
+                        mbar_wait(q_empty + 8 * slot, ((q >> 1) - 1) & 1, P.status);
+                if (!__shfl_sync(0xffffffffu, w, 0)) break;
+            }
+            int idx = 0;
+            if (lane == 0) idx = atomicAdd(P.counters + counter, 1);
+            idx = __shfl_sync(0xffffffffu, idx, 0);
+            DevChunk C{};
+            int head0 = 0;
+            if (idx < n_items) {
+                const DevItem it = P.items[item_off + idx];
+                C = P.chunks[it.chunk];
+                head0 = it.kv_head;
+                const int rows_total = C.n_q * G;
+                const int row0 = it.row_block * R;
+                const int rows_here = min(R, rows_total - row0);
+                // Q row n = (head h, row r), K-major with the 128B swizzle: row n of
+                // slab d / 64 at n * 128
+                uint8_t* qdst = base + L::kQ + slot * L::kQBuf;
+#pragma unroll
+                for (int i = 0; i < NS * 16 / 32; ++i) {
+                    const int u = lane + 32 * i, n = u / 16, ch = u % 16;
+                    const int h = n / R, r = n % R;
+                    uint4 v = make_uint4(0, 0, 0, 0);
+                    if (r < rows_here) {
+                        const int row = row0 + r;
+                        const int qid = P.chunk_q[C.q_base + row / G];
+                        v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(
+                                Q + ((int64_t)qid * Hq + (head0 + h) * G + row % G) * D) + ch * 16);
+                    }
+                    *reinterpret_cast<uint4*>(qdst + (ch / 8) * L::kQSlab + swz(n, ch % 8)) = v;
+                }
+                fence_proxy_async_smem();
+            }
+            if (lane == 0) item_idx[slot] = idx < n_items ? idx : -1;
+            __syncwarp();
+            mbar_arrive(item_full + 8 * slot);
+            if (idx >= n_items) break;
+            bool ok = true;
+            if (lane == 0)
+                ok = thin_produce<R>(P, C, head0, sbase + L::kK, sbase + L::kV, k_full, k_empty, v_full, v_empty,
+                                     &tk, &tv, gbase);
+            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            gbase += chunk_geo<kThinTT>(C).n_tiles;
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idS = umma::idesc_bf16_f32(128, NS, 0, 0);   // K and Q both K-major
+            constexpr uint32_t idO = umma::idesc_bf16_f32(128, 16, 1, 0);   // V^T MN-major, P^T K-major
+            // Descriptors are built once; an MMA only adds a compile-time byte
+            // offset (>> 4) to the start-address field, which never carries
+            // over (shared-memory addresses stay below 2^18).
+            const uint64_t dk0 = umma::smem_desc_sw128(sbase + L::kK, 16, 1024);
+            const uint64_t dv0 = umma::smem_desc_sw128(sbase + L::kV, L::kSlab, 1024);
+            const uint64_t dq0 = umma::smem_desc_sw128(sbase + L::kQ, 16, 1024);
+            const uint64_t dp0 = umma::smem_desc_sw128(sbase + L::kP, 16, 1024);
+            // O^T_h (+)= V_h^T P_h^T for global tile g, every head h (hi, then lo part of P)
+            auto issue_pv = [&](int g, bool first) -> bool {
+                const int pb = g & 1;
+                if (!mbar_wait(p_full + 8 * pb, (g >> 1) & 1, P.status)) return false;
+                if (!mbar_wait(v_full + 8 * (g % VST), (g / VST) & 1, P.status)) return false;
+                umma::fence_after_sync();
+                const uint64_t dv = dv0 + (uint64_t)(((g % VST) * L::kOp) >> 4);
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint64_t dp = dp0 + (uint64_t)(((2 * pb + part) * L::kPBuf) >> 4);
+#pragma unroll
+                    for (int h = 0; h < HB; ++h)
+                        umma::mma_bf16_ss(tmem + L::kColO + 16 * h, dv + ((h * 2048) >> 4),
+                                          dp + (((h / 4) * L::kPSlab + (h % 4) * 32) >> 4), idO,
+                                          (first && part == 0) ? 0u : 1u);
+                }
+                umma::commit(v_empty + 8 * (g % VST));
+                umma::commit(pv_done);
+                return true;
+            };
+            int gbase = 0;
+            bool ok = true;
+            for (int q = 0; ok; ++q) {
+                const int slot = q & 1;
+                if (!mbar_wait(item_full + 8 * slot, (q >> 1) & 1, P.status)) break;
+                const int idx = item_idx[slot];
+                mbar_arrive(item_empty + 8 * slot);
+                if (idx < 0) break;
+                const DevChunk C = P.chunks[P.items[item_off + idx].chunk];
+                const int n = chunk_geo<kThinTT>(C).n_tiles;
+                const uint64_t dq = dq0 + (uint64_t)((slot * L::kQBuf) >> 4);
+                for (int j = 0; j < n; ++j) {
+                    const int g = gbase + j;
+                    if (!mbar_wait(k_full + 8 * (g % KST), (g / KST) & 1, P.status)) { ok = false; break; }
+                    umma::fence_after_sync();
+                    const uint64_t dk = dk0 + (uint64_t)(((g % KST) * L::kOp) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma::mma_bf16_ss(tmem + L::colS(g & 1), dk + (((kk / 4) * L::kSlab + (kk % 4) * 32) >> 4),
+                                          dq + (((kk / 4) * L::kQSlab + (kk % 4) * 32) >> 4), idS,
+                                          kk > 0 ? 1u : 0u);
+                    umma::commit(s_full + 8 * (g & 1));
+                    umma::commit(k_empty + 8 * (g % KST));
+                    if (j == n - 1) umma::commit(q_empty + 8 * slot);
+                    if (j >= 1 && !issue_pv(g - 1, j == 1)) { ok = false; break; }
+                }
+                if (!ok || !issue_pv(gbase + n - 1, n == 1)) break;
+                umma::commit(o_full);
+                gbase += n;
+            }
+            // every MMA issued above has finished before tensor memory is released
+            umma::commit(fin);
+            mbar_wait(fin, 0, P.status);
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax and epilogue
+        const int wq = warp - 4;                  // lane quarter of tensor memory
+        const int ell = 32 * wq + lane;           // lane: (head h, token t) in S^T, channel in O^T
+        const int h = ell / 16, t = ell % 16;
+        const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16);
+        float* vote = reinterpret_cast<float*>(base + L::kVote);   // [tile parity][head][1 + R]
+        const float sl = P.scale_log2;
+        int gbase = 0, n_done = 0;
+        int n_vote0 = 0, n_vote1 = 0;   // completed phases of vote_bar[0], [1] (first tiles of an item do not vote)
+        bool ok = true;
+        for (int q = 0; ok; ++q) {
+            const int slot = q & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(item_full + 8 * slot, (q >> 1) & 1, P.status))) break;
+            const int idx = item_idx[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(item_empty + 8 * slot);
+            if (idx < 0) break;
+            const DevItem it = P.items[item_off + idx];
+            const DevChunk C = P.chunks[it.chunk];
+            const int rows_total = C.n_q * G;
+            const int row0 = it.row_block * R;
+            const int rows_here = min(R, rows_total - row0);
+            const ChunkGeo geo = chunk_geo<kThinTT>(C);
+            const int n = geo.n_tiles;
+            const bool masked = C.mask_base >= 0;
+            uint64_t mask[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+                mask[r] = (masked && r < rows_here) ? P.masks[C.mask_base + (row0 + r) / G] : ~0ull;
+            // running max (log2 units) and this lane's share of the row sums, for head h
+            float m_ref[R], lp[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                m_ref[r] = -INFINITY;
+                lp[r] = 0.f;
+            }
+            for (int j = 0; j < n; ++j) {
+                const int g = gbase + j;
+                if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * (g & 1), (g >> 1) & 1, P.status))) { ok = false; break; }
+                umma::fence_after_sync();
+                uint32_t sr[2 * R];   // this warp's two heads
+                ld_2r<R>(lane_addr + L::colS(g & 1) + 2 * wq * R, sr);
+                umma::wait_ld();
+                const int tpos = geo.tile0 + j * kThinTT;
+                const int pos = tpos + t;
+                const bool in = pos >= geo.pos_begin && pos < geo.pos_end;
+                const int tc = pos - geo.pos_begin;      // token index in the chunk
+                float s[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const bool vis = in && r < rows_here &&
+                                     (!masked || tc >= kMaskTokens || ((mask[r] >> (tc & 63)) & 1ull));
+                    s[r] = vis ? __uint_as_float((h & 1) ? sr[R + r] : sr[r]) : -INFINITY;
+                }
+                // V rows outside the chunk may hold stale or non-finite values:
+                // zero them before P V multiplies them by P = 0
+                if (tpos < geo.pos_begin || tpos + kThinTT > geo.pos_end) {
+                    const int vs = g % VST;
+                    if (!__all_sync(0xffffffffu, mbar_wait(v_full + 8 * vs, (g / VST) & 1, P.status))) { ok = false; break; }
+                    if (!in) {
+#pragma unroll
+                        for (int sl_i = 0; sl_i < L::NSLAB; ++sl_i) {
+                            uint8_t* vrow = base + L::kV + vs * L::kOp + sl_i * L::kSlab + ell * 128;
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                // tile maxima of head h's rows: over its 16 tokens (a half-warp)
+                float mt[R];
+                {
+                    float a[R];
+#pragma unroll
+                    for (int r = 0; r < R; ++r) a[r] = s[r];
+                    HRed<8, R, true>::run(a, lane);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) mt[r] = __shfl_sync(0xffffffffu, a[0], (lane & 16) | (r << kSh));
+                }
+                // running max, moved only when a row's maximum grows by more than
+                // 2^8 (the 16 lanes of a head take the same decisions)
+                float alpha[R];
+                bool resc = false;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float mts = mt[r] * sl;
+                    const bool grow = (m_ref[r] == -INFINITY) ? (mt[r] != -INFINITY) : (mts > m_ref[r] + kThinLazy);
+                    alpha[r] = 1.f;
+                    if (grow) {
+                        alpha[r] = fast_exp2(m_ref[r] - mts);   // 0 when nothing was accumulated
+                        resc = resc || m_ref[r] != -INFINITY;
+                        lp[r] *= alpha[r];
+                        m_ref[r] = mts;
+                    }
+                }
+                if (j >= 1) {
+                    // a rescale of O^T touches every lane (channel): the heads vote
+                    float* vb = vote + (g & 1) * HB * (R + 1);
+                    if (t == 0) {
+                        vb[h * (R + 1)] = resc ? 1.f : 0.f;
+#pragma unroll
+                        for (int r = 0; r < R; ++r) vb[h * (R + 1) + 1 + r] = alpha[r];
+                    }
+                    mbar_arrive(vote_bar + 8 * (g & 1));
+                    const int vph = ((g & 1) ? n_vote1++ : n_vote0++) & 1;
+                    if (!__all_sync(0xffffffffu, mbar_wait(vote_bar + 8 * (g & 1), vph, P.status))) { ok = false; break; }
+                    bool any = false;
+#pragma unroll
+                    for (int h2 = 0; h2 < HB; ++h2) any = any || vb[h2 * (R + 1)] != 0.f;
+                    if (any) {
+                        // O^T columns of the grown rows *= alpha once the previous P V is done
+                        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (g - 1) & 1, P.status))) { ok = false; break; }
+                        umma::fence_after_sync();
+#pragma unroll 1
+                        for (int h2 = 0; h2 < HB; ++h2) {
+                            if (vb[h2 * (R + 1)] == 0.f) continue;
+                            uint32_t o[16];
+                            umma::ld16(lane_addr + L::kColO + 16 * h2, o);
+                            umma::wait_ld();
+#pragma unroll
+                            for (int r = 0; r < R; ++r)
+                                o[r] = __float_as_uint(__uint_as_float(o[r]) * vb[h2 * (R + 1) + 1 + r]);
+                            umma::st16(lane_addr + L::kColO + 16 * h2, o);
+                        }
+                        umma::wait_st();
+                    }
+                }
+                // P^T = 2^(s sl - m) into shared memory as bf16 hi + lo
+                // (K-major: row r, lane ell at slab ell / 64, 16-byte unit (ell % 64) / 8)
+                {
+                    uint8_t* ph = base + L::kP + (2 * (g & 1)) * L::kPBuf;
+                    uint8_t* pl = ph + L::kPBuf;
+                    const uint32_t poff = (ell / 64) * L::kPSlab + (ell % 8) * 2;
+                    const int pc = (ell % 64) / 8;
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float mu = m_ref[r] == -INFINITY ? 0.f : m_ref[r];
+                        const float p = fast_exp2(fmaf(s[r], sl, -mu));
+                        lp[r] += p;
+                        const __nv_bfloat16 hi = __float2bfloat16_rn(p);
+                        const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
+                        const uint32_t off = poff + swz(r, pc);
+                        *reinterpret_cast<__nv_bfloat16*>(ph + off) = hi;
+                        *reinterpret_cast<__nv_bfloat16*>(pl + off) = lo;
+                    }
+                }
+                fence_proxy_async_smem();   // P^T and zeroed V rows are read by the tensor core
+                umma::fence_before_sync();
+                mbar_arrive(p_full + 8 * (g & 1));
+            }
+            if (!ok) break;
+            // ---- epilogue: row sums over each head's lanes, then O^T / l
+            float* sums = reinterpret_cast<float*>(base + L::kSum) + (n_done & 1) * 2 * HB * R;   // [head][R]
+            float* mref = sums + HB * R;                                                         // [head][R]
+            {
+                float a[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) a[r] = lp[r];
+                HRed<8, R, false>::run(a, lane);
+                if ((lane & ((1 << kSh) - 1)) == 0) sums[h * R + ((lane & 15) >> kSh)] = a[0];
+            }
+            if (t == 0) {
+#pragma unroll
+                for (int r = 0; r < R; ++r) mref[h * R + r] = m_ref[r];
+            }
+            mbar_arrive(lsum_bar);
+            if (!__all_sync(0xffffffffu, mbar_wait(lsum_bar, n_done & 1, P.status))) { ok = false; break; }
+            if (!__all_sync(0xffffffffu, mbar_wait(o_full, n_done & 1, P.status))) { ok = false; break; }
+            umma::fence_after_sync();
+#pragma unroll 1
+            for (int h2 = 0; h2 < HB; ++h2) {
+                uint32_t o[16];
+                umma::ld16(lane_addr + L::kColO + 16 * h2, o);
+                umma::wait_ld();
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    if (r >= rows_here) break;
+                    const float Lr = sums[h2 * R + r];
+                    const int row = row0 + r;
+                    const int64_t prow =
+                        (int64_t)C.part_base + (int64_t)(row / G) * Hq + (it.kv_head + h2) * G + row % G;
+                    P.part_o[prow * D + ell] = Lr > 0.f ? __uint_as_float(o[r]) / Lr : 0.f;
+                    if (ell == 0) P.part_lse[prow] = Lr > 0.f ? mref[h2 * R + r] + __log2f(Lr) : -INFINITY;
+                }
+            }
+            gbase += n;
+            ++n_done;
+        }
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        umma::fence_after_sync();
+        umma::tmem_dealloc(tmem, L::kTmemCols);
+    }
+}
+
+template <int R>
+cudaError_t launch_thin_r(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
+                          int item_off, int counter, cudaStream_t st) {
+    const size_t smem = 1024 + ThinLayout<R>::kBytes;
+    static int sms = 0;   // once per process (single device per process)
+    if (!sms) {
+        cudaError_t e = cudaFuncSetAttribute(pac_thin_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int dev_id = 0, n = 0;
+        if ((e = cudaGetDevice(&dev_id)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev_id)) != cudaSuccess) return e;
+        sms = std::max(1, n);
+    }
+    const int grid = std::min(n_items, sms);
+    pac_thin_kernel<R><<<grid, kThinThreads, smem, st>>>(P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q), item_off,
+                                                          n_items, counter);
+    return cudaGetLastError();
+}
+
+}  // namespace dev
+
+// rows_per_head: the items' row block (4 or 8); tk5 / tv5: the pools' 5-D maps
+cudaError_t launch_pac_thin(const DevPlan& P, const void* tk5, const void* tv5, const void* Q, int rows_per_head,
+                            int n_items, int item_off, int counter, cudaStream_t st) {
+    if (P.d != 128 || P.n_kv_heads % kThinHeads) return cudaErrorInvalidValue;
+    if (n_items <= 0) return cudaSuccess;
+    const CUtensorMap* k = static_cast<const CUtensorMap*>(tk5);
+    const CUtensorMap* v = static_cast<const CUtensorMap*>(tv5);
+    return rows_per_head == 4 ? dev::launch_thin_r<4>(P, k, v, Q, n_items, item_off, counter, st)
+                              : dev::launch_thin_r<8>(P, k, v, Q, n_items, item_off, counter, st);
+}
+
+}  // namespace pst

@@ -83,9 +83,15 @@ static double analytic_cost(int kind, double rows, double tokens, double bytes_p
                             int num_sms) {
     const double bw_sm = 6.0e6 / std::max(1, num_sms);        // bytes per us per SM
     const double t0 = 1.5;                                     // us per block
-    const double mem = tokens * bytes_per_tok / bw_sm;
+    // a thin-PAC item covers kThinHeads kv heads
+    const double heads = kind == 3 ? kThinHeads : 1;
+    const double mem = tokens * bytes_per_tok * heads / bw_sm;
     double cmp;
-    if (kind == 1) {
+    if (kind == 3) {
+        // tcgen05 thin PAC: one block per SM streams its 32 KB tiles at the SM's
+        // share of HBM; the small MMAs and the softmax stay below that
+        cmp = 0.0;
+    } else if (kind == 1) {
         // tcgen05 (measured on GB300): a 64-token tile costs ~3300 clk with
         // two 128-row halves (S = Q K^T and the hi and lo PV products share
         // the tensor pipe and tensor memory with the softmax's loads and
@@ -99,15 +105,16 @@ static double analytic_cost(int kind, double rows, double tokens, double bytes_p
         const double instr = 8.0 + 11.0 * rows;                // warp instructions per token
         cmp = tokens * instr * (d / 128.0) / (4.0 * 1800.0);   // 4 issue/clk at 1.8 GHz
     }
-    const double part = rows * (4.0 * d + 4.0) * 2.0 / bw_sm;
+    const double part = heads * rows * (4.0 * d + 4.0) * 2.0 / bw_sm;
     return t0 + std::max(mem, cmp) + part;
 }
 
 double cost_estimate(int kind, double rows, double tokens) {
-    return analytic_cost(kind ? 1 : 0, rows, tokens, 512.0, 128, 152);
+    return analytic_cost(kind == 3 ? 3 : kind ? 1 : 0, rows, tokens, 512.0, 128, 152);
 }
 
-// kind: 0 CUDA core, 1 tensor core (P rounded once), 2 tensor core (exact P)
+// kind: 0 CUDA core, 1 tensor core (P rounded once), 2 tensor core (exact P),
+// 3 tcgen05 thin PAC
 static double cost_us(int kind, double rows, double tokens, double bytes_per_tok, int d,
                       int num_sms) {
     {
@@ -130,7 +137,7 @@ static double cost_us(int kind, double rows, double tokens, double bytes_per_tok
             return (v0 * (1 - fr) + v1 * fr) * scale;
         }
     }
-    return analytic_cost(kind ? 1 : 0, rows, tokens, bytes_per_tok, d, num_sms);
+    return analytic_cost(kind == 3 ? 3 : kind ? 1 : 0, rows, tokens, bytes_per_tok, d, num_sms);
 }
 
 }  // namespace pst
@@ -139,7 +146,7 @@ using namespace pst;
 
 extern "C" int pst_cost_set_table(int32_t kind, int32_t n_r, const float* rows, int32_t n_n,
                                   const float* tokens, const float* us) {
-    if (kind < 0 || kind >= kCostKinds) return fail(PST_EINVAL, "cost_set_table: kind must be 0, 1 or 2");
+    if (kind < 0 || kind >= kCostKinds) return fail(PST_EINVAL, "cost_set_table: kind must be 0, 1, 2 or 3");
     std::lock_guard<std::mutex> lk(g_cost_mu);
     CostTable& T = g_cost[kind];
     if (n_r < 0) {
@@ -183,6 +190,7 @@ extern "C" void pst_plan_opts_default(pst_plan_opts* o) {
     o->tc_engine = 0;
     o->tc_block_rows = 256;
     o->p_bf16_min_tokens = kPBf16MinTokens;
+    o->thin_engine = 0;
 }
 
 namespace {
@@ -211,10 +219,15 @@ void chunk_range(const Span& s, int32_t bk, int32_t k, int32_t* b, int32_t* e) {
     *e = (int32_t)std::max<int64_t>(p1 - s.fo, p0 - s.fo);
 }
 
-// KV tokens per pipeline tile of the kernel that runs a task of `kind`.
-int32_t tile_tokens(int kind, const pst_plan_opts& o) {
-    return (kind == 1 && o.tc_engine == 0) ? kTcTileTokens : kTileTokens;
+// KV tokens per pipeline tile of the kernel that runs a task of `kind`
+// (`thin`: thin chunks run on the tcgen05 thin PAC, one 16-row box per tile).
+int32_t tile_tokens(int kind, const pst_plan_opts& o, bool thin) {
+    if (kind == 1) return o.tc_engine == 0 ? kTcTileTokens : kTileTokens;
+    return thin ? kBoxRows : kTileTokens;
 }
+
+// Rows per head of a thin-PAC item: 4 when the chunk has at most 4, else 8.
+int32_t thin_rows(int32_t rows) { return rows <= 4 ? 4 : kThinRows; }
 
 int32_t cc_row_tile(int32_t rows) {
     if (rows <= 1) return 1;
@@ -316,14 +329,14 @@ struct Planner {
     pst_plan& P;
     int num_sms = 152;
     double bytes_per_tok = 0;
-    int cc_per_sm[4] = {1, 3, 3, 3};   // row tiles 8, 4, 2, 1
+    int cc_per_sm[4] = {1, 3, 3, 3};   // row tiles 8, 4, 2, 1 (the thin PAC: class 0, one per SM)
 
     Planner(const Tree& t, pst_plan& p) : T(t), P(p) {}
 
     // cost kind of a task: 0 CUDA core, 1 tensor core with P rounded once,
     // 2 tensor core with exact P (a node shorter than p_bf16_min_tokens)
     int cost_kind(const Task& t) const {
-        if (t.kind == 0) return 0;
+        if (t.kind == 0) return P.thin ? 3 : 0;
         const int32_t p_single = P.opts.p_bf16_min_tokens < 0 ? INT32_MAX : P.opts.p_bf16_min_tokens;
         return t.n_tok < p_single ? 2 : 1;
     }
@@ -335,15 +348,18 @@ struct Planner {
     }
 
     int rows_per_block(const Task& t) const {
-        return t.kind == 1 ? tc_rows_per_block(P.opts) : cc_row_tile(t.rows);
+        return t.kind == 1 ? tc_rows_per_block(P.opts) : P.thin ? thin_rows(t.rows) : cc_row_tile(t.rows);
     }
+
+    // kv heads one item covers (the thin PAC takes kThinHeads at once)
+    int heads_per_item(const Task& t) const { return (t.kind == 0 && P.thin) ? kThinHeads : 1; }
 
     // per-item cost and item count of task t split b ways
     void task_items(const Task& t, int b, std::vector<ItemCost>* out, double* total,
                     int chunk_id_base) const {
         const int rpb = rows_per_block(t);
         const int n_rb = (t.rows + rpb - 1) / rpb;
-        Span s = t.node >= 0 ? node_span(T.first_offset[t.node], t.n_tok, tile_tokens(t.kind, P.opts))
+        Span s = t.node >= 0 ? node_span(T.first_offset[t.node], t.n_tok, tile_tokens(t.kind, P.opts, P.thin))
                               : Span{0, t.n_tok, 0, 1, kTileTokens};
         for (int k = 0; k < b; ++k) {
             int32_t tb = 0, te = t.n_tok;
@@ -351,9 +367,10 @@ struct Planner {
             for (int rb = 0; rb < n_rb; ++rb) {
                 const int rows_blk = std::min(rpb, t.rows - rb * rpb);
                 const double c = item_cost(t, rows_blk, te - tb);
-                if (total) *total += c * P.hkv;
+                const int hpi = heads_per_item(t);
+                if (total) *total += c * (P.hkv / hpi);
                 if (out)
-                    for (int h = 0; h < P.hkv; ++h)
+                    for (int h = 0; h < P.hkv; h += hpi)
                         out->push_back({c, chunk_id_base + k, (int16_t)h, (int16_t)rb, item_class(t)});
             }
         }
@@ -373,6 +390,7 @@ struct Planner {
     // launch class of a task's items (see ItemCost::klass)
     int8_t item_class(const Task& t) const {
         if (t.kind == 1) return (int8_t)((P.opts.tc_engine == 0 && cost_kind(t) == 2) ? 1 : 0);
+        if (P.thin) return (int8_t)(t.rows > 4 ? 2 : 3);   // thin PAC row blocks of 8, of 4
         const int rt = cc_row_tile(t.rows);
         return (int8_t)(2 + (rt == 8 ? 0 : rt == 4 ? 1 : rt == 2 ? 2 : 3));
     }
@@ -547,6 +565,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     P->num_pages = T.num_pages;
     P->n_nodes = T.n_nodes;
     P->opts = o;
+    P->thin = dtype == PST_BF16 && d == 128 && n_kv_heads % kThinHeads == 0 && o.thin_engine == 0;
     const int32_t N = T.n_nodes, G = P->group;
 
     // ---- QMapKV: per query, its path from the top of its tree (DEFT Alg. 1 step 1)
@@ -646,7 +665,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
         t.rows = t.n_q * G;
         t.n_tok = T.len[n];
         t.kind = (tc_ok && t.rows >= o.tc_min_rows) ? 1 : 0;
-        t.max_splits = node_span(T.first_offset[n], T.len[n], tile_tokens(t.kind, o)).n_blocks;
+        t.max_splits = node_span(T.first_offset[n], T.len[n], tile_tokens(t.kind, o, P->thin)).n_blocks;
         P->tasks.push_back(t);
     }
     for (size_t gi = 0; gi < P->groups.size(); ++gi) {
@@ -671,9 +690,13 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
         pl.num_sms = sms;
     }
     pl.bytes_per_tok = 2.0 * d * (dtype == PST_BF16 ? 2 : 4);
-    for (int k = 0; k < 4; ++k) {
-        const int n = pst::cc_blocks_per_sm(dtype, d, 8 >> k);
-        if (n > 0) pl.cc_per_sm[k] = n;
+    if (P->thin) {
+        pl.cc_per_sm[0] = pl.cc_per_sm[1] = 1;
+    } else {
+        for (int k = 0; k < 4; ++k) {
+            const int n = pst::cc_blocks_per_sm(dtype, d, 8 >> k);
+            if (n > 0) pl.cc_per_sm[k] = n;
+        }
     }
     const int m = pl.num_sms * o.slots_per_sm;
     P->num_slots = m;
@@ -697,7 +720,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     for (size_t ti = 0; ti < P->tasks.size(); ++ti) {
         const Task& t = P->tasks[ti];
         if (t.node >= 0) {
-            Span s = node_span(T.first_offset[t.node], t.n_tok, tile_tokens(t.kind, o));
+            Span s = node_span(T.first_offset[t.node], t.n_tok, tile_tokens(t.kind, o, P->thin));
             for (int k = 0; k < t.b_k; ++k) {
                 int32_t tb, te;
                 chunk_range(s, t.b_k, k, &tb, &te);
@@ -714,7 +737,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
                 c.dev.q_base = (int32_t)P->chunk_q.size();
                 c.dev.n_q = t.n_q;
                 c.dev.mask_base = -1;
-                c.dev.r_tile = t.kind == 1 ? tc_rows_per_block(o) : cc_row_tile(t.rows);
+                c.dev.r_tile = pl.rows_per_block(t);
                 P->chunk_q.insert(P->chunk_q.end(), P->nodeq.begin() + P->nodeq_ptr[t.node],
                                   P->nodeq.begin() + P->nodeq_ptr[t.node + 1]);
                 P->chunks.push_back(c);
@@ -734,7 +757,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
             c.dev.q_base = (int32_t)P->chunk_q.size();
             c.dev.n_q = t.n_q;
             c.dev.mask_base = (int32_t)P->masks.size();
-            c.dev.r_tile = t.kind == 1 ? tc_rows_per_block(o) : cc_row_tile(t.rows);
+            c.dev.r_tile = pl.rows_per_block(t);
             P->chunk_q.insert(P->chunk_q.end(), g.queries.begin(), g.queries.end());
             P->masks.insert(P->masks.end(), g.mask.begin(), g.mask.end());
             P->chunks.push_back(c);
@@ -775,7 +798,7 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
         for (int rb = 0; rb < n_rb; ++rb) {
             const int rows_blk = std::min(rpb, t.rows - rb * rpb);
             const double cst = pl.item_cost(t, rows_blk, c.dev.n_tok);
-            for (int h = 0; h < n_kv_heads; ++h)
+            for (int h = 0; h < n_kv_heads; h += pl.heads_per_item(t))
                 (t.kind == 1 ? tc : cc).push_back({cst, (int32_t)ci, (int16_t)h, (int16_t)rb, pl.item_class(t)});
         }
     }
@@ -801,11 +824,12 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     }
     P->n_tc_items = (int64_t)tc.size();
     P->n_cc_items = (int64_t)cc.size();
-    // one CUDA-core launch per row tile (8, 4, 2, 1), each in largest-first order
+    // thin chunks: one launch of the thin PAC, or one CUDA-core launch per row
+    // tile (8, 4, 2, 1); each in largest-first order
     for (int k = 0; k < 4; ++k) {
         P->cc_class_off[k] = (int64_t)P->items.size();
         for (const auto& it : cc)
-            if (P->chunks[it.chunk].dev.r_tile == (8 >> k)) P->items.push_back({it.chunk, it.head, it.rb});
+            if (it.klass - 2 == k) P->items.push_back({it.chunk, it.head, it.rb});
         P->cc_class_cnt[k] = (int64_t)P->items.size() - P->cc_class_off[k];
     }
 

@@ -19,6 +19,10 @@ inline int tc_rows_per_block(const pst_plan_opts& o) {
 }
 // Rows of the CUDA-core PAC per thread block (largest row tile).
 constexpr int kCcRowsPerBlock = 8;
+// tcgen05 thin PAC: rows per head of an item (at most; 4 or 8) and kv heads
+// per item.
+constexpr int kThinRows = 8;
+constexpr int kThinHeads = 8;
 // KV tokens per pipeline stage of the CUDA-core and mma.sync PAC kernels
 // (4 boxes of 16 rows) and of the tcgen05 PAC (8 boxes).
 constexpr int kTileTokens = 64;
@@ -40,7 +44,8 @@ struct DevChunk {
     int32_t n_q;        // queries grouped with this chunk
     int32_t part_base;  // partial row of (chunk query 0, q-head 0); row = base + qi*Hq + h
     int32_t mask_base;  // -1: every query sees every token; else index into masks[]
-    int32_t r_tile;     // rows per block: CUDA-core PAC 1, 2, 4 or 8; tensor-core 128 or 256
+    int32_t r_tile;     // rows per block (per kv head): CUDA-core PAC 1, 2, 4 or 8; thin PAC 4 or 8;
+                        // tensor-core 128 or 256
 };
 static_assert(sizeof(DevChunk) == 32, "DevChunk layout");
 
@@ -86,8 +91,8 @@ struct DevPlan {
 };
 
 // PAC kinds of the cost model: CUDA core, tensor core with P rounded once to
-// bf16, tensor core with exact (hi + lo) P.
-constexpr int kCostKinds = 3;
+// bf16, tensor core with exact (hi + lo) P, tcgen05 thin PAC.
+constexpr int kCostKinds = 4;
 
 // Work-queue counters after the status word (one per persistent launch).
 constexpr int kNumCounters = 8;
@@ -176,8 +181,10 @@ struct pst_plan {
     // most 128, exact P (nodes shorter than opts.p_bf16_min_tokens) with more
     // than 128, exact P with at most 128. Counts per group.
     int64_t tc_group_cnt[4] = {0, 0, 0, 0};
-    // CUDA-core items grouped by row tile 8, 4, 2, 1: offsets into items[] and counts
+    // thin-chunk items: with the thin PAC all in class 0 (one launch); with the
+    // CUDA-core PAC grouped by row tile 8, 4, 2, 1. Offsets into items[] and counts
     int64_t cc_class_off[4] = {0, 0, 0, 0}, cc_class_cnt[4] = {0, 0, 0, 0};
+    bool thin = false;   // thin chunks run on the tcgen05 thin PAC
     int64_t n_part_rows = 0;
     // stats
     double plan_us = 0, makespan_us = 0, cost_l_us = 0;
@@ -196,6 +203,8 @@ struct pst_plan {
     // cached TMA descriptors (built on first decode for a pool pointer)
     mutable const void* tmap_k_ptr = nullptr;
     mutable const void* tmap_v_ptr = nullptr;
-    alignas(64) mutable unsigned char tmap_k[128];
-    alignas(64) mutable unsigned char tmap_v[128];
+    // per pool: the 3-D map of the tensor-core and CUDA-core PACs, then (thin
+    // plans) the 5-D map of the thin PAC
+    alignas(64) mutable unsigned char tmap_k[256];
+    alignas(64) mutable unsigned char tmap_v[256];
 };

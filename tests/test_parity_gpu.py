@@ -70,13 +70,43 @@ def test_random_trees(lib, seed, heads, d, dtype):
 @pytest.mark.parametrize("seed", range(12))
 @pytest.mark.parametrize("opts", [dict(tc_min_rows=1), dict(split_policy="uniform", fixed_chunk=64),
                                   dict(split_policy="none"), dict(pack_masks=False),
-                                  dict(tc_min_rows=1, tc_engine="mma_sync")],
-                         ids=["all_tensor_core", "uniform64", "no_split", "no_masks", "mma_sync"])
+                                  dict(tc_min_rows=1, tc_engine="mma_sync"), dict(thin_engine="cuda_core"),
+                                  dict(tc_min_rows=17, split_policy="uniform", fixed_chunk=128)],
+                         ids=["all_tensor_core", "uniform64", "no_split", "no_masks", "mma_sync", "cuda_core_thin",
+                              "thin_uniform128"])
 def test_random_trees_plan_variants(lib, seed, opts):
     wl = synth.random_tree(8000 + seed, max_nodes=12, max_len=300, heads=(8, 2), d=128, dtype="bf16",
                            n_queries=24)
     O, L, (K, V, Q), _ = run_gpu(lib, wl, **opts)
     assert_matches(wl, O, L, K, V, Q)
+
+
+THIN_CASES = [(8500 + s, h, 400, 6 + s) for s, h in
+              enumerate([(16, 1), (8, 1), (32, 2), (4, 1), (16, 2), (2, 2), (1, 1), (6, 2)])]
+THIN_CASES += [(8607, (4, 1), 40, 10), (8607, (8, 2), 40, 10), (8694, (4, 1), 40, 10)]   # packed masked chunks
+
+
+@pytest.mark.parametrize("seed,heads,max_len,n_queries", THIN_CASES)
+def test_thin_pac_up_to_16_rows(lib, seed, heads, max_len, n_queries):
+    """Thin chunks of 1 to 16 rows (tc_min_rows=17) on the tcgen05 thin PAC:
+    GQA groups of 1-16, single-token and ragged nodes, packed masked chunks."""
+    wl = synth.random_tree(seed, max_nodes=14, max_len=max_len, heads=heads, d=128, dtype="bf16",
+                           n_queries=n_queries)
+    O, L, (K, V, Q), att = run_gpu(lib, wl, tc_min_rows=17)
+    assert att.plan.stats()["n_cc_items"] > 0
+    assert_matches(wl, O, L, K, V, Q)
+
+
+@pytest.mark.parametrize("name", ["speculative", "tree_of_thought_gqa"])
+def test_thin_pac_many_row_blocks(lib, name):
+    """Every chunk on the thin PAC (tc_min_rows above any row count): chunks
+    of up to 1024 rows in blocks of 16, DEFT's masked draft chunks."""
+    wl = synth.speculative() if name == "speculative" else synth.tree_of_thought("gqa")
+    O, L, (K, V, Q), att = run_gpu(lib, wl, tc_min_rows=1 << 20)
+    assert att.plan.stats()["n_tc_items"] == 0
+    assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
+    qs = [0, 9, 20, 40, 63, 64 * 3 + 11] if name == "speculative" else [0, 5, 77, wl.n_queries - 1]
+    assert_matches(wl, O, L, K, V, Q, queries=qs)
 
 
 def test_non_finite_junk_in_unused_page_rows(lib):
