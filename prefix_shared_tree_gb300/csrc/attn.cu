@@ -44,7 +44,9 @@ cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk
     const int n = (int)p->tc_group_cnt[g];
     if (n == 0) return cudaSuccess;
     if (p->opts.tc_engine == 1) return launch_pac_tc(dp, tk, tv, Q, n, (int)off, st);
-    return launch_pac_umma(dp, tk, tv, Q, n, (int)off, g >= 2, (g & 1) == 0, st);
+    // d = 128: V in 4 KB page boxes (the pool's second 5-D view)
+    const void* tv_umma = p->d == 128 ? static_cast<const void*>(static_cast<const unsigned char*>(tv) + 256) : tv;
+    return launch_pac_umma(dp, tk, tv_umma, Q, n, (int)off, g >= 2, (g & 1) == 0, st);
 }
 
 // Thin chunks: tcgen05 thin PAC launches for row blocks of 8 and of 4 (work
@@ -176,9 +178,10 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // TMA descriptors over a pool [num_pages][Hkv][page_size][d], 128B swizzle:
 // out[0, 128): 3-D (d, page row, page*Hkv + head), boxes of one 128-byte slab
-// x 16 rows; for thin plans out[128, 256): 5-D (64 channels, page row, head,
-// slab, page) with the slab stride 128 bytes, boxes of 16 rows x 8 heads x 2
-// slabs, which land in shared memory as [slab][head][row].
+// x 16 rows; bf16 with d = 128 also gets two 5-D views (64 channels, page row,
+// head, slab, page) with the slab stride 128 bytes: out[128, 256) for thin
+// plans, boxes of 16 rows x 8 heads x 2 slabs landing as [slab][head][row];
+// out[256, 384), boxes of 16 rows x 2 slabs of one head ([slab][row], 4 KB).
 static int make_pool_map(const pst_plan* p, const void* pool, unsigned char* out) {
     auto fn = encode_fn();
     if (!fn) return fail(PST_ECUDA, "decode_attn: cuTensorMapEncodeTiled is unavailable");
@@ -192,17 +195,20 @@ static int make_pool_map(const pst_plan* p, const void* pool, unsigned char* out
                     const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PST_ECUDA, "decode_attn: cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
-    if (p->thin) {
+    if (p->dtype == PST_BF16 && p->d == 128) {
         cuuint64_t d5[5] = {64, (cuuint64_t)p->page_size, (cuuint64_t)p->hkv, 2, (cuuint64_t)p->num_pages};
         cuuint64_t s5[4] = {(cuuint64_t)p->d * eb, (cuuint64_t)p->page_size * p->d * eb, 128,
                             (cuuint64_t)p->hkv * p->page_size * p->d * eb};
-        cuuint32_t b5[5] = {64, (cuuint32_t)kBoxRows, (cuuint32_t)kThinHeads, 2, 1};
         cuuint32_t e5[5] = {1, 1, 1, 1, 1};
-        r = fn(reinterpret_cast<CUtensorMap*>(out + 128), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(pool), d5,
-               s5, b5, e5, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS)
-            return fail(PST_ECUDA, "decode_attn: cuTensorMapEncodeTiled (5-D) failed (" + std::to_string((int)r) + ")");
+        for (int v = 0; v < 2; ++v) {
+            if (v == 0 && !p->thin) continue;
+            cuuint32_t b5[5] = {64, (cuuint32_t)kBoxRows, v == 0 ? (cuuint32_t)kThinHeads : 1u, 2, 1};
+            r = fn(reinterpret_cast<CUtensorMap*>(out + 128 * (v + 1)), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5,
+                   const_cast<void*>(pool), d5, s5, b5, e5, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+            if (r != CUDA_SUCCESS)
+                return fail(PST_ECUDA, "decode_attn: cuTensorMapEncodeTiled (5-D) failed (" + std::to_string((int)r) + ")");
+        }
     }
     return PST_OK;
 }

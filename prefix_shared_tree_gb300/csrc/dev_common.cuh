@@ -95,6 +95,18 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// 5-D tiled TMA load (64 channels, page row, head, slab, page) into shared
+// memory: the pools' second view, whose slab stride (128 bytes) lets one box
+// carry both 64-channel halves of a row.
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -227,6 +239,46 @@ __device__ void produce_tiles(const DevPlan& P, const DevChunk& C, int head, uin
 #pragma unroll
             for (int sl = 0; sl < NSLAB; ++sl)
                 tma_load_3d(dst0 + sl * kSlabBytes + b * kBoxRows * 128, map, sl * 64, row0, slab_z, full);
+        }
+    }
+}
+
+// TMA producer for one operand with d = 128 in page boxes: each 16-row box of
+// a tile is one 5-D load of both 64-channel slabs (4 KB, [slab][row]), so a
+// tile of TT tokens is TT / 16 boxes at ring + s * TT * 256 + box * 4096.
+// Boxes entirely outside the chunk are skipped.
+template <int TT, int STAGES>
+__device__ void produce_pages(const DevPlan& P, const DevChunk& C, int head, uint32_t ring, uint32_t bar_full,
+                              uint32_t bar_empty, const CUtensorMap* map5) {
+    constexpr uint32_t kBox = 2 * kBoxRows * 128;
+    constexpr uint32_t kStageBytes = TT * 256;
+    const ChunkGeo g = chunk_geo<TT>(C);
+    const int ps = P.page_size;
+    const int n_list = (g.pos_end - 1) / ps + 1;
+    for (int i = 0; i < g.n_tiles; ++i) {
+        const int s = i % STAGES;
+        if (i >= STAGES) {
+            if (!mbar_wait(bar_empty + 8 * s, ((i / STAGES) - 1) & 1, P.status)) return;
+        }
+        const int tpos = g.tile0 + i * TT;
+        int page[TT / kBoxRows];
+        uint32_t nbox = 0;
+#pragma unroll
+        for (int b = 0; b < TT / kBoxRows; ++b) {
+            const int pos = tpos + b * kBoxRows;
+            const bool in = pos + kBoxRows > g.pos_begin && pos < g.pos_end;
+            const int li = pos / ps;
+            page[b] = (in && li < n_list) ? P.pages[C.page_base + li] : 0;
+            nbox += in ? 1u : 0u;
+        }
+        const uint32_t full = bar_full + 8 * s;
+        mbar_arrive_expect_tx(full, nbox * kBox);
+        const uint32_t dst0 = ring + s * kStageBytes;
+#pragma unroll
+        for (int b = 0; b < TT / kBoxRows; ++b) {
+            const int pos = tpos + b * kBoxRows;
+            if (!(pos + kBoxRows > g.pos_begin && pos < g.pos_end)) continue;
+            tma_load_5d(dst0 + b * kBox, map5, 0, pos % ps, head, 0, page[b], full);
         }
     }
 }

@@ -61,8 +61,8 @@ struct ThinLayout {
     static constexpr uint32_t kP = kQ + 2 * kQBuf;           // [tile parity][hi, lo]
     static constexpr uint32_t kVote = kP + 4 * kPBuf;        // [tile parity][head]: grew flag, R alphas
     static constexpr uint32_t kSum = kVote + 2 * kThinHeads * (R + 1) * 4;   // [item parity][2][head][R] sums, maxima
-    static constexpr uint32_t kIdx = kSum + 2 * 2 * kThinHeads * R * 4;       // item index, 2 slots
-    static constexpr uint32_t kBars = (kIdx + 8 + 7) & ~7u;
+    static constexpr uint32_t kSlot = kSum + 2 * 2 * kThinHeads * R * 4;      // ThinSlot x 2 (item parity)
+    static constexpr uint32_t kBars = kSlot + 2 * 64;
     // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], item_full[2], item_empty[2], q_empty[2],
     // s_full[2], p_full[2], vote_bar[2], pv_done, o_full, fin, lsum_bar
     static constexpr int kNumBars = 2 * KST + 2 * VST + 12 + 4;
@@ -105,15 +105,15 @@ struct HRed {
     }
 };
 
-// 5-D tiled TMA load (channel, page row, head, slab, page) into shared memory.
-__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
-                                            int c4, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.5d.shared::cluster.global.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
-        : "memory");
-}
+// An item as the producer hands it to the MMA thread and the softmax warps
+// (index -1: no more items).
+struct alignas(16) ThinSlot {
+    DevChunk C;
+    DevItem it;
+    int32_t idx;
+    int32_t pad[5];
+};
+static_assert(sizeof(ThinSlot) == 64, "ThinSlot layout");
 
 // TMA producer (one thread): every 16-token tile of the chunk for the block's
 // 8 heads, K into the K ring and V into the V ring (one 32 KB box each: both
@@ -180,7 +180,7 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     const uint32_t pv_done = vote_bar + 16, o_full = pv_done + 8, fin = o_full + 8;
     const uint32_t lsum_bar = fin + 8;        // every head's row sums are in
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kTslot);
-    volatile int* item_idx = reinterpret_cast<volatile int*>(base + L::kIdx);
+    ThinSlot* slots = reinterpret_cast<ThinSlot*>(base + L::kSlot);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int G = P.group, Hq = P.n_q_heads;
 
@@ -237,40 +237,60 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                         mbar_wait(q_empty + 8 * slot, ((q >> 1) - 1) & 1, P.status);
                 if (!__shfl_sync(0xffffffffu, w, 0)) break;
             }
+            // claimed only now: with few items, claiming ahead leaves blocks idle
             int idx = 0;
             if (lane == 0) idx = atomicAdd(P.counters + counter, 1);
             idx = __shfl_sync(0xffffffffu, idx, 0);
             DevChunk C{};
-            int head0 = 0;
+            DevItem it{};
             if (idx < n_items) {
-                const DevItem it = P.items[item_off + idx];
+                it = P.items[item_off + idx];
                 C = P.chunks[it.chunk];
-                head0 = it.kv_head;
                 const int rows_total = C.n_q * G;
                 const int row0 = it.row_block * R;
                 const int rows_here = min(R, rows_total - row0);
-                // Q row n = (head h, row r), K-major with the 128B swizzle: row n of
-                // slab d / 64 at n * 128
-                uint8_t* qdst = base + L::kQ + slot * L::kQBuf;
+                int qid[R];
 #pragma unroll
-                for (int i = 0; i < NS * 16 / 32; ++i) {
-                    const int u = lane + 32 * i, n = u / 16, ch = u % 16;
-                    const int h = n / R, r = n % R;
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (r < rows_here) {
-                        const int row = row0 + r;
-                        const int qid = P.chunk_q[C.q_base + row / G];
-                        v = *reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(
-                                Q + ((int64_t)qid * Hq + (head0 + h) * G + row % G) * D) + ch * 16);
+                for (int r = 0; r < R; ++r) qid[r] = r < rows_here ? P.chunk_q[C.q_base + (row0 + r) / G] : 0;
+                // Q row n = (head h, row r), K-major with the 128B swizzle: row n of
+                // slab d / 64 at n * 128. All loads of a batch are issued before
+                // its shared-memory stores.
+                uint8_t* qdst = base + L::kQ + slot * L::kQBuf;
+                constexpr int kUnits = NS * 16 / 32, kBatch = 8;
+#pragma unroll
+                for (int i0 = 0; i0 < kUnits; i0 += kBatch) {
+                    uint4 v[kBatch];
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int u = lane + 32 * (i0 + i), n = u / 16, ch = u % 16;
+                        const int h = n / R, r = n % R;
+                        v[i] = make_uint4(0, 0, 0, 0);
+                        if (r < rows_here) {
+                            const int row = row0 + r;
+                            int qr = qid[0];   // qid[r] without a local-memory index
+#pragma unroll
+                            for (int rr = 1; rr < R; ++rr) qr = rr == r ? qid[rr] : qr;
+                            v[i] = __ldg(reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(
+                                Q + ((int64_t)qr * Hq + (it.kv_head + h) * G + row % G) * D) + ch * 16));
+                        }
                     }
-                    *reinterpret_cast<uint4*>(qdst + (ch / 8) * L::kQSlab + swz(n, ch % 8)) = v;
+#pragma unroll
+                    for (int i = 0; i < kBatch; ++i) {
+                        const int u = lane + 32 * (i0 + i), n = u / 16, ch = u % 16;
+                        *reinterpret_cast<uint4*>(qdst + (ch / 8) * L::kQSlab + swz(n, ch % 8)) = v[i];
+                    }
                 }
                 fence_proxy_async_smem();
             }
-            if (lane == 0) item_idx[slot] = idx < n_items ? idx : -1;
+            if (lane == 0) {
+                slots[slot].C = C;
+                slots[slot].it = it;
+                slots[slot].idx = idx < n_items ? idx : -1;
+            }
             __syncwarp();
             mbar_arrive(item_full + 8 * slot);
             if (idx >= n_items) break;
+            const int head0 = it.kv_head;
             bool ok = true;
             if (lane == 0)
                 ok = thin_produce<R>(P, C, head0, sbase + L::kK, sbase + L::kV, k_full, k_empty, v_full, v_empty,
@@ -315,10 +335,10 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             for (int q = 0; ok; ++q) {
                 const int slot = q & 1;
                 if (!mbar_wait(item_full + 8 * slot, (q >> 1) & 1, P.status)) break;
-                const int idx = item_idx[slot];
+                const int idx = slots[slot].idx;
+                const DevChunk C = slots[slot].C;
                 mbar_arrive(item_empty + 8 * slot);
                 if (idx < 0) break;
-                const DevChunk C = P.chunks[P.items[item_off + idx].chunk];
                 const int n = chunk_geo<kThinTT>(C).n_tiles;
                 const uint64_t dq = dq0 + (uint64_t)((slot * L::kQBuf) >> 4);
                 for (int j = 0; j < n; ++j) {
@@ -359,12 +379,12 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         for (int q = 0; ok; ++q) {
             const int slot = q & 1;
             if (!__all_sync(0xffffffffu, mbar_wait(item_full + 8 * slot, (q >> 1) & 1, P.status))) break;
-            const int idx = item_idx[slot];
+            const int idx = slots[slot].idx;
+            const DevItem it = slots[slot].it;
+            const DevChunk C = slots[slot].C;
             __syncwarp();
             if (lane == 0) mbar_arrive(item_empty + 8 * slot);
             if (idx < 0) break;
-            const DevItem it = P.items[item_off + idx];
-            const DevChunk C = P.chunks[it.chunk];
             const int rows_total = C.n_q * G;
             const int row0 = it.row_block * R;
             const int rows_here = min(R, rows_total - row0);

@@ -75,6 +75,10 @@ struct UmmaLayout {
     static constexpr uint32_t kOp = NSLAB * kSlab;                 // one K or V tile
     static constexpr int KST = D == 128 ? 2 : 4;                   // K stages
     static constexpr int VST = D == 128 ? 2 : 4;                   // V stages
+    // V tiles are stored by page box: [box][slab][16 rows] (with d = 64 this
+    // is the K layout); a P V MMA takes one box (16 tokens)
+    static constexpr uint32_t kVBox = NSLAB * kBoxRows * 128;
+    static constexpr uint32_t kVSlab = kBoxRows * 128;             // slab stride inside a box
     static constexpr uint32_t kQSlab = 128 * 128;                  // 128 rows x 128 B
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = kK + KST * kOp;
@@ -234,7 +238,7 @@ __device__ __forceinline__ bool zero_stray_v(const DevPlan& P, uint8_t* base, co
     if (pos < geo.pos_begin || pos >= geo.pos_end) {
 #pragma unroll
         for (int sl_i = 0; sl_i < L::NSLAB; ++sl_i) {
-            uint8_t* vrow = base + L::kV + s * L::kOp + sl_i * L::kSlab + r * 128;
+            uint8_t* vrow = base + L::kV + s * L::kOp + (r / kBoxRows) * L::kVBox + sl_i * L::kVSlab + (r % kBoxRows) * 128;
 #pragma unroll
             for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + 16 * c) = make_uint4(0, 0, 0, 0);
         }
@@ -332,7 +336,10 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 produce_tiles<NSLAB, kUT, KST>(P, C, head, sK, k_full, k_empty, &tk);
             } else {
                 prefetch_tmap(&tv);
-                produce_tiles<NSLAB, kUT, VST>(P, C, head, sV, v_full, v_empty, &tv);
+                if constexpr (D == 128)
+                    produce_pages<kUT, VST>(P, C, head, sV, v_full, v_empty, &tv);   // 4 KB page boxes
+                else
+                    produce_tiles<NSLAB, kUT, VST>(P, C, head, sV, v_full, v_empty, &tv);
             }
         }
     } else if (warp == 1) {
@@ -348,7 +355,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             const uint64_t dq_base[2] = {umma::smem_desc_sw128(sQ, 16, 1024),
                                          umma::smem_desc_sw128(sQ + NSLAB * L::kQSlab, 16, 1024)};
             const uint64_t dk_base = umma::smem_desc_sw128(sK, 16, 1024);
-            const uint64_t dv_base = umma::smem_desc_sw128(sV, L::kSlab, 1024);
+            const uint64_t dv_base = umma::smem_desc_sw128(sV, L::kVSlab, 1024);
             // S of group w for tile j: Q half (mode A) x K tile j
             auto issue_s = [&](int w, int j) {
                 const uint64_t dq = dq_base[split_rows ? w : 0];
@@ -370,11 +377,11 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 const uint32_t acc0 = k > 0 ? 1u : 0u;
 #pragma unroll
                 for (int kk = 0; kk < kUT / 16; ++kk)
-                    umma::mma_bf16_ts(dst, ph + 8 * kk, dv + ((kk * 2048) >> 4), idO, kk > 0 ? 1u : acc0);
+                    umma::mma_bf16_ts(dst, ph + 8 * kk, dv + ((kk * L::kVBox) >> 4), idO, kk > 0 ? 1u : acc0);
                 if (EXACT) {
 #pragma unroll
                     for (int kk = 0; kk < kUT / 16; ++kk)
-                        umma::mma_bf16_ts(dst, ph + 64 + 8 * kk, dv + ((kk * 2048) >> 4), idO, 1u);
+                        umma::mma_bf16_ts(dst, ph + 64 + 8 * kk, dv + ((kk * L::kVBox) >> 4), idO, 1u);
                 }
                 return true;
             };

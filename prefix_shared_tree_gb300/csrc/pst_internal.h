@@ -203,8 +203,9 @@ struct pst_plan {
     // cached TMA descriptors (built on first decode for a pool pointer)
     mutable const void* tmap_k_ptr = nullptr;
     mutable const void* tmap_v_ptr = nullptr;
-    // per pool: the 3-D map of the tensor-core and CUDA-core PACs, then (thin
-    // plans) the 5-D map of the thin PAC
-    alignas(64) mutable unsigned char tmap_k[256];
-    alignas(64) mutable unsigned char tmap_v[256];
+    // per pool: the 3-D map of the tensor-core and CUDA-core PACs, then (bf16,
+    // d = 128) the 5-D maps of the thin PAC (8-head boxes) and of the tcgen05
+    // PAC's V tiles (4 KB page boxes)
+    alignas(64) mutable unsigned char tmap_k[384];
+    alignas(64) mutable unsigned char tmap_v[384];
 };

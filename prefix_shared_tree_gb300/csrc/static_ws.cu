@@ -82,7 +82,7 @@ extern "C" int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const v
     cudaError_t e = cudaMemcpyAsync(ws, p->meta_blob.data(), p->meta_blob.size(), cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess)
         return fail(PST_ECUDA, std::string("decode_attn_noalloc: metadata copy: ") + cudaGetErrorString(e));
-    alignas(64) unsigned char tk[256], tv[256];
+    alignas(64) unsigned char tk[384], tv[384];
     rc = encode_pool_map(p, K, tk);
     if (rc) return rc;
     rc = encode_pool_map(p, V, tv);
