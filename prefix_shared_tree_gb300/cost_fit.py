@@ -43,7 +43,8 @@ PAGE = 16
 D = 128
 
 
-def measure_point(kind: int, rows: int, tokens: int, num_sms: int, seed: int, reps: int = 12) -> dict:
+def measure_point(kind: int, rows: int, tokens: int, num_sms: int, seed: int, reps: int = 12,
+                  thin_sms: int = 0) -> dict:
     import torch
     from . import pst
     from .torch_api import TreeDecodeAttention
@@ -52,7 +53,9 @@ def measure_point(kind: int, rows: int, tokens: int, num_sms: int, seed: int, re
     # amortises. Tensor-core blocks (one per SM): a single wave on about two
     # thirds of the SMs, the share they usually get beside CUDA-core work.
     hkv = 8 if kind == 3 else 1
-    if kind in (0, 3):
+    if kind == 3 and thin_sms > 0:
+        n = thin_sms       # one wave on thin_sms SMs (HBM shared with fewer blocks)
+    elif kind in (0, 3):
         n = 4 * num_sms
         n = max(n, min(16 * num_sms, (1 << 21) // max(tokens, 1)))
         n = min(n, max(num_sms, (6 << 20) // (tokens * hkv)))    # <= ~3 GiB per pool
@@ -98,7 +101,7 @@ def measure_point(kind: int, rows: int, tokens: int, num_sms: int, seed: int, re
     del K, V, Q, O, L, att
     torch.cuda.empty_cache()
     # per slot: a wave of n blocks on n SMs holds each for the launch time
-    per_slot = t_us * num_sms / n if kind in (0, 3) else t_us
+    per_slot = t_us * num_sms / n if (kind == 0 or (kind == 3 and thin_sms <= 0)) else t_us
     return {"kind": kind, "rows": rows, "tokens": tokens, "blocks": n, "launch_us": t_us, "us": per_slot}
 
 
@@ -129,6 +132,8 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=os.path.dirname(os.path.abspath(__file__)))
     ap.add_argument("--kinds", default="0,1,2,3")
+    ap.add_argument("--thin-sms", type=int, default=0,
+                    help="time thin-PAC points as one wave on this many SMs (0: waves on all SMs)")
     args = ap.parse_args()
     import torch
     props = torch.cuda.get_device_properties(0)
@@ -148,7 +153,7 @@ def main():
         us = [[0.0] * len(tok_g) for _ in rows_g]
         for i, r in enumerate(rows_g):
             for j, t in enumerate(tok_g):
-                p = measure_point(kind, r, t, num_sms, seed=1000 * kind + 10 * i + j)
+                p = measure_point(kind, r, t, num_sms, seed=1000 * kind + 10 * i + j, thin_sms=args.thin_sms)
                 us[i][j] = p["us"]
                 new_points.append(p)
                 print(json.dumps(p), flush=True)

@@ -203,9 +203,13 @@ __device__ void produce_chunk(const DevPlan& P, const DevChunk& C, int head, uin
 // tiles of TT tokens go round a ring of STAGES stages; stage s starts at
 // ring + s * NSLAB * TT * 128 and holds NSLAB slabs of TT rows x 128 bytes.
 // Boxes entirely outside the chunk are skipped.
-template <int NSLAB, int TT, int STAGES>
+// With NPART > 1, producer `part` of NPART issues the boxes b with
+// b % NPART == part and announces their bytes (bar_full then expects NPART
+// arrivals): the TMA unit takes a few hundred cycles per instruction from one
+// thread, so several issuing threads fill a stage sooner.
+template <int NSLAB, int TT, int STAGES, int NPART = 1>
 __device__ void produce_tiles(const DevPlan& P, const DevChunk& C, int head, uint32_t ring, uint32_t bar_full,
-                              uint32_t bar_empty, const CUtensorMap* map) {
+                              uint32_t bar_empty, const CUtensorMap* map, int part = 0) {
     constexpr uint32_t kSlabBytes = TT * 128;
     constexpr uint32_t kStageBytes = NSLAB * kSlabBytes;
     const ChunkGeo g = chunk_geo<TT>(C);
@@ -222,7 +226,7 @@ __device__ void produce_tiles(const DevPlan& P, const DevChunk& C, int head, uin
 #pragma unroll
         for (int b = 0; b < TT / kBoxRows; ++b) {
             const int pos = tpos + b * kBoxRows;
-            const bool in = pos + kBoxRows > g.pos_begin && pos < g.pos_end;
+            const bool in = pos + kBoxRows > g.pos_begin && pos < g.pos_end && b % NPART == part;
             const int li = pos / ps;
             page[b] = (in && li < n_list) ? P.pages[C.page_base + li] : 0;
             nbox += in ? 1u : 0u;
@@ -233,7 +237,7 @@ __device__ void produce_tiles(const DevPlan& P, const DevChunk& C, int head, uin
 #pragma unroll
         for (int b = 0; b < TT / kBoxRows; ++b) {
             const int pos = tpos + b * kBoxRows;
-            if (!(pos + kBoxRows > g.pos_begin && pos < g.pos_end)) continue;
+            if (!(pos + kBoxRows > g.pos_begin && pos < g.pos_end) || b % NPART != part) continue;
             const int slab_z = page[b] * P.n_kv_heads + head;
             const int row0 = pos % ps;
 #pragma unroll

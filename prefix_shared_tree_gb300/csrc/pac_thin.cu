@@ -21,16 +21,23 @@
 //                          head's 16 tokens (V read MN-major, P^T from shared memory)
 // R = 4 or 8 rows per head. Each head's 16 tokens sit in one half-warp, so a
 // row's tile maximum is a 16-lane shuffle reduction. P^T goes to shared memory
-// in bf16 as hi + lo parts (p = hi + lo to ~2^-16), so P V is as accurate as
-// an fp32 product. The running max only moves (and O^T is rescaled in tensor
-// memory, after a block-wide vote) when it grows by more than 2^8.
+// in bf16 as hi + lo parts (p = hi + lo to ~2^-16), rows r and R + r of one
+// 16-row operand, so one N = 16 MMA per head reads the V tile once and keeps
+// both parts in separate O^T columns (summed at the end): P V is as accurate
+// as an fp32 product. Two softmax warpgroups take alternate tiles of an item
+// (even and odd tile index, so the result does not depend on which block ran
+// the item) into their own S^T buffer and O^T accumulator (split-KV inside
+// the block) and merge at the end of the item. A group's running max only moves (and its O^T is
+// rescaled in tensor memory, after a vote of its four warps) when it grows by
+// more than 2^8.
 //
 // Persistent blocks, one per SM, take items (largest first) from a work queue:
 //   warp 0      claims an item, stages its Q rows in shared memory, then
 //               streams the chunk's K and V tiles with TMA into two rings;
 //   warp 1      allocates tensor memory and issues every MMA (one thread):
 //               S^T of tile g, then the P V products of tile g - 1;
-//   warps 4-7   softmax, one thread per tensor-memory lane, and the epilogue.
+//   warps 4-7, 8-11  two softmax warpgroups (even and odd tiles of an item),
+//               one thread per tensor-memory lane, and the epilogue.
 #include <algorithm>
 
 #include "dev_common.cuh"
@@ -40,7 +47,7 @@ namespace pst {
 namespace dev {
 
 constexpr int kThinTT = kBoxRows;                // tokens per tile (one page row-box)
-constexpr int kThinThreads = 256;
+constexpr int kThinThreads = 384;
 constexpr float kThinLazy = 8.f;
 
 template <int R>
@@ -53,27 +60,29 @@ struct ThinLayout {
     static constexpr int KST = 3, VST = R == 4 ? 3 : 2;
     static constexpr uint32_t kQSlab = NS * 128;             // NS rows x 128 B
     static constexpr uint32_t kQBuf = NSLAB * kQSlab;
-    static constexpr uint32_t kPSlab = 16 * 128;             // P^T: 16 rows x 64 lanes (bf16)
+    static constexpr uint32_t kPSlab = 16 * 128;             // P^T: 16 rows (hi r, lo R + r) x 64 lanes
     static constexpr uint32_t kPBuf = 2 * kPSlab;            // 16 rows x 128 lanes
     static constexpr uint32_t kK = 0;
     static constexpr uint32_t kV = kK + KST * kOp;
     static constexpr uint32_t kQ = kV + VST * kOp;           // 2 slots (item parity)
-    static constexpr uint32_t kP = kQ + 2 * kQBuf;           // [tile parity][hi, lo]
-    static constexpr uint32_t kVote = kP + 4 * kPBuf;        // [tile parity][head]: grew flag, R alphas
-    static constexpr uint32_t kSum = kVote + 2 * kThinHeads * (R + 1) * 4;   // [item parity][2][head][R] sums, maxima
-    static constexpr uint32_t kSlot = kSum + 2 * 2 * kThinHeads * R * 4;      // ThinSlot x 2 (item parity)
+    static constexpr uint32_t kP = kQ + 2 * kQBuf;           // [group]
+    static constexpr uint32_t kVote = kP + 2 * kPBuf;        // [group][vote parity][head]: grew flag, R alphas
+    static constexpr uint32_t kSum = kVote + 2 * 2 * kThinHeads * (R + 1) * 4;   // [item parity][group][2][head][R]
+    static constexpr uint32_t kSlot = kSum + 2 * 2 * 2 * kThinHeads * R * 4;  // ThinSlot x 2 (item parity)
     static constexpr uint32_t kBars = kSlot + 2 * 64;
     // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], item_full[2], item_empty[2], q_empty[2],
-    // s_full[2], p_full[2], vote_bar[2], pv_done, o_full, fin, lsum_bar
+    // s_full[2], p_full[2], vote_bar[2], o_full, fin, lsum_bar, epi_bar
     static constexpr int kNumBars = 2 * KST + 2 * VST + 12 + 4;
     static constexpr uint32_t kTslot = kBars + 8 * kNumBars;
     static constexpr uint32_t kBytes = kTslot + 16;
     static_assert(kBytes + 1024 <= 232448, "shared memory");
     static_assert(kQ % 1024 == 0 && kP % 1024 == 0 && kQSlab % 1024 == 0, "SW128 operand alignment");
-    static constexpr uint32_t kTmemCols = 256;               // S^T x 2 (NS each), O^T (8 heads x 16)
-    __device__ static constexpr uint32_t colS(int b) { return NS * b; }
-    static constexpr uint32_t kColO = 2 * NS;
-    static_assert(2 * NS + 16 * kThinHeads <= kTmemCols, "tensor memory columns");
+    static constexpr uint32_t kTmemCols = 512;
+    // S^T of group w's tiles; O^T of group w, head h: hi part of row r at
+    // colO(w) + 16 h + r, lo part at colO(w) + 16 h + R + r
+    __device__ static constexpr uint32_t colS(int w) { return NS * w; }
+    __device__ static constexpr uint32_t colO(int w) { return 2 * NS + 16 * kThinHeads * w; }
+    static_assert(2 * NS + 2 * 16 * kThinHeads <= kTmemCols, "tensor memory columns");
 };
 
 // R per-lane values reduced over the 16 lanes of a half-warp (max or sum):
@@ -175,10 +184,11 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     const uint32_t k_full = bars, k_empty = k_full + 8 * KST;
     const uint32_t v_full = k_empty + 8 * KST, v_empty = v_full + 8 * VST;
     const uint32_t item_full = v_empty + 8 * VST, item_empty = item_full + 16, q_empty = item_empty + 16;
-    const uint32_t s_full = q_empty + 16, p_full = s_full + 16;
-    const uint32_t vote_bar = p_full + 16;    // [tile parity]: every head's growth flag is in
-    const uint32_t pv_done = vote_bar + 16, o_full = pv_done + 8, fin = o_full + 8;
-    const uint32_t lsum_bar = fin + 8;        // every head's row sums are in
+    const uint32_t s_full = q_empty + 16, p_full = s_full + 16;   // [group]
+    const uint32_t vote_bar = p_full + 16;    // [group]: every head's growth flag is in
+    const uint32_t o_full = vote_bar + 16, fin = o_full + 8;
+    const uint32_t lsum_bar = fin + 8;        // both groups' row sums and maxima are in
+    const uint32_t epi_bar = lsum_bar + 8;    // both groups have read both accumulators
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kTslot);
     ThinSlot* slots = reinterpret_cast<ThinSlot*>(base + L::kSlot);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -195,20 +205,20 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(item_full + 8 * b, 32);       // every lane of the producer warp (its Q stores)
-            mbar_init(item_empty + 8 * b, 1 + 4);   // the MMA thread and the four softmax warps
+            mbar_init(item_empty + 8 * b, 1 + 8);   // the MMA thread and the eight softmax warps
             mbar_init(q_empty + 8 * b, 1);
             mbar_init(s_full + 8 * b, 1);
             mbar_init(p_full + 8 * b, 128);
             mbar_init(vote_bar + 8 * b, 128);
         }
-        mbar_init(pv_done, 1);
         mbar_init(o_full, 1);
         mbar_init(fin, 1);
-        mbar_init(lsum_bar, 128);
+        mbar_init(lsum_bar, 256);
+        mbar_init(epi_bar, 256);
         fence_barrier_init();
     }
-    // P^T rows R..15 of every head block stay zero (the P V MMAs read 16 rows)
-    for (uint32_t i = threadIdx.x; i < 4 * L::kPBuf / 16; i += kThinThreads)
+    // P^T rows 2R..15 stay zero (the P V MMAs read 16 rows)
+    for (uint32_t i = threadIdx.x; i < 2 * L::kPBuf / 16; i += kThinThreads)
         *reinterpret_cast<uint4*>(base + L::kP + 16 * i) = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1) {
@@ -310,24 +320,20 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             const uint64_t dv0 = umma::smem_desc_sw128(sbase + L::kV, L::kSlab, 1024);
             const uint64_t dq0 = umma::smem_desc_sw128(sbase + L::kQ, 16, 1024);
             const uint64_t dp0 = umma::smem_desc_sw128(sbase + L::kP, 16, 1024);
-            // O^T_h (+)= V_h^T P_h^T for global tile g, every head h (hi, then lo part of P)
-            auto issue_pv = [&](int g, bool first) -> bool {
-                const int pb = g & 1;
-                if (!mbar_wait(p_full + 8 * pb, (g >> 1) & 1, P.status)) return false;
+            // p_full[w] completes once per tile of group w: its P^T is in (phases so far)
+            int n_p0 = 0, n_p1 = 0;
+            // O^T_h of group w (+)= V_h^T [P_hi; P_lo]_h^T for global tile g, every head h
+            auto issue_pv = [&](int g, int w, bool first) -> bool {
+                if (!mbar_wait(p_full + 8 * w, (w ? n_p1++ : n_p0++) & 1, P.status)) return false;
                 if (!mbar_wait(v_full + 8 * (g % VST), (g / VST) & 1, P.status)) return false;
                 umma::fence_after_sync();
                 const uint64_t dv = dv0 + (uint64_t)(((g % VST) * L::kOp) >> 4);
+                const uint64_t dp = dp0 + (uint64_t)((w * L::kPBuf) >> 4);   // group w's P^T
 #pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint64_t dp = dp0 + (uint64_t)(((2 * pb + part) * L::kPBuf) >> 4);
-#pragma unroll
-                    for (int h = 0; h < HB; ++h)
-                        umma::mma_bf16_ss(tmem + L::kColO + 16 * h, dv + ((h * 2048) >> 4),
-                                          dp + (((h / 4) * L::kPSlab + (h % 4) * 32) >> 4), idO,
-                                          (first && part == 0) ? 0u : 1u);
-                }
+                for (int h = 0; h < HB; ++h)
+                    umma::mma_bf16_ss(tmem + L::colO(w) + 16 * h, dv + ((h * 2048) >> 4),
+                                      dp + (((h / 4) * L::kPSlab + (h % 4) * 32) >> 4), idO, first ? 0u : 1u);
                 umma::commit(v_empty + 8 * (g % VST));
-                umma::commit(pv_done);
                 return true;
             };
             int gbase = 0;
@@ -348,15 +354,16 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                     const uint64_t dk = dk0 + (uint64_t)(((g % KST) * L::kOp) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma::mma_bf16_ss(tmem + L::colS(g & 1), dk + (((kk / 4) * L::kSlab + (kk % 4) * 32) >> 4),
+                        umma::mma_bf16_ss(tmem + L::colS(j & 1), dk + (((kk / 4) * L::kSlab + (kk % 4) * 32) >> 4),
                                           dq + (((kk / 4) * L::kQSlab + (kk % 4) * 32) >> 4), idS,
                                           kk > 0 ? 1u : 0u);
-                    umma::commit(s_full + 8 * (g & 1));
+                    umma::commit(s_full + 8 * (j & 1));
                     umma::commit(k_empty + 8 * (g % KST));
                     if (j == n - 1) umma::commit(q_empty + 8 * slot);
-                    if (j >= 1 && !issue_pv(g - 1, j == 1)) { ok = false; break; }
+                    // a group's first tile of the item starts its accumulator
+                    if (j >= 1 && !issue_pv(g - 1, (j - 1) & 1, j - 1 < 2)) { ok = false; break; }
                 }
-                if (!ok || !issue_pv(gbase + n - 1, n == 1)) break;
+                if (!ok || !issue_pv(gbase + n - 1, (n - 1) & 1, n - 1 < 2)) break;
                 umma::commit(o_full);
                 gbase += n;
             }
@@ -367,14 +374,14 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax and epilogue
-        const int wq = warp - 4;                  // lane quarter of tensor memory
+        const int w = (warp - 4) / 4;             // group: tiles j of an item with j & 1 == w
+        const int wq = warp % 4;                  // lane quarter of tensor memory
         const int ell = 32 * wq + lane;           // lane: (head h, token t) in S^T, channel in O^T
         const int h = ell / 16, t = ell % 16;
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16);
-        float* vote = reinterpret_cast<float*>(base + L::kVote);   // [tile parity][head][1 + R]
+        float* vote = reinterpret_cast<float*>(base + L::kVote) + w * 2 * HB * (R + 1);   // [vote parity][head][1 + R]
         const float sl = P.scale_log2;
-        int gbase = 0, n_done = 0;
-        int n_vote0 = 0, n_vote1 = 0;   // completed phases of vote_bar[0], [1] (first tiles of an item do not vote)
+        int gbase = 0, n_done = 0, n_vote = 0, n_tiles_w = 0;   // n_tiles_w: this group's tiles so far
         bool ok = true;
         for (int q = 0; ok; ++q) {
             const int slot = q & 1;
@@ -402,12 +409,12 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 m_ref[r] = -INFINITY;
                 lp[r] = 0.f;
             }
-            for (int j = 0; j < n; ++j) {
+            for (int j = w; j < n; j += 2) {
                 const int g = gbase + j;
-                if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * (g & 1), (g >> 1) & 1, P.status))) { ok = false; break; }
+                if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * w, n_tiles_w++ & 1, P.status))) { ok = false; break; }
                 umma::fence_after_sync();
                 uint32_t sr[2 * R];   // this warp's two heads
-                ld_2r<R>(lane_addr + L::colS(g & 1) + 2 * wq * R, sr);
+                ld_2r<R>(lane_addr + L::colS(w) + 2 * wq * R, sr);
                 umma::wait_ld();
                 const int tpos = geo.tile0 + j * kThinTT;
                 const int pos = tpos + t;
@@ -460,44 +467,43 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                         m_ref[r] = mts;
                     }
                 }
-                if (j >= 1) {
-                    // a rescale of O^T touches every lane (channel): the heads vote
-                    float* vb = vote + (g & 1) * HB * (R + 1);
+                if (j >= 2) {
+                    // a rescale of O^T touches every lane (channel): the group's heads
+                    // vote. The group's previous P V (tile j - 2) was issued before
+                    // S^T of tile j, so it has finished. The vote area alternates, so
+                    // the vote after next reuses it when every thread has read it.
+                    float* vb = vote + (n_vote & 1) * HB * (R + 1);
                     if (t == 0) {
                         vb[h * (R + 1)] = resc ? 1.f : 0.f;
 #pragma unroll
                         for (int r = 0; r < R; ++r) vb[h * (R + 1) + 1 + r] = alpha[r];
                     }
-                    mbar_arrive(vote_bar + 8 * (g & 1));
-                    const int vph = ((g & 1) ? n_vote1++ : n_vote0++) & 1;
-                    if (!__all_sync(0xffffffffu, mbar_wait(vote_bar + 8 * (g & 1), vph, P.status))) { ok = false; break; }
+                    mbar_arrive(vote_bar + 8 * w);
+                    if (!__all_sync(0xffffffffu, mbar_wait(vote_bar + 8 * w, n_vote++ & 1, P.status))) { ok = false; break; }
                     bool any = false;
 #pragma unroll
                     for (int h2 = 0; h2 < HB; ++h2) any = any || vb[h2 * (R + 1)] != 0.f;
                     if (any) {
-                        // O^T columns of the grown rows *= alpha once the previous P V is done
-                        if (!__all_sync(0xffffffffu, mbar_wait(pv_done, (g - 1) & 1, P.status))) { ok = false; break; }
-                        umma::fence_after_sync();
 #pragma unroll 1
                         for (int h2 = 0; h2 < HB; ++h2) {
-                            if (vb[h2 * (R + 1)] == 0.f) continue;
                             uint32_t o[16];
-                            umma::ld16(lane_addr + L::kColO + 16 * h2, o);
+                            umma::ld16(lane_addr + L::colO(w) + 16 * h2, o);
                             umma::wait_ld();
 #pragma unroll
-                            for (int r = 0; r < R; ++r)
-                                o[r] = __float_as_uint(__uint_as_float(o[r]) * vb[h2 * (R + 1) + 1 + r]);
-                            umma::st16(lane_addr + L::kColO + 16 * h2, o);
+                            for (int r = 0; r < R; ++r) {
+                                const float a = vb[h2 * (R + 1) + 1 + r];
+                                o[r] = __float_as_uint(__uint_as_float(o[r]) * a);
+                                o[R + r] = __float_as_uint(__uint_as_float(o[R + r]) * a);
+                            }
+                            umma::st16(lane_addr + L::colO(w) + 16 * h2, o);
                         }
                         umma::wait_st();
                     }
                 }
-                // P^T = 2^(s sl - m) into shared memory as bf16 hi + lo
-                // (K-major: row r, lane ell at slab ell / 64, 16-byte unit (ell % 64) / 8)
+                // P^T = 2^(s sl - m) into shared memory as bf16, hi in row r and lo in
+                // row R + r (K-major: lane ell at slab ell / 64, 16-byte unit (ell % 64) / 8)
                 {
-                    uint8_t* ph = base + L::kP + (2 * (g & 1)) * L::kPBuf;
-                    uint8_t* pl = ph + L::kPBuf;
-                    const uint32_t poff = (ell / 64) * L::kPSlab + (ell % 8) * 2;
+                    uint8_t* pb = base + L::kP + w * L::kPBuf + (ell / 64) * L::kPSlab + (ell % 8) * 2;
                     const int pc = (ell % 64) / 8;
 #pragma unroll
                     for (int r = 0; r < R; ++r) {
@@ -506,50 +512,65 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                         lp[r] += p;
                         const __nv_bfloat16 hi = __float2bfloat16_rn(p);
                         const __nv_bfloat16 lo = __float2bfloat16_rn(p - __bfloat162float(hi));
-                        const uint32_t off = poff + swz(r, pc);
-                        *reinterpret_cast<__nv_bfloat16*>(ph + off) = hi;
-                        *reinterpret_cast<__nv_bfloat16*>(pl + off) = lo;
+                        *reinterpret_cast<__nv_bfloat16*>(pb + swz(r, pc)) = hi;
+                        *reinterpret_cast<__nv_bfloat16*>(pb + swz(R + r, pc)) = lo;
                     }
                 }
                 fence_proxy_async_smem();   // P^T and zeroed V rows are read by the tensor core
                 umma::fence_before_sync();
-                mbar_arrive(p_full + 8 * (g & 1));
+                mbar_arrive(p_full + 8 * w);
             }
             if (!ok) break;
-            // ---- epilogue: row sums over each head's lanes, then O^T / l
-            float* sums = reinterpret_cast<float*>(base + L::kSum) + (n_done & 1) * 2 * HB * R;   // [head][R]
-            float* mref = sums + HB * R;                                                         // [head][R]
+            // ---- epilogue: each group's row sums and maxima, then the two
+            // accumulators merged; group 0 writes heads 0-3, group 1 heads 4-7
+            float* sums = reinterpret_cast<float*>(base + L::kSum) + (n_done & 1) * 2 * 2 * HB * R;   // [group][2][head][R]
             {
                 float a[R];
 #pragma unroll
                 for (int r = 0; r < R; ++r) a[r] = lp[r];
                 HRed<8, R, false>::run(a, lane);
-                if ((lane & ((1 << kSh) - 1)) == 0) sums[h * R + ((lane & 15) >> kSh)] = a[0];
-            }
-            if (t == 0) {
+                float* mine = sums + w * 2 * HB * R;
+                if ((lane & ((1 << kSh) - 1)) == 0) mine[h * R + ((lane & 15) >> kSh)] = a[0];
+                if (t == 0) {
 #pragma unroll
-                for (int r = 0; r < R; ++r) mref[h * R + r] = m_ref[r];
+                    for (int r = 0; r < R; ++r) mine[HB * R + h * R + r] = m_ref[r];
+                }
             }
             mbar_arrive(lsum_bar);
             if (!__all_sync(0xffffffffu, mbar_wait(lsum_bar, n_done & 1, P.status))) { ok = false; break; }
             if (!__all_sync(0xffffffffu, mbar_wait(o_full, n_done & 1, P.status))) { ok = false; break; }
             umma::fence_after_sync();
+            const bool has1 = n >= 2;   // the groups that saw a tile of the item
+            const bool has0 = true;
 #pragma unroll 1
-            for (int h2 = 0; h2 < HB; ++h2) {
-                uint32_t o[16];
-                umma::ld16(lane_addr + L::kColO + 16 * h2, o);
+            for (int h2 = 4 * w; h2 < 4 * w + 4; ++h2) {
+                uint32_t o0[16], o1[16];
+                if (has0) umma::ld16(lane_addr + L::colO(0) + 16 * h2, o0);
+                if (has1) umma::ld16(lane_addr + L::colO(1) + 16 * h2, o1);
                 umma::wait_ld();
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
                     if (r >= rows_here) break;
-                    const float Lr = sums[h2 * R + r];
+                    const float l0 = sums[h2 * R + r], m0 = sums[HB * R + h2 * R + r];
+                    const float l1 = sums[2 * HB * R + h2 * R + r], m1 = sums[3 * HB * R + h2 * R + r];
+                    const float M = fmaxf(has0 ? m0 : -INFINITY, has1 ? m1 : -INFINITY);
+                    const float Mu = M == -INFINITY ? 0.f : M;
+                    const float w0 = has0 ? fast_exp2(m0 - Mu) : 0.f, w1 = has1 ? fast_exp2(m1 - Mu) : 0.f;
+                    const float Lr = (has0 ? l0 * w0 : 0.f) + (has1 ? l1 * w1 : 0.f);
+                    float acc = 0.f;
+                    if (has0) acc += (__uint_as_float(o0[r]) + __uint_as_float(o0[R + r])) * w0;
+                    if (has1) acc += (__uint_as_float(o1[r]) + __uint_as_float(o1[R + r])) * w1;
                     const int row = row0 + r;
                     const int64_t prow =
                         (int64_t)C.part_base + (int64_t)(row / G) * Hq + (it.kv_head + h2) * G + row % G;
-                    P.part_o[prow * D + ell] = Lr > 0.f ? __uint_as_float(o[r]) / Lr : 0.f;
-                    if (ell == 0) P.part_lse[prow] = Lr > 0.f ? mref[h2 * R + r] + __log2f(Lr) : -INFINITY;
+                    P.part_o[prow * D + ell] = Lr > 0.f ? acc / Lr : 0.f;
+                    if (ell == 0) P.part_lse[prow] = Lr > 0.f ? M + __log2f(Lr) : -INFINITY;
                 }
             }
+            // the next item's first P V of either group overwrites an accumulator
+            // the other group may still be reading
+            mbar_arrive(epi_bar);
+            if (!__all_sync(0xffffffffu, mbar_wait(epi_bar, n_done & 1, P.status))) { ok = false; break; }
             gbase += n;
             ++n_done;
         }

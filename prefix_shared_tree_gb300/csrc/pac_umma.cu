@@ -10,10 +10,12 @@
 // visibility inside packed draft-token chunks.
 //
 // One thread block per (chunk, kv head, block of up to 256 rows), warp-
-// specialised (12 warps, three warpgroups):
-//   warps 0, 2  TMA producers of K and of V: 128-token tiles (16-row page
-//               boxes, 128B swizzle) into their own rings; a K stage is
-//               refilled as soon as Q K^T has read it, a V stage after P V;
+// specialised (the producer/MMA warpgroup, then the softmax warpgroups):
+//   warps 0, 3  TMA producers of K (alternate 16-row page boxes), warp 2 of
+//               V (both 64-channel slabs of a page box in one load; d = 128):
+//               128-token tiles, 128B swizzle, each operand in its own ring;
+//               a K stage is refilled as soon as Q K^T has read it, a V stage
+//               after P V;
 //   warp 1      allocates all 512 tensor-memory columns and issues every MMA
 //               from one thread: S = Q K^T (M=128, N=128, Q and K from shared
 //               memory) and O += P V (M=128, N=d, P from tensor memory, V
@@ -49,7 +51,7 @@
 namespace pst {
 namespace dev {
 
-// Warps: the producer/MMA warpgroup (K producer, MMA, V producer, idle), then
+// Warps: the producer/MMA warpgroup (K producer, MMA, V producer, K producer), then
 // the softmax warpgroups: four above 128 rows (each takes 32 columns of a row
 // half, so a half's softmax runs on four warps per scheduler), two at most.
 // Registers per thread: at launch (the __launch_bounds__ cap), then after
@@ -66,6 +68,7 @@ struct UWarps {
     static_assert(128 * kRegsMma + 128 * kGroups * kRegsSoftmax <= kThreads * kRegsLaunch, "register split");
 };
 constexpr int kUT = kTcTileTokens;   // tokens per tile
+constexpr int kKProducers = 2;       // threads issuing a K tile's TMA loads
 constexpr float kLazyRescale = 8.f;
 
 template <int D>
@@ -289,7 +292,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < KST; ++s) {
-            mbar_init(k_full + 8 * s, 1);
+            mbar_init(k_full + 8 * s, kKProducers);
             mbar_init(k_empty + 8 * s, 1);
         }
         for (int s = 0; s < VST; ++s) {
@@ -326,14 +329,15 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(UWarps<SPLIT>::kRegsMma));
         else
             asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(UWarps<SPLIT>::kRegsMma));
-    if (warp == 0 || warp == 2) {
+    if (warp == 0 || warp == 2 || warp == 3) {
         // ------------------------------------------------------------ TMA producers
-        // warp 0 streams K, warp 2 streams V, each at its own pace (two lanes
-        // of one warp would reconverge and tie the two streams together)
+        // warps 0 and 3 stream K (alternate page boxes), warp 2 streams V, each
+        // at its own pace (two lanes of one warp would reconverge and tie the
+        // streams together)
         if (lane == 0) {
-            if (warp == 0) {
+            if (warp != 2) {
                 prefetch_tmap(&tk);
-                produce_tiles<NSLAB, kUT, KST>(P, C, head, sK, k_full, k_empty, &tk);
+                produce_tiles<NSLAB, kUT, KST, kKProducers>(P, C, head, sK, k_full, k_empty, &tk, warp == 0 ? 0 : 1);
             } else {
                 prefetch_tmap(&tv);
                 if constexpr (D == 128)
