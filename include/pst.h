@@ -140,6 +140,19 @@ int pst_plan_create(const pst_tree* tree, int32_t n_queries, const int32_t* quer
                     const pst_plan_opts* opts, pst_plan** out);
 void pst_plan_destroy(pst_plan* p);
 
+/* Incremental plan for the next decode step (CoDec, "workload balancing": the
+ * plan is reused across decode steps while the tree keeps its shape). `tree`
+ * has prev's node count and parents (leaves may have grown or shrunk, pages
+ * may have been added); queries stay on the nodes they sat on in prev, with
+ * prev's heads, d, dtype and options. The grouping, packing, chunks, items and
+ * metadata are rebuilt for the new lengths, but each node keeps prev's KV-axis
+ * split b_k (bounded by its tiles) instead of a new partition search; a task
+ * that did not exist in prev (a packing that changed) takes ceil(C_est /
+ * cost_l) under prev's cost_l. The new plan is independent of prev (upload it
+ * to a workspace of its own size). Errors: PST_EINVAL (null, node count or
+ * parents differ), and those of pst_plan_create. */
+int pst_plan_update(const pst_plan* prev, const pst_tree* tree, pst_plan** out);
+
 /* Bytes of device workspace the plan needs: its metadata plus the partial
  * output scratch (fp32 partial outputs and log-sum-exps). */
 int64_t pst_plan_workspace_bytes(const pst_plan* p);

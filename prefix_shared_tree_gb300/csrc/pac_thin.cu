@@ -33,7 +33,8 @@
 //
 // Persistent blocks, one per SM, take items (largest first) from a work queue:
 //   warp 0      claims an item, stages its Q rows in shared memory, then
-//               streams the chunk's K and V tiles with TMA into two rings;
+//               streams the chunk's K tiles with TMA; warp 2 streams its V
+//               tiles into a second ring at its own pace;
 //   warp 1      allocates tensor memory and issues every MMA (one thread):
 //               S^T of tile g, then the P V products of tile g - 1;
 //   warps 4-7, 8-11  two softmax warpgroups (even and odd tiles of an item),
@@ -124,34 +125,26 @@ struct alignas(16) ThinSlot {
 };
 static_assert(sizeof(ThinSlot) == 64, "ThinSlot layout");
 
-// TMA producer (one thread): every 16-token tile of the chunk for the block's
-// 8 heads, K into the K ring and V into the V ring (one 32 KB box each: both
-// 64-channel slabs x 8 heads x 16 rows, landing as [slab][head][row]). Tile i
-// is global tile g = gbase + i of this block. False if a wait gave up.
-template <int R>
-__device__ bool thin_produce(const DevPlan& P, const DevChunk& C, int head0, uint32_t sK, uint32_t sV,
-                             uint32_t k_full, uint32_t k_empty, uint32_t v_full, uint32_t v_empty,
-                             const CUtensorMap* tk, const CUtensorMap* tv, int gbase) {
-    using L = ThinLayout<R>;
+// TMA producer (one thread) of one operand: every 16-token tile of the chunk
+// for the block's 8 heads into a ring of ST stages (one 32 KB box per tile:
+// both 64-channel slabs x 8 heads x 16 rows, landing as [slab][head][row]).
+// Tile i is global tile g = gbase + i of this block. K and V have their own
+// producers: V stages free late (after the softmax and P V) and must not hold
+// back the next K tiles. False if a wait gave up.
+template <int ST>
+__device__ bool thin_produce(const DevPlan& P, const DevChunk& C, int head0, uint32_t ring, uint32_t full,
+                             uint32_t empty, const CUtensorMap* map, int gbase) {
+    constexpr uint32_t kOp = 2 * 128 * 128;
     const ChunkGeo geo = chunk_geo<kThinTT>(C);
     const int ps = P.page_size;
     for (int i = 0; i < geo.n_tiles; ++i) {
         const int g = gbase + i;
         const int tpos = geo.tile0 + i * kThinTT;
         const int page = P.pages[C.page_base + tpos / ps];
-        const int row0 = tpos % ps;
-        {
-            const int s = g % L::KST;
-            if (g >= L::KST && !mbar_wait(k_empty + 8 * s, ((g / L::KST) - 1) & 1, P.status)) return false;
-            mbar_arrive_expect_tx(k_full + 8 * s, L::kOp);
-            tma_load_5d(sK + s * L::kOp, tk, 0, row0, head0, 0, page, k_full + 8 * s);
-        }
-        {
-            const int s = g % L::VST;
-            if (g >= L::VST && !mbar_wait(v_empty + 8 * s, ((g / L::VST) - 1) & 1, P.status)) return false;
-            mbar_arrive_expect_tx(v_full + 8 * s, L::kOp);
-            tma_load_5d(sV + s * L::kOp, tv, 0, row0, head0, 0, page, v_full + 8 * s);
-        }
+        const int s = g % ST;
+        if (g >= ST && !mbar_wait(empty + 8 * s, ((g / ST) - 1) & 1, P.status)) return false;
+        mbar_arrive_expect_tx(full + 8 * s, kOp);
+        tma_load_5d(ring + s * kOp, map, 0, tpos % ps, head0, 0, page, full + 8 * s);
     }
     return true;
 }
@@ -205,7 +198,7 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(item_full + 8 * b, 32);       // every lane of the producer warp (its Q stores)
-            mbar_init(item_empty + 8 * b, 1 + 8);   // the MMA thread and the eight softmax warps
+            mbar_init(item_empty + 8 * b, 2 + 8);   // the V producer, the MMA thread, the eight softmax warps
             mbar_init(q_empty + 8 * b, 1);
             mbar_init(s_full + 8 * b, 1);
             mbar_init(p_full + 8 * b, 128);
@@ -302,12 +295,28 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             if (idx >= n_items) break;
             const int head0 = it.kv_head;
             bool ok = true;
-            if (lane == 0)
-                ok = thin_produce<R>(P, C, head0, sbase + L::kK, sbase + L::kV, k_full, k_empty, v_full, v_empty,
-                                     &tk, &tv, gbase);
+            if (lane == 0) ok = thin_produce<KST>(P, C, head0, sbase + L::kK, k_full, k_empty, &tk, gbase);
             if (!__shfl_sync(0xffffffffu, ok, 0)) break;
             gbase += chunk_geo<kThinTT>(C).n_tiles;
         }
+    } else if (warp == 2) {
+        // ------------------------------------------------------------ V producer
+        if (lane == 0) {
+            prefetch_tmap(&tv);
+            int gbase = 0;
+            for (int q = 0;; ++q) {
+                const int slot = q & 1;
+                if (!mbar_wait(item_full + 8 * slot, (q >> 1) & 1, P.status)) break;
+                const int idx = slots[slot].idx;
+                const DevChunk C = slots[slot].C;
+                const int head0 = slots[slot].it.kv_head;
+                mbar_arrive(item_empty + 8 * slot);
+                if (idx < 0) break;
+                if (!thin_produce<VST>(P, C, head0, sbase + L::kV, v_full, v_empty, &tv, gbase)) break;
+                gbase += chunk_geo<kThinTT>(C).n_tiles;
+            }
+        }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {

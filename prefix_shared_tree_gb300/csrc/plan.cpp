@@ -528,9 +528,11 @@ static bool build_packed_group(const Tree& T, int32_t root, const std::vector<in
     return false;
 }
 
-extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const int32_t* query_node,
-                               int32_t n_q_heads, int32_t n_kv_heads, int32_t d, pst_dtype dtype,
-                               const pst_plan_opts* opts, pst_plan** out) {
+// Plan creation; with `prev` the KV-axis splits are taken from it instead of
+// being searched (pst_plan_update).
+static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* query_node, int32_t n_q_heads,
+                      int32_t n_kv_heads, int32_t d, pst_dtype dtype, const pst_plan_opts* opts,
+                      const pst_plan* prev, pst_plan** out) {
     const auto t_start = std::chrono::steady_clock::now();
     if (!out) return fail(PST_EINVAL, "plan_create: out is null");
     *out = nullptr;
@@ -700,7 +702,24 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     }
     const int m = pl.num_sms * o.slots_per_sm;
     P->num_slots = m;
-    if (o.split_policy == PST_SPLIT_NONE) {
+    if (prev) {
+        // CoDec reuses a plan across decode steps: a node keeps its previous
+        // split b_k (bounded by its tiles now); a task that is new (a packing
+        // that changed) gets the split its cost bound under the previous
+        // cost_l gives, ceil(C_est / cost_l)
+        std::vector<int32_t> bk_of_node(T.n_nodes, 0);
+        for (const auto& t : prev->tasks)
+            if (t.node >= 0 && t.node < T.n_nodes) bk_of_node[t.node] = t.b_k;
+        P->cost_l_us = prev->cost_l_us;
+        for (auto& t : P->tasks) {
+            int32_t b = t.node >= 0 ? bk_of_node[t.node] : 1;
+            if (b <= 0) {
+                const double c = pl.item_cost(t, pl.rows_per_block(t), t.n_tok);
+                b = prev->cost_l_us > 0 ? (int32_t)std::ceil(c / prev->cost_l_us - 1e-9) : 1;
+            }
+            t.b_k = std::max(1, std::min(b, t.max_splits));
+        }
+    } else if (o.split_policy == PST_SPLIT_NONE) {
         for (auto& t : P->tasks) t.b_k = 1;
     } else if (o.split_policy == PST_SPLIT_UNIFORM) {
         for (auto& t : P->tasks)
@@ -865,6 +884,34 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     P->plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t_start).count();
     *out = guard.release();
     return PST_OK;
+}
+
+extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const int32_t* query_node,
+                               int32_t n_q_heads, int32_t n_kv_heads, int32_t d, pst_dtype dtype,
+                               const pst_plan_opts* opts, pst_plan** out) {
+    return plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, opts, nullptr, out);
+}
+
+extern "C" int pst_plan_update(const pst_plan* prev, const pst_tree* tree, pst_plan** out) {
+    if (!out) return fail(PST_EINVAL, "plan_update: out is null");
+    *out = nullptr;
+    if (!prev || !tree) return fail(PST_EINVAL, "plan_update: null plan or tree");
+    const Tree& T = tree->t;
+    if (T.n_nodes != prev->n_nodes) return fail(PST_EINVAL, "plan_update: the tree has a different node count");
+    // the queries sit where they sat: the last node of each query's path
+    std::vector<int32_t> qn(prev->n_queries);
+    for (int32_t q = 0; q < prev->n_queries; ++q) qn[q] = prev->qpath_node[prev->qpath_ptr[q + 1] - 1];
+    // the node structure must be the same: every query's path is unchanged
+    for (int32_t q = 0; q < prev->n_queries; ++q) {
+        int32_t v = qn[q];
+        for (int32_t k = prev->qpath_ptr[q + 1] - 1; k >= prev->qpath_ptr[q]; --k) {
+            if (v < 0 || prev->qpath_node[k] != v) return fail(PST_EINVAL, "plan_update: the tree's parents changed");
+            v = T.parent[v];
+        }
+        if (v != -1) return fail(PST_EINVAL, "plan_update: the tree's parents changed");
+    }
+    return plan_build(tree, prev->n_queries, qn.data(), prev->hq, prev->hkv, prev->d, prev->dtype, &prev->opts, prev,
+                      out);
 }
 
 namespace pst {

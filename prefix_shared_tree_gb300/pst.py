@@ -82,6 +82,7 @@ def lib() -> C.CDLL:
         "pst_tree_destroy": (None, [vp]),
         "pst_plan_opts_default": (None, [C.POINTER(PlanOpts)]),
         "pst_plan_create": (C.c_int, [vp, i32, vp, i32, i32, i32, C.c_int, C.POINTER(PlanOpts), C.POINTER(vp)]),
+        "pst_plan_update": (C.c_int, [vp, vp, C.POINTER(vp)]),
         "pst_plan_destroy": (None, [vp]),
         "pst_plan_workspace_bytes": (i64, [vp]),
         "pst_plan_upload": (C.c_int, [vp, vp, i64, vp]),
@@ -228,6 +229,14 @@ def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int,
     _check(lib().pst_plan_create(tree._h, len(qn), qnp, n_q_heads, n_kv_heads, d, DTYPES[dtype],
                                  C.byref(o), C.byref(h)))
     return Plan(h, len(qn), n_q_heads, n_kv_heads, d, dtype)
+
+
+def plan_update(prev: Plan, tree: Tree) -> Plan:
+    """Plan for the same queries on a tree whose node lengths (and pages)
+    changed, keeping prev's KV-axis splits (no partition search)."""
+    h = C.c_void_p()
+    _check(lib().pst_plan_update(prev._h, tree._h, C.byref(h)))
+    return Plan(h, prev.n_queries, prev.hq, prev.hkv, prev.d, prev.dtype)
 
 
 def decode_attn(plan: Plan, q: int, k_pool: int, v_pool: int, o: int, lse: int, stream: int = 0):

@@ -43,6 +43,22 @@ class TreeDecodeAttention:
             self.plan.upload(self.workspace.data_ptr(), self.workspace.numel(), stream.cuda_stream,
                              keepalive=self.workspace)
 
+    def update_tree(self, node_len, parent, page_ptr, page_ids, first_offset, num_pages=None):
+        """Next decode step on the same tree shape (leaves grown, pages added):
+        rebuild the tree and derive the plan from the current one with
+        pst_plan_update (no partition search), then upload it."""
+        if num_pages is not None:
+            self.num_pages = int(num_pages)
+        tree = pst.tree_build(node_len, parent, page_ptr, page_ids, first_offset, self.page_size, self.num_pages)
+        with torch.cuda.device(self.device):
+            plan = pst.plan_update(self.plan, tree)
+            if plan.workspace_bytes > self.workspace.numel():
+                self.workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=self.device)
+            stream = torch.cuda.current_stream(self.device)
+            plan.upload(self.workspace.data_ptr(), self.workspace.numel(), stream.cuda_stream,
+                        keepalive=self.workspace)
+        self.tree, self.plan = tree, plan
+
     @classmethod
     def from_workload(cls, wl, device="cuda", **plan_opts):
         return cls(wl.node_len, wl.parent, wl.page_ptr, wl.page_ids, wl.first_offset, wl.page_size,

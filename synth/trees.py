@@ -364,6 +364,49 @@ def flat_control(wl: Workload) -> Workload:
     return out
 
 
+def grow_query_nodes(wl: Workload, tokens: int = 1) -> Workload:
+    """The next decode steps' tree: every node a query sits on gains `tokens`
+    tokens (new logical ids), in free rows of its last page or in new pages
+    appended to the pool; the shape, the other nodes and every existing row
+    stay as they are."""
+    ps = wl.page_size
+    grow = np.zeros(wl.n_nodes, dtype=np.int64)
+    grow[np.unique(wl.query_node)] = tokens
+    node_len = wl.node_len.astype(np.int64) + grow
+    next_lid = int(wl.lid.max()) + 1 if wl.lid.size else 0
+    num_pages = wl.num_pages
+    page_lists, lid_lists = [], []
+    for n in range(wl.n_nodes):
+        pages = [int(p) for p in wl.page_ids[wl.page_ptr[n]:wl.page_ptr[n + 1]]]
+        need = (int(wl.first_offset[n]) + int(node_len[n]) + ps - 1) // ps if node_len[n] > 0 else len(pages)
+        while len(pages) < need:
+            pages.append(num_pages)
+            num_pages += 1
+        page_lists.append(pages)
+        lids = wl.lid[wl.lid_ptr[n]:wl.lid_ptr[n + 1]]
+        if grow[n]:
+            lids = np.concatenate([lids, np.arange(next_lid, next_lid + grow[n], dtype=np.int64)])
+            next_lid += int(grow[n])
+        lid_lists.append(lids)
+    page_ptr = np.zeros(wl.n_nodes + 1, dtype=np.int64)
+    page_ptr[1:] = np.cumsum([len(p) for p in page_lists])
+    lid_ptr = np.zeros(wl.n_nodes + 1, dtype=np.int64)
+    lid_ptr[1:] = np.cumsum([len(x) for x in lid_lists])
+    # the new rows must be free (a page shared with another node may not be)
+    used = wl.row_lids()
+    for n in np.flatnonzero(grow):
+        pos = int(wl.first_offset[n]) + int(wl.node_len[n]) + np.arange(tokens)
+        pages = np.array(page_lists[n], dtype=np.int64)
+        rows = pages[pos // ps] * ps + pos % ps
+        old = rows[rows < used.shape[0]]
+        if np.any(used[old] >= 0):
+            raise ValueError(f"node {n} cannot grow in place: its next page rows hold other tokens")
+    return dataclasses.replace(
+        wl, name=wl.name + f"+{tokens}", node_len=node_len.astype(np.int32), page_ptr=page_ptr,
+        page_ids=np.array([p for pl in page_lists for p in pl], dtype=np.int32), num_pages=num_pages,
+        lid_ptr=lid_ptr, lid=np.concatenate(lid_lists) if lid_lists else wl.lid)
+
+
 def random_tree(seed: int, max_nodes: int = 12, max_len: int = 70, max_depth: int = 4,
                 heads=(4, 2), d: int = 64, dtype: str = "bf16", n_queries: int | None = None,
                 allow_empty: bool = True, random_offsets: bool = True) -> Workload:

@@ -202,3 +202,63 @@ def test_cost_table_interpolation(lib):
     finally:
         lib.cost_set_table(1, "builtin", None, None)
         lib.cost_set_table(2, "builtin", None, None)
+
+
+# ------------------------------------------------------------ incremental plan (next decode step)
+
+def _chunks_per_node(e, n_nodes):
+    cnt = np.zeros(n_nodes, np.int64)
+    for c in range(len(e["chunk_q_ptr"]) - 1):
+        nodes = set(e["chunk_tok_node"][e["chunk_tok_ptr"][c]:e["chunk_tok_ptr"][c + 1]].tolist())
+        if len(nodes) == 1:
+            cnt[nodes.pop()] += 1
+    return cnt
+
+
+@pytest.mark.parametrize("wl", [synth.few_shot(), synth.document_qa()] +
+                         [synth.random_tree(8600 + s, max_nodes=12, max_len=150, heads=(8, 2), d=128,
+                                            dtype="bf16", n_queries=12) for s in range(6)],
+                         ids=lambda w: w.name)
+def test_plan_update_keeps_splits_and_covers(lib, wl):
+    """The next step's plan (query nodes one token longer) covers every
+    (query, token) pair of the grown tree exactly once and keeps each node's
+    KV-axis split."""
+    p = _plan(lib, wl)
+    wl2 = synth.grow_query_nodes(wl, 1)
+    p2 = lib.plan_update(p, _tree(lib, wl2))
+    e, e2 = p.export(), p2.export()
+    assert np.array_equal(_covered_pairs(wl2, e2), _visible_pairs(wl2))
+    c1, c2 = _chunks_per_node(e, wl.n_nodes), _chunks_per_node(e2, wl.n_nodes)
+    grown = np.zeros(wl.n_nodes, bool)
+    grown[np.unique(wl.query_node)] = True
+    # nodes that did not grow are cut exactly as before; grown ones keep their split
+    # unless one more token needs a new tile boundary (never fewer chunks)
+    assert np.array_equal(c1[~grown], c2[~grown])
+    assert np.all(c2[grown] >= c1[grown])
+    assert p2.stats()["n_chunks"] >= p.stats()["n_chunks"]
+
+
+def test_plan_update_skips_the_partition_search(lib):
+    wl = synth.tree_of_thought("gqa")
+    p = _plan(lib, wl)
+    p2 = lib.plan_update(p, _tree(lib, synth.grow_query_nodes(wl, 1)))
+    assert p2.stats()["plan_us"] < p.stats()["plan_us"]
+    assert abs(p2.stats()["cost_lower_bound_us"] - p.stats()["cost_lower_bound_us"]) < 1e-9
+
+
+def test_plan_update_rejects_a_changed_shape(lib):
+    wl = synth.random_tree(8603, max_nodes=12, max_len=150, heads=(8, 2), d=128, dtype="bf16", n_queries=12)
+    p = _plan(lib, wl)
+    t_small = lib.tree_build([5], [-1], [0, 1], [0], num_pages=1)
+    with pytest.raises(lib.PstError) as e:
+        lib.plan_update(p, t_small)
+    assert e.value.code == -1
+    # re-hang a queried node elsewhere: the paths change
+    q0 = int(wl.query_node[0])
+    parent = wl.parent.copy()
+    parent[q0] = -1 if parent[q0] >= 0 else (0 if q0 != 0 else 1)
+    t_moved = lib.tree_build(wl.node_len, parent, wl.page_ptr, wl.page_ids, wl.first_offset, wl.page_size,
+                             wl.num_pages)
+    with pytest.raises(lib.PstError) as e:
+        lib.plan_update(p, t_moved)
+    assert e.value.code == -1

@@ -109,6 +109,30 @@ def test_thin_pac_many_row_blocks(lib, name):
     assert_matches(wl, O, L, K, V, Q, queries=qs)
 
 
+@pytest.mark.parametrize("name", ["few_shot", "random_a", "random_b"])
+def test_plan_update_next_step(lib, name):
+    """Two decode steps: the plan of step 2 (every query node one token longer,
+    new pages appended to the pool) comes from pst_plan_update on step 1's plan."""
+    import torch
+    from prefix_shared_tree_gb300.torch_api import TreeDecodeAttention, to_device
+    wl = synth.few_shot() if name == "few_shot" else synth.random_tree(
+        8600 + (name == "random_b"), max_nodes=12, max_len=150, heads=(8, 2), d=128, dtype="bf16", n_queries=12)
+    att = TreeDecodeAttention.from_workload(wl)
+    K, V = wl.kv_pools()
+    Q = wl.q()
+    O, L = att(to_device(Q, wl.dtype), to_device(K, wl.dtype), to_device(V, wl.dtype))
+    torch.cuda.synchronize()
+    assert_matches(wl, O.cpu().numpy(), L.cpu().numpy(), K, V, Q, queries=range(min(wl.n_queries, 8)))
+    wl2 = synth.grow_query_nodes(wl, 1)
+    att.update_tree(wl2.node_len, wl2.parent, wl2.page_ptr, wl2.page_ids, wl2.first_offset, wl2.num_pages)
+    K2, V2 = wl2.kv_pools()
+    Q2 = wl2.q()
+    O2, L2 = att(to_device(Q2, wl2.dtype), to_device(K2, wl2.dtype), to_device(V2, wl2.dtype))
+    torch.cuda.synchronize()
+    assert att.check_status() == 0
+    assert_matches(wl2, O2.cpu().numpy(), L2.cpu().numpy(), K2, V2, Q2)
+
+
 def test_non_finite_junk_in_unused_page_rows(lib):
     """Rows of a page that no node covers may hold NaN; they never reach O."""
     for seed in range(6):
