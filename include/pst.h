@@ -253,7 +253,7 @@ typedef struct {
     int64_t n_chunks;             /* KV chunks (a node part or a packed subtree)     */
     int64_t n_items;              /* PAC thread blocks: chunk x kv head x row block  */
     int64_t n_tc_items;           /* ... on the tensor-core PAC                      */
-    int64_t n_cc_items;           /* ... on the CUDA-core PAC                        */
+    int64_t n_cc_items;           /* ... on the thin-chunk PAC (tcgen05 thin or CUDA core) */
     int64_t n_partial_rows;       /* partial outputs written per call                */
     int64_t unique_kv_tokens;     /* sum of node lengths                             */
     int64_t kv_tokens_read;       /* tokens loaded per kv head (chunks' page span)   */

@@ -262,3 +262,59 @@ def test_plan_update_rejects_a_changed_shape(lib):
     with pytest.raises(lib.PstError) as e:
         lib.plan_update(p, t_moved)
     assert e.value.code == -1
+
+
+# ------------------------------------------------------------ thin-chunk engine selection
+
+def _thin_item_count(wl, e, thin):
+    G = wl.n_q_heads // wl.n_kv_heads
+    n = 0
+    for c in range(len(e["chunk_q_ptr"]) - 1):
+        if e["chunk_kind"][c] != 0:
+            continue
+        rows = int(e["chunk_q_ptr"][c + 1] - e["chunk_q_ptr"][c]) * G
+        if thin:
+            rb = 4 if rows <= 4 else 8
+            n += -(-rows // rb) * (wl.n_kv_heads // 8)
+        else:
+            rt = 1 if rows <= 1 else 2 if rows <= 2 else 4 if rows <= 4 else 8
+            n += -(-rows // rt) * wl.n_kv_heads
+    return n
+
+
+@pytest.mark.parametrize("case", ["bf16_d128_hkv8", "cuda_core_engine", "d64", "f32", "hkv2"])
+def test_thin_engine_selection_and_items(lib, case):
+    """Thin chunks take the tcgen05 thin PAC (items of 8 kv heads, row blocks of
+    4 or 8) for bf16, d = 128 and Hkv a multiple of 8, else the CUDA-core PAC
+    (one item per kv head and row tile)."""
+    heads, d, dtype, opts = (32, 8), 128, "bf16", {}
+    if case == "cuda_core_engine":
+        opts = dict(thin_engine="cuda_core")
+    elif case == "d64":
+        d = 64
+    elif case == "f32":
+        dtype = "f32"
+    elif case == "hkv2":
+        heads = (8, 2)
+    wl = synth.random_tree(8620, max_nodes=14, max_len=200, heads=heads, d=d, dtype=dtype, n_queries=10)
+    p = _plan(lib, wl, **opts)
+    e = p.export()
+    thin = case == "bf16_d128_hkv8"
+    assert p.stats()["n_cc_items"] == _thin_item_count(wl, e, thin)
+    assert np.array_equal(_covered_pairs(wl, e), _visible_pairs(wl))
+
+
+def test_thin_chunks_start_on_page_row_boxes(lib):
+    """The thin PAC's tiles are 16-row page boxes: a thin chunk that does not
+    start its node starts on a multiple of 16 in page space."""
+    for s in range(6):
+        wl = synth.random_tree(8630 + s, max_nodes=14, max_len=400, heads=(32, 8), d=128, dtype="bf16",
+                               n_queries=10)
+        e = _plan(lib, wl, split_policy="uniform", fixed_chunk=64).export()
+        for c in range(len(e["chunk_q_ptr"]) - 1):
+            if e["chunk_kind"][c] != 0:
+                continue
+            n0 = int(e["chunk_tok_node"][e["chunk_tok_ptr"][c]])
+            t0 = int(e["chunk_tok_t"][e["chunk_tok_ptr"][c]])
+            if t0 > 0:
+                assert (int(wl.first_offset[n0]) + t0) % 16 == 0
