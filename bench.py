@@ -225,6 +225,19 @@ def bench_config(args, wl, world):
 
 # ------------------------------------------------------------------ arms
 
+def max_over_ranks(values, world, device="cpu"):
+    """Per-rank timings -> their maximum over the ranks (every rank gets it).
+    Replicas run independently; the job's step time is the slowest replica's.
+    `device` is where the collective's tensor lives (cuda for NCCL, cpu for gloo)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
 def run_ours(args, rank, world):
     import numpy as np
     import torch
@@ -311,10 +324,7 @@ def run_ours(args, rank, world):
     e2e_us = e0.elapsed_time(e1) * 1e3 / e2e_steps
 
     us = total_ms * 1e3 / args.steps
-    if world > 1:
-        t = torch.tensor([us, e2e_us], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        us, e2e_us = float(t[0]), float(t[1])
+    us, e2e_us = max_over_ranks([us, e2e_us], world, dev)
     if rank != 0:
         return None
 
