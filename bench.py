@@ -272,6 +272,8 @@ def run_ours(args, rank, world):
     att = TreeDecodeAttention.from_workload(wl, device=dev, **plan_opts)
     plan_wall_us = (time.perf_counter() - t0) * 1e6
     st = att.plan.stats()
+    # the next decode step's plan on the same tree (host only, not uploaded)
+    update_us = pst.plan_update(att.plan, att.tree).stats()["plan_us"]
     ex = att.plan.export()
     O = [torch.empty((wl.n_queries, wl.n_q_heads, wl.d), dtype=torch.float32, device=dev) for _ in range(copies)]
     L = [torch.empty((wl.n_queries, wl.n_q_heads), dtype=torch.float32, device=dev) for _ in range(copies)]
@@ -377,6 +379,7 @@ def run_ours(args, rank, world):
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(dom_achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": alg[dom]},
         "plan": {"plan_us": round(st["plan_us"], 1), "plan_wall_us": round(plan_wall_us, 1),
+                 "plan_update_us": round(update_us, 1),
                  "predicted_makespan_us": round(st["predicted_makespan_us"], 2),
                  "n_chunks": st["n_chunks"], "n_items": st["n_items"], "n_tc_items": st["n_tc_items"],
                  "n_cc_items": st["n_cc_items"], "n_partial_rows": st["n_partial_rows"]},
