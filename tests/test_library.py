@@ -318,3 +318,18 @@ def test_thin_chunks_start_on_page_row_boxes(lib):
             t0 = int(e["chunk_tok_t"][e["chunk_tok_ptr"][c]])
             if t0 > 0:
                 assert (int(wl.first_offset[n0]) + t0) % 16 == 0
+
+
+def test_grow_query_nodes_input():
+    """The grown-tree generator keeps every existing row and adds k new tokens
+    to each node a query sits on, in free rows."""
+    wl = synth.random_tree(8605, max_nodes=12, max_len=150, heads=(8, 2), d=128, dtype="bf16", n_queries=12)
+    w2 = synth.grow_query_nodes(wl, 3)
+    q_nodes = np.unique(wl.query_node)
+    want = wl.node_len.astype(np.int64).copy()
+    want[q_nodes] += 3
+    assert np.array_equal(w2.node_len, want)
+    r1, r2 = wl.row_lids(), w2.row_lids()
+    assert np.array_equal(r2[:r1.size][r1 >= 0], r1[r1 >= 0])
+    assert (r2 >= 0).sum() == (r1 >= 0).sum() + 3 * q_nodes.size
+    assert len(np.unique(r2[r2 >= 0])) == (r2 >= 0).sum()
