@@ -41,34 +41,60 @@ def to_f64(x: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(dtype)
 
 
-def path_kv(tr, K_pool, V_pool, path) -> tuple[np.ndarray, np.ndarray]:
-    """K, V of the concatenated path nodes (node order, then token order), read
-    through each node's own pages: fp64 arrays [L, Hkv, d]."""
+def node_kv(tr, K_pool, V_pool, n):
+    """K, V of node n's tokens in token order, read through the node's own
+    pages: fp64 arrays [Hkv, len, d] (each kv head's block contiguous)."""
+    pages, rows = _tree.node_rows(tr, n)
+    k = to_f64(K_pool[pages, :, rows, :], tr.dtype)   # [len, Hkv, d]
+    v = to_f64(V_pool[pages, :, rows, :], tr.dtype)
+    return np.ascontiguousarray(k.transpose(1, 0, 2)), np.ascontiguousarray(v.transpose(1, 0, 2))
+
+
+def path_kv(tr, K_pool, V_pool, path, cache=None) -> tuple[list, list]:
+    """K, V of the path's nodes in path order (each node's tokens in token
+    order, read through its own pages): two lists of fp64 blocks [Hkv, len, d],
+    whose concatenation along the token axis is the path's K and V.
+
+    ``cache`` (optional dict, node id -> node_kv result) keeps the blocks of
+    nodes already read, so that queries sharing a prefix decode it once."""
     ks, vs = [], []
     for n in path:
+        n = int(n)
         if int(tr.node_len[n]) == 0:
             continue
-        pages, rows = _tree.node_rows(tr, n)
-        ks.append(to_f64(K_pool[pages, :, rows, :], tr.dtype))
-        vs.append(to_f64(V_pool[pages, :, rows, :], tr.dtype))
-    Hkv, d = K_pool.shape[1], K_pool.shape[3]
-    if not ks:
-        z = np.zeros((0, Hkv, d))
-        return z, z.copy()
-    return np.concatenate(ks), np.concatenate(vs)
+        if cache is not None and n in cache:
+            k, v = cache[n]
+        else:
+            k, v = node_kv(tr, K_pool, V_pool, n)
+            if cache is not None:
+                cache[n] = (k, v)
+        ks.append(k)
+        vs.append(v)
+    return ks, vs
 
 
-def attention_definition(q: np.ndarray, K: np.ndarray, V: np.ndarray):
-    """One query row q [d] against K, V [L, d]: (o [d], lse) with
-    o = softmax(q K^T / sqrt(d)) V and lse = ln sum_j exp(s_j), both fp64."""
+def attention_definition(q: np.ndarray, K, V):
+    """Query rows q [d] (or [R, d]) against K, V [L, d]: (o, lse) with
+    o = softmax(q K^T / sqrt(d)) V and lse = ln sum_j exp(s_j) per row, in
+    fp64; o is [d] (or [R, d]) and lse a float (or [R]).
+
+    K and V may also be given as lists of row blocks [L_i, d] (a path's nodes
+    in order) that stack to the full K and V: the scores are then the stacked
+    blocks' scores, and o the sum of the blocks' weighted rows."""
+    Ks = list(K) if isinstance(K, (list, tuple)) else [K]
+    Vs = list(V) if isinstance(V, (list, tuple)) else [V]
     d = q.shape[-1]
-    s = (K @ q) / math.sqrt(d)
-    m = np.max(s)
-    e = np.exp(s - m)
-    total = np.sum(e)
-    lse = m + math.log(total)
-    o = (np.exp(s - lse)) @ V
-    return o, lse
+    s = np.concatenate([Kb @ q.T for Kb in Ks], axis=0) / math.sqrt(d)   # s_j = q . k_j / sqrt(d)
+    m = np.max(s, axis=0)
+    total = np.sum(np.exp(s - m), axis=0)
+    lse = m + np.log(total)
+    p = np.exp(s - lse)                        # softmax weights, token axis first
+    o = 0.0
+    j = 0
+    for Vb in Vs:
+        o = o + p[j:j + Vb.shape[0]].T @ Vb
+        j += Vb.shape[0]
+    return o, (float(lse) if np.ndim(lse) == 0 else lse)
 
 
 def decode_attention(tr, K_pool, V_pool, Q, queries=None):
@@ -85,15 +111,23 @@ def decode_attention(tr, K_pool, V_pool, Q, queries=None):
     O = np.full((B, Hq, d), np.nan)
     LSE = np.full((B, Hq), np.nan)
     qs = range(B) if queries is None else queries
+    cache: dict = {}
     for qi in qs:
         path = _tree.root_path(tr.parent, int(tr.query_node[qi]))
-        Kq, Vq = path_kv(tr, K_pool, V_pool, path)
-        if Kq.shape[0] == 0:
+        # keep only the decoded blocks of this query's path (queries listed in
+        # tree order share most of theirs)
+        on_path = set(int(n) for n in path)
+        for n in list(cache):
+            if n not in on_path:
+                del cache[n]
+        Kq, Vq = path_kv(tr, K_pool, V_pool, path, cache)
+        if not Kq:
             raise ValueError(f"query {qi} sees no token")
         qf = to_f64(Q[qi], tr.dtype)
-        for h in range(Hq):
-            g = h // G
-            O[qi, h], LSE[qi, h] = attention_definition(qf[h], Kq[:, g, :], Vq[:, g, :])
+        for g in range(Hkv):
+            # the q-heads h with h // G == g read kv head g
+            O[qi, g * G:(g + 1) * G], LSE[qi, g * G:(g + 1) * G] = attention_definition(
+                qf[g * G:(g + 1) * G], [k[g] for k in Kq], [v[g] for v in Vq])
     return O, LSE
 
 

@@ -355,10 +355,12 @@ def test_cycle_detected():
 def _planted(monkeypatch, kind):
     if kind == "scale":
         def bad(q, K, V):
-            s = (K @ q) / q.shape[-1]
-            m = np.max(s)
-            lse = m + math.log(np.sum(np.exp(s - m)))
-            return np.exp(s - lse) @ V, lse
+            K = np.concatenate(K) if isinstance(K, list) else K
+            V = np.concatenate(V) if isinstance(V, list) else V
+            s = (K @ q.T) / q.shape[-1]
+            m = np.max(s, axis=0)
+            lse = m + np.log(np.sum(np.exp(s - m), axis=0))
+            return np.exp(s - lse).T @ V, lse
         monkeypatch.setattr(oa, "attention_definition", bad)
     elif kind == "gqa":
         orig = oa.decode_attention
@@ -372,7 +374,8 @@ def _planted(monkeypatch, kind):
                 Kq, Vq = oa.path_kv(tr, K_pool, V_pool, path)
                 qf = oa.to_f64(Q[qi], tr.dtype)
                 for h in range(Hq):
-                    O[qi, h], L[qi, h] = oa.attention_definition(qf[h], Kq[:, h % Hkv], Vq[:, h % Hkv])
+                    O[qi, h], L[qi, h] = oa.attention_definition(qf[h], [k[h % Hkv] for k in Kq],
+                                                                  [v[h % Hkv] for v in Vq])
             return O, L
         monkeypatch.setattr(oa, "decode_attention", bad)
     elif kind == "drop_own_node":
@@ -389,8 +392,8 @@ def _planted(monkeypatch, kind):
     elif kind == "transposed_v":
         orig = oa.path_kv
 
-        def bad(tr, K, V, path):
-            k, v = orig(tr, K, V, path)
+        def bad(tr, K, V, path, cache=None):
+            k, v = orig(tr, K, V, path, cache)
             return v, k
         monkeypatch.setattr(oa, "path_kv", bad)
 
