@@ -317,6 +317,17 @@ int pst_cost_set_table(int32_t kind, int32_t n_r, const float* rows, int32_t n_n
                        const float* tokens, const float* us);
 double pst_cost_estimate(int32_t kind, double rows, double tokens);
 
+/* The partitioner's list schedule, exported for checks (host only): CoDec,
+ * "workload balancing", assigns the sub-tasks to the m thread-block slots
+ * largest first, each to the least-loaded slot (Graham's list scheduling,
+ * whose makespan is at most (2 - 1/m) times the optimum; largest-first order
+ * tightens that to 4/3 - 1/(3m)). n costs (>= 0) go onto m slots; slot[i]
+ * (nullable) receives task i's slot in [0, m), ties going to the lowest slot
+ * index and equal costs to the lower task index first; *makespan (nullable)
+ * the largest slot load. Errors: PST_EINVAL (n < 0, m <= 0, a negative or
+ * NaN cost). */
+int pst_list_schedule(int32_t n, const double* cost, int32_t m, int32_t* slot, double* makespan);
+
 const char* pst_last_error(void);
 
 #ifdef __cplusplus

@@ -243,9 +243,11 @@ struct ItemCost {
     int8_t klass;   // launch: 0 tensor core, 1 tensor core exact P, 2 + k CUDA core row tile 8 >> k
 };
 
-// Graham list scheduling (largest first) of item costs onto m slots: returns
-// the makespan.
-double list_schedule(std::vector<ItemCost>& v, int m) {
+// Graham list scheduling (largest first) of item costs onto m slots: sorts
+// v into that order and returns the makespan; slot (nullable) receives, per
+// position of the sorted v, the slot the item went to (the least-loaded one,
+// the lowest index among equals).
+double list_schedule(std::vector<ItemCost>& v, int m, std::vector<int>* slot = nullptr) {
     std::sort(v.begin(), v.end(), [](const ItemCost& a, const ItemCost& b) {
         if (a.cost != b.cost) return a.cost > b.cost;
         if (a.chunk != b.chunk) return a.chunk < b.chunk;
@@ -255,12 +257,14 @@ double list_schedule(std::vector<ItemCost>& v, int m) {
     using Slot = std::pair<double, int>;
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> pq;
     for (int i = 0; i < m; ++i) pq.push({0.0, i});
+    if (slot) slot->assign(v.size(), 0);
     double mk = 0;
-    for (const auto& it : v) {
+    for (size_t k = 0; k < v.size(); ++k) {
         Slot s = pq.top();
         pq.pop();
-        s.first += it.cost;
+        s.first += v[k].cost;
         mk = std::max(mk, s.first);
+        if (slot) (*slot)[k] = s.second;
         pq.push(s);
     }
     return mk;
@@ -998,5 +1002,20 @@ extern "C" int pst_plan_export(const pst_plan* p, pst_export* e) {
     }
     if (e->chunk_q_ptr) e->chunk_q_ptr[nc] = qacc;
     if (e->chunk_tok_ptr) e->chunk_tok_ptr[nc] = tacc;
+    return PST_OK;
+}
+
+extern "C" int pst_list_schedule(int32_t n, const double* cost, int32_t m, int32_t* slot, double* makespan) {
+    if (n < 0 || m <= 0 || (n > 0 && !cost)) return fail(PST_EINVAL, "list_schedule: bad argument");
+    std::vector<ItemCost> v((size_t)n);
+    for (int32_t i = 0; i < n; ++i) {
+        if (!(cost[i] >= 0.0)) return fail(PST_EINVAL, "list_schedule: costs must be >= 0");
+        v[i] = {cost[i], i, 0, 0, 0};
+    }
+    std::vector<int> s;
+    const double mk = list_schedule(v, m, &s);
+    if (slot)
+        for (int32_t k = 0; k < n; ++k) slot[v[k].chunk] = s[k];
+    if (makespan) *makespan = mk;
     return PST_OK;
 }

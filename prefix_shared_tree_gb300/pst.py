@@ -99,6 +99,7 @@ def lib() -> C.CDLL:
         "pst_plan_export": (C.c_int, [vp, C.POINTER(Export)]),
         "pst_cost_set_table": (C.c_int, [i32, i32, vp, i32, vp, vp]),
         "pst_cost_estimate": (C.c_double, [i32, C.c_double, C.c_double]),
+        "pst_list_schedule": (C.c_int, [i32, vp, i32, vp, C.POINTER(C.c_double)]),
         "pst_last_error": (C.c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -300,3 +301,14 @@ def cost_set_table(kind: int, rows, tokens, us):
 
 def cost_estimate(kind: int, rows: float, tokens: float) -> float:
     return float(lib().pst_cost_estimate(kind, rows, tokens))
+
+
+def list_schedule(costs, m: int):
+    """The planner's largest-first list schedule of `costs` onto m slots:
+    (slot of each task, makespan)."""
+    c, cp = _arr(costs, np.float64)
+    n = 0 if c is None else c.size
+    slot = np.zeros(max(n, 1), dtype=np.int32)
+    mk = C.c_double(0.0)
+    _check(lib().pst_list_schedule(n, cp, int(m), slot.ctypes.data_as(C.c_void_p), C.byref(mk)))
+    return slot[:n], float(mk.value)
