@@ -20,16 +20,17 @@
 //               from one thread: S = Q K^T (M=128, N=128, Q and K from shared
 //               memory) and O += P V (M=128, N=d, P from tensor memory, V
 //               MN-major from shared memory);
-//   warps 4-11  two softmax warpgroups, one thread per tensor-memory lane.
-//               With more than 128 rows the MMA warp alternates between the
-//               two 128-row halves (P V and S of half 0, then of half 1) and
-//               both groups work on each half as soon as its S is ready: group
-//               w takes S columns [64w, 64w + 64), the row max is the larger of
-//               the two groups' maxima (exchanged through shared memory), so a
-//               half's softmax takes half as long and overlaps the other
-//               half's MMAs. With at most 128 rows the groups take alternate
-//               tiles into separate S buffers and O accumulators and merge at
-//               the end (split-KV inside the block).
+//   softmax warpgroups, one thread per tensor-memory lane: four above 128
+//               rows (warps 4-19), two at most (warps 4-11). Above 128 rows
+//               the MMA warp alternates between the two 128-row halves (P V
+//               and S of half 0, then of half 1) and all four groups work on
+//               each half as soon as its S is ready: group w takes S columns
+//               [32w, 32w + 32), the row max (and, for the precision guard
+//               below, the row sum so far) is combined from the groups'
+//               values exchanged through shared memory, so a half's softmax
+//               overlaps the other half's MMAs. With at most 128 rows the two
+//               groups take alternate tiles into separate S buffers and O
+//               accumulators and merge at the end (split-KV inside the block).
 // The first warpgroup hands registers to the softmax warpgroups
 // (setmaxnreg), which hold a whole 128-column row of S in registers.
 // Tensor memory: S of half w in columns [128w, 128w+128), O of half w in
@@ -38,13 +39,20 @@
 // tcgen05 MMAs from one thread run in issue order.
 // Softmax works in the log2 domain with 1/sqrt(d) folded into one FMA; the
 // running max only moves (and O is rescaled in tensor memory) when it grows
-// by more than 2^8, so the result is exact in fp32. The EXACT instance (chunks
-// of nodes shorter than the plan's p_bf16_min_tokens) splits P into bf16 hi + lo parts
-// (p = hi + lo to ~2^-16), which makes P V as accurate as an fp32 product; the
-// other rounds P once to bf16, whose relative error (2^-8 per weight, random
-// in sign) averages out over a long node's many weights. Scores a row may
-// not see (tile edges, bit causal masks) are set to -inf in tensor memory
-// before the row is loaded, which keeps masking out of the hot code.
+// by more than 2^8, so the result is exact in fp32.
+// Precision of P in P V. The EXACT instance (chunks of nodes shorter than the
+// plan's p_bf16_min_tokens) splits every weight into a bf16 hi part and the
+// bf16 remainder lo (p = hi + lo to ~2^-16) and multiplies V by both, which
+// makes P V as accurate as an fp32 product. The other instance rounds each
+// weight once to bf16 (relative error at most 2^-9) and keeps the row sum of
+// the rounded weights, so O is an exact convex combination of V rows with
+// slightly perturbed weights: a weight's error moves O by at most its share
+// p (1 - p) of 2^-9 |v - O|, and the errors of many small weights, random in
+// sign, average out. A weight that holds a large share of its row's sum so
+// far (above kExactShare of it) is made exact instead: the running max moves
+// to it (rescaling O), so it becomes 2^0 = 1 exactly. Scores a row may not
+// see (tile edges, bit causal masks) are set to -inf in tensor memory before
+// the row is loaded, which keeps masking out of the hot code.
 #include "dev_common.cuh"
 #include "umma.cuh"
 
@@ -70,6 +78,9 @@ struct UWarps {
 constexpr int kUT = kTcTileTokens;   // tokens per tile
 constexpr int kKProducers = 2;       // threads issuing a K tile's TMA loads
 constexpr float kLazyRescale = 8.f;
+// A weight above this share of its row's softmax sum so far (itself included)
+// is made exact (see the precision note above).
+constexpr float kExactShare = 0.125f;
 
 template <int D>
 struct UmmaLayout {
@@ -88,7 +99,8 @@ struct UmmaLayout {
     static constexpr uint32_t kQ = kV + VST * kOp;                 // 2 halves x NSLAB slabs
     static constexpr uint32_t kXchg = kQ + 2 * NSLAB * kQSlab;     // 128 x (m, l) for the split-KV merge
     static constexpr uint32_t kRed = kXchg + 128 * 8;              // [2][4][128] row maxima, then [2][4][128] sums
-    static constexpr uint32_t kBars = kRed + 2048 * 4;
+    static constexpr uint32_t kLRed = kRed + 2048 * 4;             // [2][4][128] row sums of the earlier tiles
+    static constexpr uint32_t kBars = kLRed + 1024 * 4;
     // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], q_ready, s_full[2], p_full[2], mma_done,
     // xchg[2], lfin
     static constexpr int kNumBars = 2 * KST + 2 * VST + 9;
@@ -159,7 +171,8 @@ __device__ __forceinline__ void mask_in_tmem(uint32_t s_addr, int col0, int c_lo
 
 // P = 2^(x*sl - m) for NC scores into tensor memory as bf16 pairs (P[2i],
 // P[2i+1] in one column): at p_hi, and with EXACT the remainder p - hi at
-// p_lo. Returns the row sum of the unrounded weights.
+// p_lo. Returns the row sum of the weights P V multiplies: the unrounded ones
+// with EXACT (hi + lo), the rounded ones (hi) without.
 template <int NC, bool EXACT>
 __device__ __forceinline__ float softmax_p(const float (&x)[NC], float sl, float nmu, uint32_t p_hi, uint32_t p_lo) {
     const u64 sl2 = pk2(sl, sl), nmu2 = pk2(nmu, nmu);
@@ -174,8 +187,8 @@ __device__ __forceinline__ float softmax_p(const float (&x)[NC], float sl, float
                 upk2(fma2(pk2(x[32 * q + 2 * c], x[32 * q + 2 * c + 1]), sl2, nmu2), a, b);
                 a = fast_exp2(a);
                 b = fast_exp2(b);
-                sum2[c & 3] = add2(sum2[c & 3], pk2(a, b));
                 hi[c] = bf16x2_bits(a, b);
+                sum2[c & 3] = add2(sum2[c & 3], pk2(bf16lo(hi[c]), bf16hi(hi[c])));
             }
             umma::st16(p_hi + 16 * q, hi);
         }
@@ -485,6 +498,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             constexpr int kCols = 128 / NG;
             nk = n;
             float* red = reinterpret_cast<float*>(base + L::kRed);   // [half][group][128]
+            float* lred = reinterpret_cast<float*>(base + L::kLRed); // [half][group][128]
             float m_ref[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
             uint64_t mask_h[2] = {~0ull, ~0ull};
             if (masked_chunk) {
@@ -508,13 +522,25 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                     float x[kCols];
                     ld_cols<kCols>(s_addr + col0, x);
                     red[(NG * h + w) * 128 + r] = row_max(x);
+                    if (!EXACT) lred[(NG * h + w) * 128 + r] = lsum[h];
                     mbar_arrive(xchg_bar + 8 * h);
                     if (!__all_sync(0xffffffffu, mbar_wait(xchg_bar + 8 * h, k & 1, P.status))) { ok = false; break; }
                     float mx = red[(NG * h) * 128 + r];
 #pragma unroll
                     for (int g = 1; g < NG; ++g) mx = fmaxf(mx, red[(NG * h + g) * 128 + r]);
                     const float mxs = mx * sl;   // scale > 0: max commutes with it
-                    const bool grow = (m_ref[h] == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref[h] + kLazyRescale);
+                    bool grow = (m_ref[h] == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref[h] + kLazyRescale);
+                    if (!EXACT && !grow && mx != -INFINITY && mxs > m_ref[h]) {
+                        // the tile's largest weight, 2^(mxs - m_ref) <= 2^8, against
+                        // the row's sum so far (every group adds the same values in
+                        // the same order, so all take the same decision): if it is a
+                        // large share, move the max to it so that it becomes 1 exactly
+                        float lb = 0.f;
+#pragma unroll
+                        for (int g = 0; g < NG; ++g) lb += lred[(NG * h + g) * 128 + r];
+                        const float wmax = fast_exp2(mxs - m_ref[h]);
+                        grow = wmax > kExactShare * (lb + wmax);
+                    }
                     float alpha = 1.f;
                     bool rescale = false;
                     if (grow) {
@@ -568,7 +594,13 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 ld_cols<kUT>(s_addr, x);
                 const float mx = row_max(x);
                 const float mxs = mx * sl;
-                const bool grow = (m_ref == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref + kLazyRescale);
+                bool grow = (m_ref == -INFINITY) ? (mx != -INFINITY) : (mxs > m_ref + kLazyRescale);
+                if (!EXACT && !grow && mx != -INFINITY && mxs > m_ref) {
+                    // the tile's largest weight against the group's sum so far:
+                    // if it is a large share, it becomes 1 exactly (see above)
+                    const float wmax = fast_exp2(mxs - m_ref);
+                    grow = wmax > kExactShare * (l + wmax);
+                }
                 float alpha = 1.f;
                 bool rescale = false;
                 if (grow) {
