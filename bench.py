@@ -47,7 +47,13 @@ WORKLOADS = {
     "tree_of_thought_mqa": lambda s: s.tree_of_thought("mqa"),
     "document_qa_flat": lambda s: s.flat_control(s.document_qa()),
     "few_shot_flat": lambda s: s.flat_control(s.few_shot()),
+    "speculative_flat": lambda s: s.flat_control(s.speculative()),
 }
+
+# configurations measured next to the headline in the same run (the other
+# workloads of the pages, and the no-sharing flat controls of the shared ones)
+PER_CONFIG = ["few_shot", "speculative", "tree_of_thought_gqa", "tree_of_thought_mha", "tree_of_thought_mqa",
+              "tiny_two_level", "document_qa_flat", "few_shot_flat", "speculative_flat"]
 
 DESCRIPTIONS = {
     "document_qa": "document QA: 32768-token shared prefix + 64 suffixes U{64..512}, 1 query each; "
@@ -66,9 +72,13 @@ def parse():
     ap.add_argument("--warmup", type=int, default=30)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="document_qa", choices=sorted(WORKLOADS))
-    ap.add_argument("--timed-steps", type=int, default=256, help="steps with per-kernel events")
+    ap.add_argument("--timer-steps", type=int, default=64,
+                    help="steps of a separate loop with the library's per-group events (after the timed loop)")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the other workloads")
+    ap.add_argument("--per-config", default=",".join(PER_CONFIG), help="comma-separated workloads for per_config")
     ap.add_argument("--cpu-sample-s", type=float, default=12.0)
-    ap.add_argument("--ref-budget-s", type=float, default=90.0)
+    ap.add_argument("--ref-budget-s", type=float, default=150.0,
+                    help="host seconds the reference arm's warm-up and timed steps may take")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--plan-opt", action="append", default=[],
                     help="planner option key=value (split_policy, fixed_chunk, tc_min_rows, tc_engine, ...)")
@@ -238,105 +248,59 @@ def max_over_ranks(values, world, device="cpu"):
     return [float(x) for x in t.cpu()]
 
 
-def run_ours(args, rank, world):
+def _plan_opts(args):
+    plan_opts = {}
+    for kv in args.plan_opt:
+        k, v = kv.split("=", 1)
+        plan_opts[k] = int(v) if v.lstrip("-").isdigit() else v
+    return plan_opts
+
+
+def device_inputs(name, dev, copies):
+    """(workload, [K], [V], [Q], Q host array): `copies` device copies of the
+    pools and queries. A flat control's pools are filled on the device from
+    its shared workload's pools (a token's K/V depend on its logical id only)."""
     import numpy as np
     import torch
 
     import synth
-    from prefix_shared_tree_gb300 import build as _build
-    _build.build()
-    from prefix_shared_tree_gb300 import pst
-    from prefix_shared_tree_gb300.torch_api import TreeDecodeAttention, to_device
+    from prefix_shared_tree_gb300.torch_api import to_device
+    if name.endswith("_flat"):
+        base = WORKLOADS[name[:-len("_flat")]](synth)
+        wl = synth.flat_control(base)
+        Kb, Vb = base.kv_pools()
+        src = torch.from_numpy(np.maximum(synth.source_rows(base, wl), 0)).to(dev)
 
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    torch.cuda.set_device(dev)
-    wl = WORKLOADS[args.workload](synth)
-    K_np, V_np = wl.kv_pools()
+        def gather(pool):
+            P, H, S, D = pool.shape
+            rows = to_device(pool, wl.dtype, dev).permute(0, 2, 1, 3).reshape(P * S, H, D)
+            out = rows[src].reshape(wl.num_pages, S, H, D).permute(0, 2, 1, 3).contiguous()
+            del rows
+            return out
+        Kd, Vd = [gather(Kb)], [gather(Vb)]
+        del Kb, Vb
+    else:
+        wl = WORKLOADS[name](synth)
+        K_np, V_np = wl.kv_pools()
+        Kd, Vd = [to_device(K_np, wl.dtype, dev)], [to_device(V_np, wl.dtype, dev)]
+        del K_np, V_np
     Q_np = wl.q()
-    U = wl.unique_kv_bytes()
-    copies = rotating_copies(U)
-    Kd = [to_device(K_np, wl.dtype, dev)]
-    Vd = [to_device(V_np, wl.dtype, dev)]
     Qd = [to_device(Q_np, wl.dtype, dev)]
     for _ in range(copies - 1):
         Kd.append(Kd[0].clone())
         Vd.append(Vd[0].clone())
         Qd.append(Qd[0].clone())
-    del K_np, V_np
+    return wl, Kd, Vd, Qd, Q_np
 
-    t0 = time.perf_counter()
-    plan_opts = {}
-    for kv in args.plan_opt:
-        k, v = kv.split("=", 1)
-        plan_opts[k] = int(v) if v.lstrip("-").isdigit() else v
-    att = TreeDecodeAttention.from_workload(wl, device=dev, **plan_opts)
-    plan_wall_us = (time.perf_counter() - t0) * 1e6
-    st = att.plan.stats()
-    # the next decode step's plan on the same tree (host only, not uploaded)
-    update_us = pst.plan_update(att.plan, att.tree).stats()["plan_us"]
-    ex = att.plan.export()
-    O = [torch.empty((wl.n_queries, wl.n_q_heads, wl.d), dtype=torch.float32, device=dev) for _ in range(copies)]
-    L = [torch.empty((wl.n_queries, wl.n_q_heads), dtype=torch.float32, device=dev) for _ in range(copies)]
-    stream = torch.cuda.current_stream(dev)
 
-    for i in range(max(3, args.warmup)):
-        c = i % copies
-        att(Qd[c], Kd[c], Vd[c], O[c], L[c])
-    torch.cuda.synchronize(dev)
-    if att.check_status() != 0:
-        raise RuntimeError("device status word set during warm-up")
-
-    timer = pst.Timer(max(1, min(args.timed_steps, args.steps)))
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize(dev)
-    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
-        ev0.record(stream)
-        for i in range(args.steps):
-            c = i % copies
-            att(Qd[c], Kd[c], Vd[c], O[c], L[c], timer=timer if i < args.timed_steps else None)
-        ev1.record(stream)
-        torch.cuda.synchronize(dev)
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = ev0.elapsed_time(ev1)
-    kern_ms, kern_calls = timer.read()
-    if att.check_status() != 0:
-        raise RuntimeError("device status word set during the timed region")
-
-    # e2e: per step, Q from pinned host -> device, decode, O and LSE back to pinned host
-    Qh = torch.from_numpy(Q_np.view(np.int16) if wl.dtype == "bf16" else Q_np).pin_memory()
-    Oh = torch.empty(O[0].shape, dtype=torch.float32).pin_memory()
-    Lh = torch.empty(L[0].shape, dtype=torch.float32).pin_memory()
-    Qstage = torch.empty(Qh.shape, dtype=Qh.dtype, device=dev)
-    e2e_steps = max(10, args.steps // 4)
-    torch.cuda.synchronize(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
-        c = i % copies
-        Qstage.copy_(Qh, non_blocking=True)
-        qv = Qstage.view(torch.bfloat16) if wl.dtype == "bf16" else Qstage
-        att(qv, Kd[c], Vd[c], O[c], L[c])
-        Oh.copy_(O[c], non_blocking=True)
-        Lh.copy_(L[c], non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_us = e0.elapsed_time(e1) * 1e3 / e2e_steps
-
-    us = total_ms * 1e3 / args.steps
-    us, e2e_us = max_over_ranks([us, e2e_us], world, dev)
-    if rank != 0:
-        return None
-
-    peak, peak_src = measured_peaks()
-    achieved_gbs = U / (us * 1e-6) / 1e9
-    # per-kernel algorithmic bytes: unique KV of the chunks each PAC kernel reads
+def algorithmic_bytes(wl, ex, st, plan_opts):
+    """Unique K/V bytes of the chunks each PAC launch group reads, and POR's
+    partial-row traffic."""
+    import numpy as np
     per_tok = wl.n_kv_heads * 2 * wl.d * wl.elem_bytes
     ntok = np.diff(ex["chunk_tok_ptr"])
     kinds = ex["chunk_kind"]
-    # tensor-core chunks shorter than p_bf16_min_tokens run in the exact-P launch (tcgen05 engine)
+    # tensor-core chunks of nodes shorter than p_bf16_min_tokens run in the exact-P launch (tcgen05 engine)
     thr = int(plan_opts.get("p_bf16_min_tokens", 0)) or 1024
     thr = np.inf if thr < 0 else thr
     tok_ptr = ex["chunk_tok_ptr"]
@@ -344,25 +308,178 @@ def run_ours(args, rank, world):
                             if len(set(ex["chunk_tok_node"][tok_ptr[c]:tok_ptr[c + 1]].tolist())) == 1 else 0
                             for c in range(len(ntok))])
     exact = (kinds == 1) & (node_tokens < thr) & (plan_opts.get("tc_engine", "tcgen05") == "tcgen05")
-    alg = {"pac_tc": int(ntok[(kinds == 1) & ~exact].sum()) * per_tok,
-           "pac_tc_exact": int(ntok[exact].sum()) * per_tok,
-           "pac_thin": int(ntok[kinds == 0].sum()) * per_tok,
-           "por": int(st["n_partial_rows"]) * (wl.d * 4 + 4) + wl.n_queries * wl.n_q_heads * (wl.d * 4 + 4)}
-    shares = {k: v / max(1e-9, sum(kern_ms.values())) for k, v in kern_ms.items()}
-    # the PAC launch groups start together; each group's time runs from the
-    # call's start to its end. The dominant kernel is the one with the most bytes.
+    return {"pac_tc": int(ntok[(kinds == 1) & ~exact].sum()) * per_tok,
+            "pac_tc_exact": int(ntok[exact].sum()) * per_tok,
+            "pac_thin": int(ntok[kinds == 0].sum()) * per_tok,
+            "por": int(st["n_partial_rows"]) * (wl.d * 4 + 4) + wl.n_queries * wl.n_q_heads * (wl.d * 4 + 4)}
+
+
+def measure(name, args, dev, steps, warmup, timer_steps, plan_opts, e2e=False, world=1):
+    """Times `steps` decode steps of workload `name` (after `warmup`), with no
+    per-group events inside the timed loop; then `timer_steps` steps with the
+    library's per-group events; optionally the end-to-end loop. Returns a dict
+    (times in us)."""
+    import numpy as np
+    import torch
+
+    from prefix_shared_tree_gb300 import pst
+    from prefix_shared_tree_gb300.torch_api import TreeDecodeAttention
+
+    peak, _ = measured_peaks()
+    # rotate over device copies whose total exceeds L2 (the flat controls are far larger)
+    probe = WORKLOADS[name[:-5] if name.endswith("_flat") else name]
+    copies_hint = None
+    wl0 = None
+    if not name.endswith("_flat"):
+        import synth
+        wl0 = probe(synth)
+        copies_hint = rotating_copies(wl0.unique_kv_bytes())
+    wl, Kd, Vd, Qd, Q_np = device_inputs(name, dev, copies_hint or 2)
+    U = wl.unique_kv_bytes()
+    copies = len(Kd)
+    t0 = time.perf_counter()
+    att = TreeDecodeAttention.from_workload(wl, device=dev, **plan_opts)
+    plan_wall_us = (time.perf_counter() - t0) * 1e6
+    st = att.plan.stats()
+    update_us = pst.plan_update(att.plan, att.tree).stats()["plan_us"]
+    ex = att.plan.export()
+    O = [torch.empty((wl.n_queries, wl.n_q_heads, wl.d), dtype=torch.float32, device=dev) for _ in range(copies)]
+    L = [torch.empty((wl.n_queries, wl.n_q_heads), dtype=torch.float32, device=dev) for _ in range(copies)]
+    stream = torch.cuda.current_stream(dev)
+    for i in range(max(3, warmup)):
+        c = i % copies
+        att(Qd[c], Kd[c], Vd[c], O[c], L[c])
+    torch.cuda.synchronize(dev)
+    if att.check_status() != 0:
+        raise RuntimeError(f"{name}: device status word set during warm-up")
+
+    # ---- the timed loop: plain calls, CUDA events on the launching stream
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        ev0.record(stream)
+        for i in range(steps):
+            c = i % copies
+            att(Qd[c], Kd[c], Vd[c], O[c], L[c])
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    us = ev0.elapsed_time(ev1) * 1e3 / steps
+    if att.check_status() != 0:
+        raise RuntimeError(f"{name}: device status word set during the timed region")
+
+    # ---- per launch group: a separate loop with the library's events
+    timer = pst.Timer(max(1, timer_steps))
+    for i in range(max(1, timer_steps)):
+        c = i % copies
+        att(Qd[c], Kd[c], Vd[c], O[c], L[c], timer=timer)
+    kern_ms, kern_calls = timer.read()
+    group_us = {k: round(v * 1e3 / max(1, kern_calls), 3) for k, v in kern_ms.items()}
+
+    alg = algorithmic_bytes(wl, ex, st, plan_opts)
     dom = max(("pac_tc", "pac_tc_exact", "pac_thin"), key=lambda k: alg[k])
-    dom_ms = kern_ms[dom] / max(1, kern_calls)
-    dom_achieved = alg[dom] / (dom_ms * 1e-3) / 1e9
-    traffic = recorded_traffic(dom, args.workload)
-    clocks = clk.summary()
+    dom_us = group_us[dom]
+    dom_achieved = alg[dom] / (dom_us * 1e-6) / 1e9 if dom_us > 0 else 0.0
+    out = {
+        "workload": name, "wl": wl, "us": us, "U": U, "copies": copies, "clocks": clk.summary(),
+        "plan": {"plan_us": round(st["plan_us"], 1), "plan_wall_us": round(plan_wall_us, 1),
+                 "plan_update_us": round(update_us, 1),
+                 "predicted_makespan_us": round(st["predicted_makespan_us"], 2),
+                 "n_chunks": st["n_chunks"], "n_items": st["n_items"], "n_tc_items": st["n_tc_items"],
+                 "n_cc_items": st["n_cc_items"], "n_partial_rows": st["n_partial_rows"]},
+        "n_launches": int(st["n_launches"]),
+        "group_end_us": {k: v for k, v in group_us.items() if k != "por"},
+        "por_us": group_us["por"],
+        "alg": alg, "dom": dom, "dom_us": dom_us, "dom_achieved": dom_achieved, "peak": peak,
+    }
+    if e2e:
+        # per step: Q from pinned host memory to the device, decode, O and LSE back to pinned host memory
+        Qh = torch.from_numpy(Q_np.view(np.int16) if wl.dtype == "bf16" else Q_np).pin_memory()
+        Oh = torch.empty(O[0].shape, dtype=torch.float32).pin_memory()
+        Lh = torch.empty(L[0].shape, dtype=torch.float32).pin_memory()
+        Qstage = torch.empty(Qh.shape, dtype=Qh.dtype, device=dev)
+        e2e_steps = max(10, steps // 4)
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(e2e_steps):
+            c = i % copies
+            Qstage.copy_(Qh, non_blocking=True)
+            qv = Qstage.view(torch.bfloat16) if wl.dtype == "bf16" else Qstage
+            att(qv, Kd[c], Vd[c], O[c], L[c])
+            Oh.copy_(O[c], non_blocking=True)
+            Lh.copy_(L[c], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        out["e2e_us"] = e0.elapsed_time(e1) * 1e3 / e2e_steps
+        out["h2d"] = int(Qh.numel() * Qh.element_size())
+        out["d2h"] = int(Oh.numel() * 4 + Lh.numel() * 4)
+    del Kd, Vd, Qd, O, L, att
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return out
+
+
+def _config_entry(m):
+    peak = m["peak"]
+    gbs = m["U"] / (m["us"] * 1e-6) / 1e9
+    return {
+        "us_per_step": round(m["us"], 3), "unique_kv_bytes": m["U"], "achieved_unique_kv_gbs": round(gbs, 1),
+        "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "frac_of_measured_hbm": round(gbs / peak, 4),
+        "dominant_kernel": {"kernel": m["dom"], "algorithmic_bytes": m["alg"][m["dom"]],
+                            "group_end_us": m["dom_us"], "achieved_gbs": round(m["dom_achieved"], 1),
+                            "frac": round(m["dom_achieved"] / peak, 4)},
+        "group_end_us": m["group_end_us"], "por_us": m["por_us"], "n_launches": m["n_launches"],
+        "plan_us": m["plan"]["plan_us"], "sm_mhz": m["clocks"].get("sm_mhz"),
+    }
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    from prefix_shared_tree_gb300 import build as _build
+    _build.build()
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    plan_opts = _plan_opts(args)
+    warm = max(3, args.warmup)
+    h = measure(args.workload, args, dev, args.steps, warm, args.timer_steps, plan_opts, e2e=True, world=world)
+    us, e2e_us = max_over_ranks([h["us"], h["e2e_us"]], world, dev)
+    per_config = {}
+    if world == 1 and not args.no_per_config:
+        steps_pc = max(20, min(args.steps, 200))
+        shared_us = {args.workload: h["us"]}
+        for name in [n for n in args.per_config.split(",") if n and n != args.workload]:
+            m = measure(name, args, dev, steps_pc, 5, min(args.timer_steps, 32), plan_opts)
+            per_config[name] = _config_entry(m)
+            shared_us[name] = m["us"]
+            per_config[name]["steps"] = steps_pc
+        for name, e in per_config.items():
+            base = name[:-len("_flat")] if name.endswith("_flat") else None
+            if base and base in shared_us:
+                import synth
+                U_shared = WORKLOADS[base](synth).unique_kv_bytes()
+                e["vs_shared_tree"] = {"shared_us": round(shared_us[base], 3),
+                                       "flat_over_shared_time": round(e["us_per_step"] / shared_us[base], 3),
+                                       "flat_over_shared_unique_bytes": round(e["unique_kv_bytes"] / U_shared, 3)}
+    if rank != 0:
+        return None
+    peak, peak_src = measured_peaks()
+    U = h["U"]
+    wl = h["wl"]
+    achieved_gbs = U / (us * 1e-6) / 1e9
+    traffic = recorded_traffic(h["dom"], args.workload)
     line = {
         "metric": METRIC,
         "value": round(us, 3),
         "unit": "us/step",
         "n_gpus": world,
         "steps": args.steps,
-        "warmup": max(3, args.warmup),
+        "warmup": warm,
         "ms_per_step": round(us / 1e3, 6),
         "higher_is_better": False,
         "scaling": "weak",
@@ -373,25 +490,30 @@ def run_ours(args, rank, world):
         "achieved_unique_kv_gbs": round(achieved_gbs, 1),
         "frac_of_8tbs": round(achieved_gbs / NOMINAL_HBM_GBS, 4),
         "frac_of_measured_hbm": round(achieved_gbs / peak, 4),
-        "kernel_ms_share": {k: round(v, 4) for k, v in shares.items()},
-        "kernel_us_per_call": {k: round(v * 1e3 / max(1, kern_calls), 3) for k, v in kern_ms.items()},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": round(dom_achieved, 1), "peak": peak,
-                     "peak_source": peak_src, "unit": "GB/s", "frac": round(dom_achieved / peak, 4),
-                     "traffic": traffic, "algorithmic_bytes": alg[dom]},
-        "plan": {"plan_us": round(st["plan_us"], 1), "plan_wall_us": round(plan_wall_us, 1),
-                 "plan_update_us": round(update_us, 1),
-                 "predicted_makespan_us": round(st["predicted_makespan_us"], 2),
-                 "n_chunks": st["n_chunks"], "n_items": st["n_items"], "n_tc_items": st["n_tc_items"],
-                 "n_cc_items": st["n_cc_items"], "n_partial_rows": st["n_partial_rows"]},
-        "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": int(Qh.numel() * Qh.element_size()),
-                "d2h_bytes_per_step": int(Oh.numel() * 4 + Lh.numel() * 4)},
-        "gpu_launches": int(st["n_launches"]) * args.steps,
-        "clocks": clocks,
+        "group_end_us": h["group_end_us"],
+        "por_us": h["por_us"],
+        "timer_note": f"group_end_us: from the call's start to the end of each PAC launch group (the groups run "
+                      f"side by side), and POR alone, over a separate loop of {args.timer_steps} calls with the "
+                      f"library's events; the timed loop above records none",
+        "roofline": {"bound": "hbm", "kernel": h["dom"], "achieved": round(h["dom_achieved"], 1), "peak": peak,
+                     "peak_source": peak_src, "unit": "GB/s", "frac": round(h["dom_achieved"] / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes": h["alg"][h["dom"]]},
+        "plan": h["plan"],
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": h["h2d"],
+                "d2h_bytes_per_step": h["d2h"]},
+        "gpu_launches": h["n_launches"] * args.steps,
+        "clocks": h["clocks"],
     }
+    if per_config:
+        line["per_config"] = per_config
     return line, wl
 
 
 def run_reference(args, rank):
+    """The oracle as it stands on the host cores. A step is the whole batch
+    (every query and head) when W + K such steps fit in --ref-budget-s, else a
+    fixed sample of queries per step with the full-batch time extrapolated
+    (and said so in the line)."""
     if rank != 0:
         return None
     import numpy as np  # noqa: F401
@@ -402,31 +524,43 @@ def run_reference(args, rank):
     wl = WORKLOADS[args.workload](synth)
     K, V = wl.kv_pools()
     Q = wl.q()
-    order = [(i * 37) % wl.n_queries for i in range(wl.n_queries)]
-    oa.decode_attention(wl, K, V, Q, [order[0]])             # one untimed warm-up query
+    nq = wl.n_queries
+    order = [(i * 37) % nq for i in range(nq)]
     t0 = time.perf_counter()
-    done = 0
-    while done < args.steps and time.perf_counter() - t0 < args.ref_budget_s:
-        oa.decode_attention(wl, K, V, Q, [order[(done + 1) % len(order)]])
-        done += 1
-    el = time.perf_counter() - t0
-    us = el / done * wl.n_queries * 1e6
+    oa.decode_attention(wl, K, V, Q, order[:2])             # probe: two queries
+    per_q = (time.perf_counter() - t0) / 2
+    runs = max(1, args.steps) + max(1, args.warmup)
+    per_step = max(1, min(nq, int(args.ref_budget_s / max(per_q * runs, 1e-9))))
+    sampled = per_step < nq
+    for w in range(max(1, args.warmup)):                    # untimed warm-up steps
+        oa.decode_attention(wl, K, V, Q, [order[(w * per_step + i) % nq] for i in range(per_step)])
+    times = []
+    for st in range(max(1, args.steps)):
+        qs = [order[(st * per_step + i) % nq] for i in range(per_step)]
+        t0 = time.perf_counter()
+        oa.decode_attention(wl, K, V, Q, qs)
+        times.append(time.perf_counter() - t0)
+    step_s = sum(times) / len(times)
+    us = step_s / per_step * nq * 1e6
     ncpu = 1
     try:
         import threadpoolctl  # noqa: F401
         ncpu = max(i.get("num_threads", 1) for i in threadpoolctl.threadpool_info()) or 1
     except Exception:
         ncpu = int(os.environ.get("OPENBLAS_NUM_THREADS", os.cpu_count() or 1))
-    sample = (f"{done} of {args.steps} requested steps ran within {args.ref_budget_s:.0f} s; each timed one "
-              f"query (all heads) of the batch; us/step = mean per query x {wl.n_queries} queries")
+    if sampled:
+        sample = (f"each of the {len(times)} timed steps ran {per_step} of the batch's {nq} queries (all heads, "
+                  f"fp64); us/step is the full batch extrapolated from them")
+    else:
+        sample = f"each of the {len(times)} timed steps ran the whole batch ({nq} queries, all heads, fp64)"
     return {
         "impl": "reference",
         "metric": METRIC,
         "value": round(us, 1),
         "unit": "us/step",
         "n_gpus": 1,
-        "steps": done,
-        "warmup": 1,
+        "steps": len(times),
+        "warmup": max(1, args.warmup),
         "ms_per_step": round(us / 1e3, 3),
         "higher_is_better": False,
         "scaling": "weak",
@@ -434,6 +568,9 @@ def run_reference(args, rank):
         "dtype": "f64",
         "data": "synthetic",
         "config": bench_config(args, wl, 1),
+        "queries_per_step": per_step,
+        "extrapolated": sampled,
+        "executed_ms_per_step": round(step_s * 1e3, 3),
         "cpu_baseline": {"value": round(us, 1), "unit": "us/step", "cores": ncpu, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(us, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

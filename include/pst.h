@@ -194,8 +194,10 @@ int pst_plan_check_status(const pst_plan* p, void* stream, int32_t* code);
 /* ---------------------------------------------------------------- timing
  * Per-kernel device times of pst_decode_attn, for roofline accounting. A timer
  * holds CUDA events for up to `max_calls` calls; pst_decode_attn_timed records
- * an event at the start of the call, after each PAC launch group (on the
- * stream that ran it) and around POR. Slots (pst_timer_kernel_name):
+ * an event at the start of the call, after each PAC launch group that has
+ * work (on the stream that ran it) and around POR. The events themselves add
+ * to the call's time: time steps for throughput with pst_decode_attn.
+ * Slots (pst_timer_kernel_name):
  *   0 "pac_tc"        tensor-core PAC that rounds P once to bf16 (every
  *                     tensor-core item of the mma.sync engine)
  *   1 "pac_tc_exact"  tensor-core PAC with P split into bf16 hi + lo
@@ -203,7 +205,9 @@ int pst_plan_check_status(const pst_plan* p, void* stream, int32_t* code);
  *                     tcgen05 thin PAC, or every CUDA-core row-tile launch
  *   3 "por"           partial-output reduction
  * The PAC groups run side by side on forked streams, so slots 0-2 give the
- * time from the call's start to the end of that group; slot 3 is POR alone.
+ * time from the call's start to the end of that group (overlapping
+ * intervals, not shares of the call; 0 for a call in which the slot's groups
+ * had no work); slot 3 is POR alone.
  * pst_timer_read synchronises on the last event, writes the summed
  * milliseconds per slot into ms[0..n-1], the number of timed calls into
  * *calls, and resets the timer. */

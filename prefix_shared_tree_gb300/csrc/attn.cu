@@ -262,6 +262,7 @@ struct pst_timer {
     int32_t max_calls = 0;
     int32_t calls = 0;
     std::vector<cudaEvent_t> ev;         // max_calls x kEvents
+    std::vector<uint8_t> ran;            // max_calls x 5: launch group g had work in call c
     static constexpr int kEvents = 8;
 };
 
@@ -349,14 +350,15 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
             cudaStreamWaitEvent(static_cast<cudaStream_t>(p->side_stream[k]), static_cast<cudaEvent_t>(p->ev_fork), 0);
     }
     for (int g = 0; g < kGroups; ++g) {
-        if (has[g]) {
-            e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g, gst[g])
-                      : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, gst[g]);
-            if (e != cudaSuccess) return cuda_fail(g < 4 ? "decode_attn: PAC (tensor core) launch"
-                                                         : "decode_attn: PAC (thin chunks) launch", e);
-        }
+        if (!has[g]) continue;
+        e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g, gst[g])
+                  : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, gst[g]);
+        if (e != cudaSuccess) return cuda_fail(g < 4 ? "decode_attn: PAC (tensor core) launch"
+                                                     : "decode_attn: PAC (thin chunks) launch", e);
         if (ev) cudaEventRecord(ev[1 + g], gst[g]);
     }
+    if (ev)
+        for (int g = 0; g < kGroups; ++g) timer->ran[(size_t)timer->calls * kGroups + g] = has[g] ? 1 : 0;
     for (int k = 0; k < n_side; ++k) {
         cudaEventRecord(static_cast<cudaEvent_t>(p->ev_join[k]), static_cast<cudaStream_t>(p->side_stream[k]));
         cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(p->ev_join[k]), 0);
@@ -414,6 +416,7 @@ extern "C" int pst_timer_create(int32_t max_calls, pst_timer** out) {
     if (!t) return fail(PST_ENOMEM, "timer_create: out of memory");
     t->max_calls = max_calls;
     t->ev.resize((size_t)max_calls * pst_timer::kEvents, nullptr);
+    t->ran.assign((size_t)max_calls * 5, 0);
     for (auto& e : t->ev) {
         cudaError_t r = cudaEventCreate(&e);
         if (r != cudaSuccess) {
@@ -440,16 +443,28 @@ extern "C" int pst_timer_read(pst_timer* t, float* ms, int32_t n, int32_t* calls
         cudaError_t e = cudaEventSynchronize(t->ev[(size_t)(t->calls - 1) * stride + stride - 1]);
         if (e != cudaSuccess) return cuda_fail("timer_read: cudaEventSynchronize", e);
     }
-    // slot k: from event, the later of two end events
-    static const int from[4] = {0, 0, 0, 6}, to_a[4] = {1, 3, 5, 7}, to_b[4] = {2, 4, 5, 7};
+    // slot k covers launch groups grp[k][0..1] (end events 1 + g); a slot
+    // whose groups had no work in a call adds 0 for that call
+    static const int grp[3][2] = {{0, 1}, {2, 3}, {4, 4}};
     for (int c = 0; c < t->calls; ++c) {
         const cudaEvent_t* e0 = t->ev.data() + (size_t)c * stride;
+        const uint8_t* ran = t->ran.data() + (size_t)c * 5;
         for (int k = 0; k < 4 && k < n; ++k) {
-            float xa = 0.f, xb = 0.f;
-            cudaError_t e = cudaEventElapsedTime(&xa, e0[from[k]], e0[to_a[k]]);
-            if (e == cudaSuccess) e = cudaEventElapsedTime(&xb, e0[from[k]], e0[to_b[k]]);
+            float x = 0.f;
+            cudaError_t e = cudaSuccess;
+            if (k == 3) {
+                e = cudaEventElapsedTime(&x, e0[6], e0[7]);
+            } else {
+                for (int g : grp[k]) {
+                    if (!ran[g]) continue;
+                    float y = 0.f;
+                    e = cudaEventElapsedTime(&y, e0[0], e0[1 + g]);
+                    if (e != cudaSuccess) break;
+                    x = std::max(x, y);
+                }
+            }
             if (e != cudaSuccess) return cuda_fail("timer_read: cudaEventElapsedTime", e);
-            ms[k] += std::max(xa, xb);
+            ms[k] += x;
         }
     }
     if (calls) *calls = t->calls;

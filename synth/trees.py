@@ -364,6 +364,23 @@ def flat_control(wl: Workload) -> Workload:
     return out
 
 
+def source_rows(src: Workload, dst: Workload) -> np.ndarray:
+    """int64 [dst.num_pages * page_size]: for every pool row of `dst`, the pool
+    row of `src` that holds the same logical token (-1 where `dst`'s row is
+    unused or `src` lacks the token). With it, `dst`'s pools (e.g. the flat
+    control of `src`) can be filled by copying `src`'s rows, since a token's
+    K/V depend on its logical id only."""
+    where = np.full(int(src.lid.max()) + 1 if src.lid.size else 1, -1, dtype=np.int64)
+    srows = src.row_lids()
+    used = np.nonzero(srows >= 0)[0]
+    where[srows[used]] = used
+    drows = dst.row_lids()
+    out = np.full(drows.shape, -1, dtype=np.int64)
+    ok = (drows >= 0) & (drows < where.size)
+    out[ok] = where[drows[ok]]
+    return out
+
+
 def grow_query_nodes(wl: Workload, tokens: int = 1) -> Workload:
     """The next decode steps' tree: every node a query sits on gains `tokens`
     tokens (new logical ids), in free rows of its last page or in new pages
