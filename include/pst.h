@@ -82,6 +82,13 @@ typedef struct {
                                M side and query rows (at most 16 per block) on N;
                                bf16 with d = 128 only, other shapes take the
                                CUDA-core PAC; 1 the CUDA-core PAC always         */
+    int32_t debug_stall;    /* test only; 0 (default) off. 1: the tcgen05 PAC's MMA
+                               thread first waits on a barrier nothing arrives on,
+                               so that bounded wait runs out; every role of the
+                               block then leaves through its error path (bounded
+                               waits, TMA loads drained) and the device status word
+                               is set. The outputs of such a call are undefined;
+                               pst_plan_check_status reports PST_EDEVICE.        */
 } pst_plan_opts;
 
 /* Fill `o` with the defaults above. */

@@ -238,6 +238,7 @@ DevPlan dev_plan_at(const pst_plan* p, void* ws) {
     d.d = p->d;
     d.page_size = p->page_size;
     d.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)p->d));
+    d.debug_stall = p->opts.debug_stall;
     return d;
 }
 

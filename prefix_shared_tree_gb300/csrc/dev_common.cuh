@@ -70,18 +70,30 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t par
 // status word and lets the caller leave the kernel.
 constexpr long long kWaitCycles = 4000000000LL;
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* status,
+                                          long long limit = kWaitCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
 #pragma unroll 1
         for (int i = 0; i < 16; ++i)
-            if (mbar_try_wait_suspend(bar, parity, 100000u)) return true;
-        if (clock64() - t0 > kWaitCycles) {
+            if (mbar_try_wait_suspend(bar, parity, limit < kWaitCycles ? 1000u : 100000u)) return true;
+        if (clock64() - t0 > limit) {
             atomicOr(status, kStatusWaitTimeout);
             return false;
         }
     }
+}
+
+// Before a block leaves after a wait gave up, a TMA producer waits (bounded)
+// until the loads it issued into a ring's last stages have landed, so that no
+// bulk copy still writes into the block's shared memory when it exits: ring
+// tile g (global count, `issued` tiles so far) completes phase (g / ST) & 1
+// of full barrier g % ST, and for the last ST tiles issued that phase is the
+// barrier's latest.
+template <int ST>
+__device__ __forceinline__ void drain_ring(uint32_t bar_full, int issued, int32_t* status) {
+    for (int g = issued > ST ? issued - ST : 0; g < issued; ++g) mbar_wait(bar_full + 8 * (g % ST), (g / ST) & 1, status);
 }
 
 // 3-D tiled TMA load (dims: channel, row-in-page, page*Hkv + head) into shared
@@ -155,7 +167,7 @@ __device__ __forceinline__ ChunkGeo chunk_geo(const DevChunk& c) {
 // `tbase` tiles went through the ring before this chunk (stage and phase
 // continue from there).
 template <int NSLAB, int STAGES, int ELEMS_PER_SLAB>
-__device__ void produce_chunk(const DevPlan& P, const DevChunk& C, int head, uint32_t ring,
+__device__ bool produce_chunk(const DevPlan& P, const DevChunk& C, int head, uint32_t ring,
                               uint32_t bar_full, uint32_t bar_empty, const CUtensorMap* tk,
                               const CUtensorMap* tv, int tbase = 0) {
     constexpr uint32_t kSlabBytes = kTileTokens * 128;
@@ -167,7 +179,10 @@ __device__ void produce_chunk(const DevPlan& P, const DevChunk& C, int head, uin
         const int I = tbase + i;
         const int s = I % STAGES;
         if (I >= STAGES) {
-            if (!mbar_wait(bar_empty + 8 * s, ((I / STAGES) - 1) & 1, P.status)) return;
+            if (!mbar_wait(bar_empty + 8 * s, ((I / STAGES) - 1) & 1, P.status)) {
+                drain_ring<STAGES>(bar_full, I, P.status);
+                return false;
+            }
         }
         const int tpos = g.tile0 + i * kTileTokens;
         uint32_t nbox = 0;
@@ -197,6 +212,14 @@ __device__ void produce_chunk(const DevPlan& P, const DevChunk& C, int head, uin
             }
         }
     }
+    return true;
+}
+
+// The end of a producer's work: its last loads have landed before it leaves
+// (when its consumers stopped early they would not wait for them).
+template <int ST>
+__device__ __forceinline__ void producer_done(uint32_t bar_full, int issued, int32_t* status) {
+    drain_ring<ST>(bar_full, issued, status);
 }
 
 // TMA producer for one operand (K or V) with its own full/empty barriers:
@@ -208,7 +231,7 @@ __device__ void produce_chunk(const DevPlan& P, const DevChunk& C, int head, uin
 // arrivals): the TMA unit takes a few hundred cycles per instruction from one
 // thread, so several issuing threads fill a stage sooner.
 template <int NSLAB, int TT, int STAGES, int NPART = 1>
-__device__ void produce_tiles(const DevPlan& P, const DevChunk& C, int head, uint32_t ring, uint32_t bar_full,
+__device__ bool produce_tiles(const DevPlan& P, const DevChunk& C, int head, uint32_t ring, uint32_t bar_full,
                               uint32_t bar_empty, const CUtensorMap* map, int part = 0) {
     constexpr uint32_t kSlabBytes = TT * 128;
     constexpr uint32_t kStageBytes = NSLAB * kSlabBytes;
@@ -218,7 +241,10 @@ __device__ void produce_tiles(const DevPlan& P, const DevChunk& C, int head, uin
     for (int i = 0; i < g.n_tiles; ++i) {
         const int s = i % STAGES;
         if (i >= STAGES) {
-            if (!mbar_wait(bar_empty + 8 * s, ((i / STAGES) - 1) & 1, P.status)) return;
+            if (!mbar_wait(bar_empty + 8 * s, ((i / STAGES) - 1) & 1, P.status)) {
+                drain_ring<STAGES>(bar_full, i, P.status);
+                return false;
+            }
         }
         const int tpos = g.tile0 + i * TT;
         int page[TT / kBoxRows];
@@ -245,6 +271,8 @@ __device__ void produce_tiles(const DevPlan& P, const DevChunk& C, int head, uin
                 tma_load_3d(dst0 + sl * kSlabBytes + b * kBoxRows * 128, map, sl * 64, row0, slab_z, full);
         }
     }
+    producer_done<STAGES>(bar_full, g.n_tiles, P.status);
+    return true;
 }
 
 // TMA producer for one operand with d = 128 in page boxes: each 16-row box of
@@ -252,7 +280,7 @@ __device__ void produce_tiles(const DevPlan& P, const DevChunk& C, int head, uin
 // tile of TT tokens is TT / 16 boxes at ring + s * TT * 256 + box * 4096.
 // Boxes entirely outside the chunk are skipped.
 template <int TT, int STAGES>
-__device__ void produce_pages(const DevPlan& P, const DevChunk& C, int head, uint32_t ring, uint32_t bar_full,
+__device__ bool produce_pages(const DevPlan& P, const DevChunk& C, int head, uint32_t ring, uint32_t bar_full,
                               uint32_t bar_empty, const CUtensorMap* map5) {
     constexpr uint32_t kBox = 2 * kBoxRows * 128;
     constexpr uint32_t kStageBytes = TT * 256;
@@ -262,7 +290,10 @@ __device__ void produce_pages(const DevPlan& P, const DevChunk& C, int head, uin
     for (int i = 0; i < g.n_tiles; ++i) {
         const int s = i % STAGES;
         if (i >= STAGES) {
-            if (!mbar_wait(bar_empty + 8 * s, ((i / STAGES) - 1) & 1, P.status)) return;
+            if (!mbar_wait(bar_empty + 8 * s, ((i / STAGES) - 1) & 1, P.status)) {
+                drain_ring<STAGES>(bar_full, i, P.status);
+                return false;
+            }
         }
         const int tpos = g.tile0 + i * TT;
         int page[TT / kBoxRows];
@@ -285,6 +316,8 @@ __device__ void produce_pages(const DevPlan& P, const DevChunk& C, int head, uin
             tma_load_5d(dst0 + b * kBox, map5, 0, pos % ps, head, 0, page[b], full);
         }
     }
+    producer_done<STAGES>(bar_full, g.n_tiles, P.status);
+    return true;
 }
 
 using u64 = unsigned long long;

@@ -383,9 +383,14 @@ pac_cc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
                 if (idx >= n_items) break;
                 const DevItem it = P.items[item_off + idx];
                 const DevChunk C = P.chunks[it.chunk];
-                produce_chunk<NSLAB, kCcStages, 128 / EB>(P, C, it.kv_head, ring, bar_full, bar_empty, &tk, &tv, tbase);
+                if (!produce_chunk<NSLAB, kCcStages, 128 / EB>(P, C, it.kv_head, ring, bar_full, bar_empty, &tk, &tv,
+                                                              tbase)) {
+                    tbase = -1;
+                    break;
+                }
                 tbase += chunk_geo(C).n_tiles;
             }
+            if (tbase >= 0) producer_done<kCcStages>(bar_full, tbase, P.status);
         }
         return;
     }

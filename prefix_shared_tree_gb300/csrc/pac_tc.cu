@@ -91,7 +91,8 @@ pac_tc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
         if (lane == 0) {
             prefetch_tmap(&tk);
             prefetch_tmap(&tv);
-            produce_chunk<NSLAB, kTcStages, 64>(P, C, head, ring, bar_full, bar_empty, &tk, &tv);
+            if (produce_chunk<NSLAB, kTcStages, 64>(P, C, head, ring, bar_full, bar_empty, &tk, &tv))
+                producer_done<kTcStages>(bar_full, chunk_geo(C).n_tiles, P.status);
         }
         return;
     }

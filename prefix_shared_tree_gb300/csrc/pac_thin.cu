@@ -142,7 +142,10 @@ __device__ bool thin_produce(const DevPlan& P, const DevChunk& C, int head0, uin
         const int tpos = geo.tile0 + i * kThinTT;
         const int page = P.pages[C.page_base + tpos / ps];
         const int s = g % ST;
-        if (g >= ST && !mbar_wait(empty + 8 * s, ((g / ST) - 1) & 1, P.status)) return false;
+        if (g >= ST && !mbar_wait(empty + 8 * s, ((g / ST) - 1) & 1, P.status)) {
+            drain_ring<ST>(full, g, P.status);
+            return false;
+        }
         mbar_arrive_expect_tx(full + 8 * s, kOp);
         tma_load_5d(ring + s * kOp, map, 0, tpos % ps, head0, 0, page, full + 8 * s);
     }
@@ -296,9 +299,14 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             const int head0 = it.kv_head;
             bool ok = true;
             if (lane == 0) ok = thin_produce<KST>(P, C, head0, sbase + L::kK, k_full, k_empty, &tk, gbase);
-            if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+            if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                gbase = -1;   // drained already
+                break;
+            }
             gbase += chunk_geo<kThinTT>(C).n_tiles;
         }
+        // the last K loads have landed before the producer leaves
+        if (lane == 0 && gbase >= 0) drain_ring<KST>(k_full, gbase, P.status);
     } else if (warp == 2) {
         // ------------------------------------------------------------ V producer
         if (lane == 0) {
@@ -312,9 +320,13 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 const int head0 = slots[slot].it.kv_head;
                 mbar_arrive(item_empty + 8 * slot);
                 if (idx < 0) break;
-                if (!thin_produce<VST>(P, C, head0, sbase + L::kV, v_full, v_empty, &tv, gbase)) break;
+                if (!thin_produce<VST>(P, C, head0, sbase + L::kV, v_full, v_empty, &tv, gbase)) {
+                    gbase = -1;   // drained already
+                    break;
+                }
                 gbase += chunk_geo<kThinTT>(C).n_tiles;
             }
+            if (gbase >= 0) drain_ring<VST>(v_full, gbase, P.status);
         }
         __syncwarp();
     } else if (warp == 1) {

@@ -365,6 +365,10 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             constexpr uint32_t idS = umma::idesc_bf16_f32(128, kUT, 0, 0);
             constexpr uint32_t idO = umma::idesc_bf16_f32(128, D, 0, 1);   // V is MN-major
             bool ok = mbar_wait(q_ready, 0, P.status);
+            // test only: mma_done gets its first arrival from this thread's
+            // final commit below, so this bounded wait (about a millisecond)
+            // runs out and the block leaves through its error path
+            if (P.debug_stall) ok = mbar_wait(mma_done, 0, P.status, 2000000LL) && ok;
             umma::fence_after_sync();
             // Descriptors are built once; an MMA only adds a compile-time byte
             // offset (>> 4) to the start-address field. Shared-memory

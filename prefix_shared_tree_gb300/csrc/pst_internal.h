@@ -88,6 +88,7 @@ struct DevPlan {
     int32_t* counters;  // work-queue counters of the persistent PAC launches (zeroed by POR)
     int32_t n_queries, n_q_heads, n_kv_heads, group, d, page_size;
     float scale_log2;  // log2(e) / sqrt(d)
+    int32_t debug_stall;  // test only: see pst_plan_opts::debug_stall
 };
 
 // PAC kinds of the cost model: CUDA core, tensor core with P rounded once to
