@@ -160,6 +160,24 @@ void pst_plan_destroy(pst_plan* p);
  * parents differ), and those of pst_plan_create. */
 int pst_plan_update(const pst_plan* prev, const pst_tree* tree, pst_plan** out);
 
+/* Incremental plan for a decode step whose tree changed shape, e.g. after the
+ * verification of a speculative decoding step (CoDec, "workload balancing":
+ * the plan is reused across steps; DEFT section 3.3: the accepted drafts stay,
+ * the rejected ones are pruned and a new draft tree grows). `tree` is the new
+ * tree, n_queries / query_node its queries (as for pst_plan_create), and
+ * prev_node[N] (N = the new tree's node count) gives for each node the id of
+ * the same node in prev's tree (its tokens may have grown or shrunk), or -1
+ * for a node that is new. Heads, d, dtype and options come from prev. The
+ * grouping, packing (bit causal masks of the new draft chunks), chunks, items
+ * and metadata are built for the new tree, but a node mapped to prev keeps
+ * prev's KV-axis split b_k (bounded by its tiles), and a new node takes
+ * ceil(C_est / cost_l) under prev's cost bound cost_l, with no partition
+ * search. The new plan is independent of prev (upload it to a workspace of its
+ * own size). Errors: PST_EINVAL (null argument), PST_ERANGE (a prev_node entry
+ * outside [-1, prev's node count)), and those of pst_plan_create. */
+int pst_plan_update_tree(const pst_plan* prev, const pst_tree* tree, int32_t n_queries, const int32_t* query_node,
+                         const int32_t* prev_node, pst_plan** out);
+
 /* Bytes of device workspace the plan needs: its metadata plus the partial
  * output scratch (fp32 partial outputs and log-sum-exps). */
 int64_t pst_plan_workspace_bytes(const pst_plan* p);

@@ -537,7 +537,7 @@ static bool build_packed_group(const Tree& T, int32_t root, const std::vector<in
 // being searched (pst_plan_update).
 static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* query_node, int32_t n_q_heads,
                       int32_t n_kv_heads, int32_t d, pst_dtype dtype, const pst_plan_opts* opts,
-                      const pst_plan* prev, pst_plan** out) {
+                      const pst_plan* prev, const int32_t* prev_node, pst_plan** out) {
     const auto t_start = std::chrono::steady_clock::now();
     if (!out) return fail(PST_EINVAL, "plan_create: out is null");
     *out = nullptr;
@@ -709,15 +709,20 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
     P->num_slots = m;
     if (prev) {
         // CoDec reuses a plan across decode steps: a node keeps its previous
-        // split b_k (bounded by its tiles now); a task that is new (a packing
-        // that changed) gets the split its cost bound under the previous
-        // cost_l gives, ceil(C_est / cost_l)
-        std::vector<int32_t> bk_of_node(T.n_nodes, 0);
+        // split b_k (bounded by its tiles now); a node that is new (or a
+        // packing that changed) gets the split its cost bound under the
+        // previous cost_l gives, ceil(C_est / cost_l). prev_node maps a node
+        // to its id in prev's tree (-1: new); null means the same ids.
+        std::vector<int32_t> bk_of_old(prev->n_nodes, 0);
         for (const auto& t : prev->tasks)
-            if (t.node >= 0 && t.node < T.n_nodes) bk_of_node[t.node] = t.b_k;
+            if (t.node >= 0 && t.node < prev->n_nodes) bk_of_old[t.node] = t.b_k;
         P->cost_l_us = prev->cost_l_us;
         for (auto& t : P->tasks) {
-            int32_t b = t.node >= 0 ? bk_of_node[t.node] : 1;
+            int32_t b = 1;
+            if (t.node >= 0) {
+                const int32_t old_id = prev_node ? prev_node[t.node] : t.node;
+                b = (old_id >= 0 && old_id < prev->n_nodes) ? bk_of_old[old_id] : 0;
+            }
             if (b <= 0) {
                 const double c = pl.item_cost(t, pl.rows_per_block(t), t.n_tok);
                 b = prev->cost_l_us > 0 ? (int32_t)std::ceil(c / prev->cost_l_us - 1e-9) : 1;
@@ -894,7 +899,7 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
 extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const int32_t* query_node,
                                int32_t n_q_heads, int32_t n_kv_heads, int32_t d, pst_dtype dtype,
                                const pst_plan_opts* opts, pst_plan** out) {
-    return plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, opts, nullptr, out);
+    return plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, opts, nullptr, nullptr, out);
 }
 
 extern "C" int pst_plan_update(const pst_plan* prev, const pst_tree* tree, pst_plan** out) {
@@ -916,7 +921,20 @@ extern "C" int pst_plan_update(const pst_plan* prev, const pst_tree* tree, pst_p
         if (v != -1) return fail(PST_EINVAL, "plan_update: the tree's parents changed");
     }
     return plan_build(tree, prev->n_queries, qn.data(), prev->hq, prev->hkv, prev->d, prev->dtype, &prev->opts, prev,
-                      out);
+                      nullptr, out);
+}
+
+extern "C" int pst_plan_update_tree(const pst_plan* prev, const pst_tree* tree, int32_t n_queries,
+                                    const int32_t* query_node, const int32_t* prev_node, pst_plan** out) {
+    if (!out) return fail(PST_EINVAL, "plan_update_tree: out is null");
+    *out = nullptr;
+    if (!prev || !tree || !prev_node) return fail(PST_EINVAL, "plan_update_tree: null plan, tree or node map");
+    const Tree& T = tree->t;
+    for (int32_t n = 0; n < T.n_nodes; ++n)
+        if (prev_node[n] < -1 || prev_node[n] >= prev->n_nodes)
+            return fail(PST_ERANGE, "plan_update_tree: prev_node[" + std::to_string(n) + "] out of range");
+    return plan_build(tree, n_queries, query_node, prev->hq, prev->hkv, prev->d, prev->dtype, &prev->opts, prev,
+                      prev_node, out);
 }
 
 namespace pst {

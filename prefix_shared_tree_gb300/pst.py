@@ -83,6 +83,7 @@ def lib() -> C.CDLL:
         "pst_plan_opts_default": (None, [C.POINTER(PlanOpts)]),
         "pst_plan_create": (C.c_int, [vp, i32, vp, i32, i32, i32, C.c_int, C.POINTER(PlanOpts), C.POINTER(vp)]),
         "pst_plan_update": (C.c_int, [vp, vp, C.POINTER(vp)]),
+        "pst_plan_update_tree": (C.c_int, [vp, vp, i32, vp, vp, C.POINTER(vp)]),
         "pst_plan_destroy": (None, [vp]),
         "pst_plan_workspace_bytes": (i64, [vp]),
         "pst_plan_upload": (C.c_int, [vp, vp, i64, vp]),
@@ -239,6 +240,19 @@ def plan_update(prev: Plan, tree: Tree) -> Plan:
     h = C.c_void_p()
     _check(lib().pst_plan_update(prev._h, tree._h, C.byref(h)))
     return Plan(h, prev.n_queries, prev.hq, prev.hkv, prev.d, prev.dtype)
+
+
+def plan_update_tree(prev: Plan, tree: Tree, query_node, prev_node) -> Plan:
+    """Plan for a tree whose shape changed (nodes kept, pruned or added; new
+    queries): prev_node[n] is node n's id in prev's tree, or -1 if new. Kept
+    nodes keep prev's KV-axis splits (no partition search)."""
+    qn, qnp = _arr(query_node, np.int32)
+    pn, pnp = _arr(prev_node, np.int32)
+    if pn.size != tree.n_nodes:
+        raise ValueError("prev_node needs one entry per node of the new tree")
+    h = C.c_void_p()
+    _check(lib().pst_plan_update_tree(prev._h, tree._h, len(qn), qnp, pnp, C.byref(h)))
+    return Plan(h, len(qn), prev.hq, prev.hkv, prev.d, prev.dtype)
 
 
 def decode_attn(plan: Plan, q: int, k_pool: int, v_pool: int, o: int, lse: int, stream: int = 0):

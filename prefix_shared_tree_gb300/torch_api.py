@@ -59,6 +59,23 @@ class TreeDecodeAttention:
                         keepalive=self.workspace)
         self.tree, self.plan = tree, plan
 
+    def update_shape(self, node_len, parent, page_ptr, page_ids, first_offset, num_pages, query_node, prev_node):
+        """Next decode step on a tree whose shape changed (e.g. speculative
+        drafts accepted and pruned, a new draft tree with new queries): rebuild
+        the tree and derive the plan with pst_plan_update_tree, where
+        prev_node[n] is node n's id in the current tree or -1, then upload."""
+        self.num_pages = int(num_pages)
+        tree = pst.tree_build(node_len, parent, page_ptr, page_ids, first_offset, self.page_size, self.num_pages)
+        with torch.cuda.device(self.device):
+            plan = pst.plan_update_tree(self.plan, tree, query_node, prev_node)
+            if plan.workspace_bytes > self.workspace.numel():
+                self.workspace = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device=self.device)
+            stream = torch.cuda.current_stream(self.device)
+            plan.upload(self.workspace.data_ptr(), self.workspace.numel(), stream.cuda_stream,
+                        keepalive=self.workspace)
+        self.tree, self.plan = tree, plan
+        self.n_queries = len(query_node)
+
     @classmethod
     def from_workload(cls, wl, device="cuda", **plan_opts):
         return cls(wl.node_len, wl.parent, wl.page_ptr, wl.page_ids, wl.first_offset, wl.page_size,

@@ -424,6 +424,95 @@ def grow_query_nodes(wl: Workload, tokens: int = 1) -> Workload:
         lid_ptr=lid_ptr, lid=np.concatenate(lid_lists) if lid_lists else wl.lid)
 
 
+def speculative_next_step(wl: Workload, seed: int, n_draft: int = 64, depth: int = 6):
+    """The tree of the next speculative decoding step, and for each of its
+    nodes the id of the same node in `wl` (-1 for a new node).
+
+    In every tree (a top-level prompt node and its single-token draft nodes)
+    one draft is accepted, together with the drafts on its path: those keep
+    their tokens and pages and now form a chain under the prompt; every other
+    draft is pruned (its page rows become unused). A new draft tree of
+    `n_draft` single-token nodes and exactly `depth` levels (a seeded
+    composition of the level sizes, parents uniform over the previous level)
+    hangs off the last accepted draft, in new pages appended to the pool with
+    new logical ids; the new drafts are the step's queries."""
+    ps = wl.page_size
+    kids = [[] for _ in range(wl.n_nodes)]
+    for n in range(wl.n_nodes):
+        if wl.parent[n] >= 0:
+            kids[int(wl.parent[n])].append(n)
+    next_lid = int(wl.lid.max()) + 1 if wl.lid.size else 0
+    num_pages = wl.num_pages
+    node_len, parent, fo, page_lists, lid_lists, prev_node, qn = [], [], [], [], [], [], []
+
+    def keep(old, new_parent):
+        prev_node.append(old)
+        node_len.append(int(wl.node_len[old]))
+        parent.append(new_parent)
+        fo.append(int(wl.first_offset[old]))
+        page_lists.append([int(p) for p in wl.page_ids[wl.page_ptr[old]:wl.page_ptr[old + 1]]])
+        lid_lists.append(wl.lid[wl.lid_ptr[old]:wl.lid_ptr[old + 1]])
+        return len(node_len) - 1
+
+    roots = [n for n in range(wl.n_nodes) if wl.parent[n] < 0]
+    for t, r in enumerate(roots):
+        kt = rng.stream_key(seed, 51, t)
+        drafts, stack = [], list(kids[r])
+        while stack:
+            n = stack.pop()
+            drafts.append(n)
+            stack.extend(kids[n])
+        drafts.sort()
+        # the accepted draft and its path below the prompt
+        path = []
+        if drafts:
+            a = drafts[rng.uniform_int(kt, 0, 0, len(drafts) - 1)]
+            while a != r:
+                path.append(a)
+                a = int(wl.parent[a])
+            path.reverse()
+        last = keep(r, -1)
+        for a in path:
+            last = keep(a, last)
+        # the new draft tree
+        cand = list(range(1, n_draft))
+        for i in range(depth - 1):
+            j = rng.uniform_int(kt, 1 + i, i, len(cand) - 1)
+            cand[i], cand[j] = cand[j], cand[i]
+        cuts = sorted(cand[:depth - 1])
+        sizes = [b - a for a, b in zip([0] + cuts, cuts + [n_draft])]
+        base_page = num_pages
+        num_pages += -(-n_draft // ps)
+        prev_level = [last]
+        j = 0
+        for sz in sizes:
+            cur = []
+            for _ in range(sz):
+                pidx = rng.uniform_int(kt, 1000 + j, 0, len(prev_level) - 1)
+                prev_node.append(-1)
+                node_len.append(1)
+                parent.append(prev_level[pidx])
+                fo.append(j % ps)
+                page_lists.append([base_page + j // ps])
+                lid_lists.append(np.array([next_lid], dtype=np.int64))
+                next_lid += 1
+                qn.append(len(node_len) - 1)
+                cur.append(len(node_len) - 1)
+                j += 1
+            prev_level = cur
+    N = len(node_len)
+    page_ptr = np.zeros(N + 1, dtype=np.int64)
+    page_ptr[1:] = np.cumsum([len(p) for p in page_lists])
+    lid_ptr = np.zeros(N + 1, dtype=np.int64)
+    lid_ptr[1:] = np.cumsum([len(x) for x in lid_lists])
+    nxt = dataclasses.replace(
+        wl, name=wl.name + "+step", node_len=np.array(node_len, dtype=np.int32),
+        parent=np.array(parent, dtype=np.int32), first_offset=np.array(fo, dtype=np.int32), page_ptr=page_ptr,
+        page_ids=np.array([p for pl in page_lists for p in pl], dtype=np.int32), num_pages=num_pages,
+        query_node=np.array(qn, dtype=np.int32), lid_ptr=lid_ptr, lid=np.concatenate(lid_lists))
+    return nxt, np.array(prev_node, dtype=np.int32)
+
+
 def random_tree(seed: int, max_nodes: int = 12, max_len: int = 70, max_depth: int = 4,
                 heads=(4, 2), d: int = 64, dtype: str = "bf16", n_queries: int | None = None,
                 allow_empty: bool = True, random_offsets: bool = True) -> Workload:

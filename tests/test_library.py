@@ -333,3 +333,50 @@ def test_grow_query_nodes_input():
     assert np.array_equal(r2[:r1.size][r1 >= 0], r1[r1 >= 0])
     assert (r2 >= 0).sum() == (r1 >= 0).sum() + 3 * q_nodes.size
     assert len(np.unique(r2[r2 >= 0])) == (r2 >= 0).sum()
+
+
+# ------------------------------------------------------------ plan update across a changed tree shape
+
+@pytest.mark.parametrize("seed", [3, 11])
+def test_plan_update_tree_after_accept_and_prune(lib, seed):
+    """Speculative decoding, next step: in each tree one draft path is
+    accepted (kept as a chain under the prompt), the rest pruned, and a new
+    64-node draft tree with new queries hangs off the last accepted draft. The
+    updated plan covers every (query, token) pair of the new tree exactly once,
+    its index equals the oracle's, the prompts keep their KV-axis split and the
+    new drafts are packed with bit causal masks."""
+    wl = synth.speculative(batch=3, prompt=2000)
+    p = _plan(lib, wl)
+    wl2, prev_node = synth.speculative_next_step(wl, seed)
+    p2 = lib.plan_update_tree(p, _tree(lib, wl2), wl2.query_node, prev_node)
+    e, e2 = p.export(), p2.export()
+    assert np.array_equal(_covered_pairs(wl2, e2), _visible_pairs(wl2))
+    # the index (query -> path, node -> queries) is the oracle's
+    paths = ot.query_paths(wl2.parent, wl2.query_node)
+    for q, path in enumerate(paths):
+        assert e2["qpath_node"][e2["qpath_ptr"][q]:e2["qpath_ptr"][q + 1]].tolist() == path
+    nq = ot.node_queries(wl2.parent, wl2.query_node, wl2.n_nodes)
+    for n in range(wl2.n_nodes):
+        assert e2["nodeq"][e2["nodeq_ptr"][n]:e2["nodeq_ptr"][n + 1]].tolist() == nq[n]
+    # kept prompts: split as before
+    c1, c2 = _chunks_per_node(e, wl.n_nodes), _chunks_per_node(e2, wl2.n_nodes)
+    for n in range(wl2.n_nodes):
+        if prev_node[n] >= 0 and wl2.parent[n] < 0:
+            assert c2[n] == c1[prev_node[n]], (n, c2[n], c1[prev_node[n]])
+    # the new drafts are packed: some chunk of the new plan carries masks
+    masks = e2["chunk_q_mask"]
+    assert np.any(masks != np.uint64(0xFFFFFFFFFFFFFFFF))
+    assert p2.stats()["plan_us"] < p.stats()["plan_us"] * 4
+
+
+def test_plan_update_tree_rejects_a_bad_node_map(lib):
+    wl = synth.speculative(batch=2, prompt=500)
+    p = _plan(lib, wl)
+    wl2, prev_node = synth.speculative_next_step(wl, 5)
+    t2 = _tree(lib, wl2)
+    bad = prev_node.copy()
+    bad[0] = wl.n_nodes          # no such node in the previous tree
+    with pytest.raises(lib.PstError):
+        lib.plan_update_tree(p, t2, wl2.query_node, bad)
+    with pytest.raises(ValueError):
+        lib.plan_update_tree(p, t2, wl2.query_node, prev_node[:-1])

@@ -150,6 +150,31 @@ def test_plan_update_next_step(lib, name):
     assert_matches(wl2, O2.cpu().numpy(), L2.cpu().numpy(), K2, V2, Q2)
 
 
+@pytest.mark.parametrize("seed", [3, 11])
+def test_plan_update_tree_speculative_two_steps(lib, seed):
+    """Two speculative decoding steps: after step 1 one draft path per tree is
+    accepted, the other drafts are pruned and a new draft tree (new queries)
+    grows; step 2's plan comes from pst_plan_update_tree on step 1's plan."""
+    import torch
+    from prefix_shared_tree_gb300.torch_api import TreeDecodeAttention, to_device
+    wl = synth.speculative(batch=4, prompt=3000)
+    att = TreeDecodeAttention.from_workload(wl)
+    K, V = wl.kv_pools()
+    Q = wl.q()
+    O, L = att(to_device(Q, wl.dtype), to_device(K, wl.dtype), to_device(V, wl.dtype))
+    torch.cuda.synchronize()
+    assert_matches(wl, O.cpu().numpy(), L.cpu().numpy(), K, V, Q, queries=range(0, wl.n_queries, 9))
+    wl2, prev_node = synth.speculative_next_step(wl, seed)
+    att.update_shape(wl2.node_len, wl2.parent, wl2.page_ptr, wl2.page_ids, wl2.first_offset, wl2.num_pages,
+                     wl2.query_node, prev_node)
+    K2, V2 = wl2.kv_pools()
+    Q2 = wl2.q()
+    O2, L2 = att(to_device(Q2, wl2.dtype), to_device(K2, wl2.dtype), to_device(V2, wl2.dtype))
+    torch.cuda.synchronize()
+    assert att.check_status() == 0
+    assert_matches(wl2, O2.cpu().numpy(), L2.cpu().numpy(), K2, V2, Q2)
+
+
 def test_non_finite_junk_in_unused_page_rows(lib):
     """Rows of a page that no node covers may hold NaN; they never reach O."""
     for seed in range(6):
