@@ -268,11 +268,18 @@ const char* pst_timer_kernel_name(int32_t slot);
  *     different streams, or from different threads) race and corrupt each
  *     other. Serialise them.
  *   - The device status word used by the kernels' bounded waits lives in the
- *     array too and is not reported by this entry point.
+ *     array too; pst_noalloc_check_status reads it.
  */
 #define PST_NOALLOC_WORKSPACE_BYTES (32ll << 20)
 int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const void* K_pool, const void* V_pool,
                             float* O, float* LSE, void* stream);
+
+/* Reads and clears the device status word in the built-in scratch of
+ * pst_decode_attn_noalloc on the current device (synchronises `stream`):
+ * 0 = clean, PST_EDEVICE = a kernel of the last calls gave up (a bounded wait
+ * ran out or an index check failed; those calls' outputs are undefined);
+ * *code (nullable) receives the raw word. Allocates nothing. */
+int pst_noalloc_check_status(void* stream, int32_t* code);
 
 /* ---------------------------------------------------------------- introspection */
 typedef struct {

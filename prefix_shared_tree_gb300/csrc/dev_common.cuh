@@ -8,10 +8,40 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "pst_internal.h"
 
 namespace pst {
+
+// One-time set-up per device of a kernel's launch (its shared-memory limit,
+// the register-count check, the SM count or resident blocks): the runtime
+// keeps function attributes per device, so each device runs the set-up once,
+// under a lock, and keeps two values from it.
+constexpr int kMaxCachedDevices = 64;
+struct DeviceOnce {
+    std::mutex mu;
+    int v0[kMaxCachedDevices] = {}, v1[kMaxCachedDevices] = {};   // v0 == 0: not set up yet
+};
+template <typename F>
+inline cudaError_t per_device(DeviceOnce& c, int* v0, int* v1, F&& setup) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxCachedDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lk(c.mu);
+    if (!c.v0[dev]) {
+        int a = 0, b = 0;
+        e = setup(dev, &a, &b);
+        if (e != cudaSuccess) return e;
+        c.v0[dev] = a > 0 ? a : 1;
+        c.v1[dev] = b;
+    }
+    if (v0) *v0 = c.v0[dev];
+    if (v1) *v1 = c.v1[dev];
+    return cudaSuccess;
+}
+
 namespace dev {
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -423,25 +423,27 @@ size_t cc_smem_bytes() {
     return 1024 + kCcStages * 2 * NSLAB * kTileTokens * 128 + kCcWarps * RT * (D + 2) * 4 + 2 * kCcStages * 8 + 48;
 }
 
-// Blocks that fit on the GPU at once (single device per process); sets the
-// kernel's shared-memory limit on first use. 0 if the runtime cannot say.
+// Blocks that fit on the current device at once; sets the kernel's
+// shared-memory limit on first use on each device. 0 if the runtime cannot say.
 template <typename T, int D, int RT>
 int cc_resident_blocks(int* per_sm_out = nullptr) {
-    static int per_sm = 0, resident = 0;
-    if (!resident) {
+    static DeviceOnce once;   // per device: resident blocks, blocks per SM
+    int resident = 0, per_sm = 0;
+    const cudaError_t e = per_device(once, &resident, &per_sm, [&](int dev, int* a, int* b) {
         const size_t smem = cc_smem_bytes<T, D, RT>();
-        if (cudaFuncSetAttribute(pac_cc_kernel<T, D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess)
-            return 0;
-        int n = 0, dev = 0, sms = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pac_cc_kernel<T, D, RT>, (kCcWarps + 1) * 32, smem) !=
-                cudaSuccess ||
-            cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return 0;
-        per_sm = std::max(1, n);
-        resident = per_sm * std::max(1, sms);
-    }
+        cudaError_t r = cudaFuncSetAttribute(pac_cc_kernel<T, D, RT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)smem);
+        if (r != cudaSuccess) return r;
+        int n = 0, sms = 0;
+        r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pac_cc_kernel<T, D, RT>, (kCcWarps + 1) * 32, smem);
+        if (r != cudaSuccess) return r;
+        r = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (r != cudaSuccess) return r;
+        *b = std::max(1, n);
+        *a = *b * std::max(1, sms);
+        return cudaSuccess;
+    });
+    if (e != cudaSuccess) return 0;
     if (per_sm_out) *per_sm_out = per_sm;
     return resident;
 }

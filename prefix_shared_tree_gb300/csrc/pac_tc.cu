@@ -287,12 +287,12 @@ template <int D>
 cudaError_t launch_tc_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q,
                         int n_items, int item_off, cudaStream_t st) {
     const size_t smem = tc_smem_bytes<D>();
-    static bool attr_set = false;  // once per process (single device per process)
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(pac_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static DeviceOnce once;   // per device
+    cudaError_t e = per_device(once, nullptr, nullptr, [&](int, int* a, int*) {
+        *a = 1;
+        return cudaFuncSetAttribute(pac_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    });
+    if (e != cudaSuccess) return e;
     pac_tc_kernel<D><<<n_items, (kTcWarps + 1) * 32, smem, st>>>(P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q),
                                                                   item_off);
     return cudaGetLastError();

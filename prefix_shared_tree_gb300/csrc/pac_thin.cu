@@ -608,15 +608,14 @@ template <int R>
 cudaError_t launch_thin_r(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
                           int item_off, int counter, cudaStream_t st) {
     const size_t smem = 1024 + ThinLayout<R>::kBytes;
-    static int sms = 0;   // once per process (single device per process)
-    if (!sms) {
-        cudaError_t e = cudaFuncSetAttribute(pac_thin_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        int dev_id = 0, n = 0;
-        if ((e = cudaGetDevice(&dev_id)) != cudaSuccess) return e;
-        if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev_id)) != cudaSuccess) return e;
-        sms = std::max(1, n);
-    }
+    static DeviceOnce once;   // per device: the shared-memory limit, the SM count
+    int sms = 0;
+    cudaError_t e = per_device(once, &sms, nullptr, [&](int dev_id, int* a, int*) {
+        cudaError_t r = cudaFuncSetAttribute(pac_thin_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (r != cudaSuccess) return r;
+        return cudaDeviceGetAttribute(a, cudaDevAttrMultiProcessorCount, dev_id);
+    });
+    if (e != cudaSuccess) return e;
     const int grid = std::min(n_items, sms);
     pac_thin_kernel<R><<<grid, kThinThreads, smem, st>>>(P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q), item_off,
                                                           n_items, counter);

@@ -704,19 +704,20 @@ template <int D, bool EXACT, bool SPLIT>
 cudaError_t launch_umma_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
                           int item_off, cudaStream_t st) {
     const size_t smem = 1024 + UmmaLayout<D>::kBytes;
-    static bool attr_set = false;  // once per process (single device per process)
-    if (!attr_set) {
+    static DeviceOnce once;   // per device
+    cudaError_t e = per_device(once, nullptr, nullptr, [&](int, int* a, int*) {
         // setmaxnreg.inc waits for registers another warpgroup released: the
         // split is only valid for the launch register count it was sized for
         cudaFuncAttributes fa;
-        cudaError_t e = cudaFuncGetAttributes(&fa, pac_umma_kernel<D, EXACT, SPLIT>);
-        if (e != cudaSuccess) return e;
+        cudaError_t r = cudaFuncGetAttributes(&fa, pac_umma_kernel<D, EXACT, SPLIT>);
+        if (r != cudaSuccess) return r;
         if (fa.numRegs != UWarps<SPLIT>::kRegsLaunch) return cudaErrorInvalidConfiguration;
-        e = cudaFuncSetAttribute(pac_umma_kernel<D, EXACT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        r = cudaFuncSetAttribute(pac_umma_kernel<D, EXACT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+        *a = 1;
+        return r;
+    });
+    if (e != cudaSuccess) return e;
     pac_umma_kernel<D, EXACT, SPLIT><<<n_items, UWarps<SPLIT>::kThreads, smem, st>>>(P, *tk, *tv,
                                                                        static_cast<const __nv_bfloat16*>(Q), item_off);
     return cudaGetLastError();

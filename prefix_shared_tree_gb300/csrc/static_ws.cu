@@ -97,3 +97,19 @@ extern "C" int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const v
     if (e != cudaSuccess) return fail(PST_ECUDA, std::string("decode_attn_noalloc: POR launch: ") + cudaGetErrorString(e));
     return PST_OK;
 }
+
+extern "C" int pst_noalloc_check_status(void* stream, int32_t* code) {
+    void* ws = nullptr;
+    int rc = static_ws_address(&ws);
+    if (rc) return rc;
+    // every plan's metadata image starts with the status word (offset 0)
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t word = 0;
+    cudaError_t e = cudaMemcpyAsync(&word, ws, 4, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws, 0, 4, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return fail(PST_ECUDA, std::string("noalloc_check_status: ") + cudaGetErrorString(e));
+    if (code) *code = word;
+    if (word) return fail(PST_EDEVICE, "noalloc_check_status: device status word " + std::to_string(word));
+    return PST_OK;
+}

@@ -89,6 +89,7 @@ def lib() -> C.CDLL:
         "pst_plan_upload": (C.c_int, [vp, vp, i64, vp]),
         "pst_decode_attn": (C.c_int, [vp, vp, vp, vp, vp, vp, vp]),
         "pst_decode_attn_noalloc": (C.c_int, [vp, vp, vp, vp, vp, vp, vp]),
+        "pst_noalloc_check_status": (C.c_int, [vp, C.POINTER(i32)]),
         "pst_plan_check_status": (C.c_int, [vp, vp, C.POINTER(i32)]),
         "pst_timer_create": (C.c_int, [i32, C.POINTER(vp)]),
         "pst_timer_destroy": (None, [vp]),
@@ -327,3 +328,13 @@ def list_schedule(costs, m: int):
     mk = C.c_double(0.0)
     _check(lib().pst_list_schedule(n, cp, int(m), slot.ctypes.data_as(C.c_void_p), C.byref(mk)))
     return slot[:n], float(mk.value)
+
+
+def noalloc_check_status(stream: int = 0) -> int:
+    """Raw device status word of pst_decode_attn_noalloc's built-in scratch
+    (read and cleared; 0 = clean)."""
+    code = C.c_int32(0)
+    rc = lib().pst_noalloc_check_status(C.c_void_p(stream), C.byref(code))
+    if rc not in (PST_OK, -7):
+        _check(rc)
+    return int(code.value)
