@@ -82,6 +82,24 @@ class TreeDecodeAttention:
                    wl.num_pages, wl.query_node, wl.n_q_heads, wl.n_kv_heads, wl.d, wl.dtype, device,
                    **plan_opts)
 
+    def capture(self, Q, K_pool, V_pool, O, LSE):
+        """One decode step captured as a CUDA graph (torch.cuda.CUDAGraph) on
+        these tensors: replaying it reruns every launch of pst_decode_attn
+        (the PAC launch groups on their forked streams, the join, POR) with
+        no host work per step. The plan, its workspace and the tensors must
+        stay alive and in place while the graph is used; a new plan needs a
+        new capture. One ordinary call first sets up the kernels and the
+        plan's streams outside the capture."""
+        side = torch.cuda.Stream(self.device)
+        side.wait_stream(torch.cuda.current_stream(self.device))
+        with torch.cuda.stream(side):
+            self(Q, K_pool, V_pool, O, LSE)
+        torch.cuda.current_stream(self.device).wait_stream(side)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self(Q, K_pool, V_pool, O, LSE)
+        return g
+
     def _check(self, Q, K, V):
         td = _TORCH_DTYPE[self.dtype]
         for name, t in (("Q", Q), ("K_pool", K), ("V_pool", V)):

@@ -175,6 +175,37 @@ def test_plan_update_tree_speculative_two_steps(lib, seed):
     assert_matches(wl2, O2.cpu().numpy(), L2.cpu().numpy(), K2, V2, Q2)
 
 
+@pytest.mark.parametrize("name", ["few_shot", "speculative", "tiny"])
+def test_cuda_graph_replay_equals_direct_call(lib, name):
+    """A decode step captured as a CUDA graph (forked launch groups, join,
+    POR) and replayed gives the direct call's outputs bit for bit, also after
+    new queries are copied into the captured input tensor."""
+    import torch
+    from prefix_shared_tree_gb300.torch_api import TreeDecodeAttention, to_device
+    wl = {"few_shot": synth.few_shot, "speculative": lambda: synth.speculative(batch=3, prompt=2500),
+          "tiny": synth.tiny_two_level}[name]()
+    att = TreeDecodeAttention.from_workload(wl)
+    K, V = wl.kv_pools()
+    Q = wl.q()
+    Qd, Kd, Vd = to_device(Q, wl.dtype), to_device(K, wl.dtype), to_device(V, wl.dtype)
+    O_ref, L_ref = att(Qd, Kd, Vd)
+    O = torch.full_like(O_ref, float("nan"))
+    L = torch.full_like(L_ref, float("nan"))
+    g = att.capture(Qd, Kd, Vd, O, L)
+    for _ in range(2):
+        O.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(O, O_ref) and torch.equal(L, L_ref)
+    # new queries through the same graph
+    Q2 = np.roll(Q, 1, axis=0)
+    Qd.copy_(to_device(Q2, wl.dtype))
+    g.replay()
+    torch.cuda.synchronize()
+    assert att.check_status() == 0
+    assert_matches(wl, O.cpu().numpy(), L.cpu().numpy(), K, V, Q2, queries=range(0, wl.n_queries, 5))
+
+
 def test_non_finite_junk_in_unused_page_rows(lib):
     """Rows of a page that no node covers may hold NaN; they never reach O."""
     for seed in range(6):
