@@ -89,6 +89,16 @@ typedef struct {
                                waits, TMA loads drained) and the device status word
                                is set. The outputs of such a call are undefined;
                                pst_plan_check_status reports PST_EDEVICE.        */
+    int32_t side_streams;   /* how the PAC launch groups of one call share the GPU.
+                               0 (default): all on the caller's stream, each
+                               launch after the first with a programmatic
+                               dependency on the one before (it starts once every
+                               block of that one has started; POR waits for all
+                               on the device). 1: each group on its own stream
+                               forked from the caller's and joined before POR.
+                               pst_decode_attn_timed always uses 1; the
+                               no-allocation entry point runs the groups one
+                               after the other with 1.                        */
 } pst_plan_opts;
 
 /* Fill `o` with the defaults above. */

@@ -26,39 +26,41 @@
 namespace pst {
 
 cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const void* tv, const void* Q,
-                          int r_tile, int n_items, int item_off, int counter, cudaStream_t st);
+                          int r_tile, int n_items, int item_off, int counter, cudaStream_t st, bool pdl);
 cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
-                          int item_off, cudaStream_t st);
+                          int item_off, cudaStream_t st, bool pdl);
 cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
-                            int item_off, bool exact_p, bool split_rows, cudaStream_t st);
+                            int item_off, bool exact_p, bool split_rows, cudaStream_t st, bool pdl);
 cudaError_t launch_pac_thin(const DevPlan& P, const void* tk5, const void* tv5, const void* Q, int rows_per_head,
-                            int n_items, int item_off, int counter, cudaStream_t st);
+                            int n_items, int item_off, int counter, cudaStream_t st, bool pdl);
 
 // Tensor-core PAC launch group g (pst_plan::tc_group_cnt): P rounded once
 // (g < 2) or exact, more than 128 rows per block (even g) or at most 128.
 // The mma.sync engine has all its items in group 1.
 cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
-                            int g, cudaStream_t st) {
+                            int g, LaunchSeq& ls) {
     int64_t off = 0;
     for (int k = 0; k < g; ++k) off += p->tc_group_cnt[k];
     const int n = (int)p->tc_group_cnt[g];
     if (n == 0) return cudaSuccess;
-    if (p->opts.tc_engine == 1) return launch_pac_tc(dp, tk, tv, Q, n, (int)off, st);
+    if (p->opts.tc_engine == 1) return launch_pac_tc(dp, tk, tv, Q, n, (int)off, ls.st, ls.next_pdl());
     // d = 128: V in 4 KB page boxes (the pool's second 5-D view)
     const void* tv_umma = p->d == 128 ? static_cast<const void*>(static_cast<const unsigned char*>(tv) + 256) : tv;
-    return launch_pac_umma(dp, tk, tv_umma, Q, n, (int)off, g >= 2, (g & 1) == 0, st);
+    return launch_pac_umma(dp, tk, tv_umma, Q, n, (int)off, g >= 2, (g & 1) == 0, ls.st, ls.next_pdl());
 }
 
 // Thin chunks: tcgen05 thin PAC launches for row blocks of 8 and of 4 (work
 // counters 4, 5; the pools' 5-D maps follow their 3-D maps), or one CUDA-core
 // launch per row tile (counters 0-3).
 cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
-                            cudaStream_t st) {
+                            LaunchSeq& ls) {
     if (p->thin) {
         for (int k = 0; k < 2; ++k) {
+            if (p->cc_class_cnt[k] == 0) continue;
             cudaError_t e = launch_pac_thin(dp, static_cast<const unsigned char*>(tk) + 128,
                                             static_cast<const unsigned char*>(tv) + 128, Q, k == 0 ? 8 : 4,
-                                            (int)p->cc_class_cnt[k], (int)p->cc_class_off[k], 4 + k, st);
+                                            (int)p->cc_class_cnt[k], (int)p->cc_class_off[k], 4 + k, ls.st,
+                                            ls.next_pdl());
             if (e != cudaSuccess) return e;
         }
         return cudaSuccess;
@@ -66,7 +68,7 @@ cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk
     for (int k = 0; k < 4; ++k) {
         if (p->cc_class_cnt[k] == 0) continue;
         cudaError_t e = launch_pac_cc(dp, p->dtype, tk, tv, Q, 8 >> k, (int)p->cc_class_cnt[k],
-                                      (int)p->cc_class_off[k], k, st);
+                                      (int)p->cc_class_off[k], k, ls.st, ls.next_pdl());
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
@@ -79,6 +81,7 @@ constexpr int kPorWarps = 8;
 template <int D>
 __global__ void __launch_bounds__(kPorWarps * 32) por_kernel(DevPlan P, float* __restrict__ O, float* __restrict__ LSE) {
     constexpr int EPL = D / 32;
+    pdl_wait();   // launched early behind the PAC grids: wait for all of them
     // every PAC launch of this call has finished: rearm their work queues
     if (blockIdx.x == 0 && threadIdx.x < kNumCounters) P.counters[threadIdx.x] = 0;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -244,12 +247,13 @@ DevPlan dev_plan_at(const pst_plan* p, void* ws) {
 
 static DevPlan dev_plan(const pst_plan* p) { return dev_plan_at(p, p->d_ws); }
 
-cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, cudaStream_t st) {
+cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, LaunchSeq& ls) {
     const int64_t warps = (int64_t)dp.n_queries * dp.n_q_heads;
     const int blocks = (int)((warps + dev::kPorWarps - 1) / dev::kPorWarps);
-    if (dp.d == 128) dev::por_kernel<128><<<blocks, dev::kPorWarps * 32, 0, st>>>(dp, O, LSE);
-    else dev::por_kernel<64><<<blocks, dev::kPorWarps * 32, 0, st>>>(dp, O, LSE);
-    return cudaGetLastError();
+    const bool pdl = ls.next_pdl();
+    if (dp.d == 128)
+        return launch_kernel(dev::por_kernel<128>, dim3(blocks), dim3(dev::kPorWarps * 32), 0, ls.st, pdl, dp, O, LSE);
+    return launch_kernel(dev::por_kernel<64>, dim3(blocks), dim3(dev::kPorWarps * 32), 0, ls.st, pdl, dp, O, LSE);
 }
 
 }  // namespace pst
@@ -313,14 +317,36 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
         cudaEventRecord(ev[0], st);
     }
     cudaError_t e;
-    // The PAC launch groups (four tensor-core ones, the CUDA-core one) write
-    // disjoint partial rows. The first non-empty one runs on `st`, the others
-    // on side streams forked from it, so their blocks fill the SMs the other
-    // groups' blocks leave idle; POR waits on the joins.
+    // The PAC launch groups (four tensor-core ones, the thin one) write
+    // disjoint partial rows, so they may run side by side; POR merges after
+    // all of them. Two ways to let them share the SMs:
+    //  - one stream, every launch after the first with a programmatic
+    //    dependency on the one before (the default): a group's blocks start
+    //    once every block of the groups launched before it has started, so the
+    //    SMs fill in launch order (tensor-core groups first), which is the
+    //    order the planner's list schedule assumes, and no event crosses
+    //    streams; POR waits for all of them on the device;
+    //  - the first non-empty group on `st`, the others on side streams forked
+    //    from it and joined before POR (also the timed path: its events
+    //    between launches would break a chain).
     constexpr int kGroups = 5;
     bool has[kGroups];
     for (int g = 0; g < 4; ++g) has[g] = p->tc_group_cnt[g] > 0;
     has[4] = p->n_cc_items > 0;
+    const bool chain = p->opts.side_streams == 0 && !ev;
+    if (chain) {
+        LaunchSeq ls(st, true);
+        for (int g = 0; g < kGroups; ++g) {
+            if (!has[g]) continue;
+            e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g, ls)
+                      : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, ls);
+            if (e != cudaSuccess) return cuda_fail(g < 4 ? "decode_attn: PAC (tensor core) launch"
+                                                         : "decode_attn: PAC (thin chunks) launch", e);
+        }
+        e = launch_por(dp, O, LSE, ls);
+        if (e != cudaSuccess) return cuda_fail("decode_attn: POR launch", e);
+        return PST_OK;
+    }
     cudaStream_t gst[kGroups] = {st, st, st, st, st};
     int n_side = 0;
     bool first = true;
@@ -352,8 +378,9 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
     }
     for (int g = 0; g < kGroups; ++g) {
         if (!has[g]) continue;
-        e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g, gst[g])
-                  : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, gst[g]);
+        LaunchSeq ls(gst[g], false);
+        e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g, ls)
+                  : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, ls);
         if (e != cudaSuccess) return cuda_fail(g < 4 ? "decode_attn: PAC (tensor core) launch"
                                                      : "decode_attn: PAC (thin chunks) launch", e);
         if (ev) cudaEventRecord(ev[1 + g], gst[g]);
@@ -365,7 +392,8 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
         cudaStreamWaitEvent(st, static_cast<cudaEvent_t>(p->ev_join[k]), 0);
     }
     if (ev) cudaEventRecord(ev[6], st);
-    e = launch_por(dp, O, LSE, st);
+    LaunchSeq lpor(st, false);
+    e = launch_por(dp, O, LSE, lpor);
     if (e != cudaSuccess) return cuda_fail("decode_attn: POR launch", e);
     if (ev) {
         cudaEventRecord(ev[7], st);

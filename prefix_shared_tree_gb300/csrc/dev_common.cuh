@@ -9,6 +9,7 @@
 
 #include <cstdint>
 #include <mutex>
+#include <utility>
 
 #include "pst_internal.h"
 
@@ -42,7 +43,55 @@ inline cudaError_t per_device(DeviceOnce& c, int* v0, int* v1, F&& setup) {
     return cudaSuccess;
 }
 
+// Kernel launch with an optional programmatic dependency on the kernel
+// before it on `st` (programmatic dependent launch, sm_90 and later). With
+// `pdl` the kernel may start as soon as every block of that kernel has
+// executed griddepcontrol.launch_dependents (each PAC kernel does so first
+// thing), instead of when it has finished: the PAC launch groups of one call
+// then share the SMs in launch order on a single stream. A later launch
+// without the attribute still waits for every kernel before it to finish,
+// and griddepcontrol.wait waits for all of them too.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                 bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+// The kernels of one decode call in launch order: on one stream (`chain`)
+// every kernel after the first gets the programmatic dependency above; on
+// per-group streams none does.
+struct LaunchSeq {
+    cudaStream_t st;
+    bool chain;
+    int n = 0;
+    LaunchSeq(cudaStream_t s, bool c) : st(s), chain(c) {}
+    bool next_pdl() {
+        const bool r = chain && n > 0;
+        ++n;
+        return r;
+    }
+};
+
 namespace dev {
+
+// Let the next kernel on the stream start once every block of this one has
+// started (no-op when it was not launched with the attribute).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until every kernel this one depends on has finished and its writes
+// are visible (returns at once for a launch without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -348,6 +348,7 @@ pac_cc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
     constexpr int NSLAB = D * EB / 128;
     constexpr uint32_t kStage = 2 * NSLAB * kTileTokens * 128;
     extern __shared__ uint8_t smem_raw[];
+    pdl_launch_dependents();   // the next launch group may take the SMs this grid leaves
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring = smem_u32(base);
     float* scratch = reinterpret_cast<float*>(base + kCcStages * kStage);
@@ -450,14 +451,13 @@ int cc_resident_blocks(int* per_sm_out = nullptr) {
 
 template <typename T, int D, int RT>
 cudaError_t launch_cc_rt(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q,
-                         int n_items, int item_off, int counter, cudaStream_t st) {
+                         int n_items, int item_off, int counter, cudaStream_t st, bool pdl) {
     const size_t smem = cc_smem_bytes<T, D, RT>();
     const int resident = cc_resident_blocks<T, D, RT>();
     if (!resident) return cudaErrorInvalidConfiguration;
     const int grid = std::min(n_items, resident);
-    pac_cc_kernel<T, D, RT><<<grid, (kCcWarps + 1) * 32, smem, st>>>(P, *tk, *tv, static_cast<const T*>(Q), item_off,
-                                                                    n_items, counter);
-    return cudaGetLastError();
+    return launch_kernel(pac_cc_kernel<T, D, RT>, dim3(grid), dim3((kCcWarps + 1) * 32), smem, st, pdl, P, *tk, *tv,
+                         static_cast<const T*>(Q), item_off, n_items, counter);
 }
 
 template <typename T, int D>
@@ -474,12 +474,12 @@ int cc_per_sm_t(int r_tile) {
 
 template <typename T, int D>
 cudaError_t launch_cc_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int r_tile,
-                        int n_items, int item_off, int counter, cudaStream_t st) {
+                        int n_items, int item_off, int counter, cudaStream_t st, bool pdl) {
     switch (r_tile) {
-        case 1: return launch_cc_rt<T, D, 1>(P, tk, tv, Q, n_items, item_off, counter, st);
-        case 2: return launch_cc_rt<T, D, 2>(P, tk, tv, Q, n_items, item_off, counter, st);
-        case 4: return launch_cc_rt<T, D, 4>(P, tk, tv, Q, n_items, item_off, counter, st);
-        default: return launch_cc_rt<T, D, 8>(P, tk, tv, Q, n_items, item_off, counter, st);
+        case 1: return launch_cc_rt<T, D, 1>(P, tk, tv, Q, n_items, item_off, counter, st, pdl);
+        case 2: return launch_cc_rt<T, D, 2>(P, tk, tv, Q, n_items, item_off, counter, st, pdl);
+        case 4: return launch_cc_rt<T, D, 4>(P, tk, tv, Q, n_items, item_off, counter, st, pdl);
+        default: return launch_cc_rt<T, D, 8>(P, tk, tv, Q, n_items, item_off, counter, st, pdl);
     }
 }
 
@@ -496,15 +496,15 @@ int cc_blocks_per_sm(pst_dtype dt, int d, int r_tile) {
 }
 
 cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const void* tv, const void* Q,
-                          int r_tile, int n_items, int item_off, int counter, cudaStream_t st) {
+                          int r_tile, int n_items, int item_off, int counter, cudaStream_t st, bool pdl) {
     const CUtensorMap* k = static_cast<const CUtensorMap*>(tk);
     const CUtensorMap* v = static_cast<const CUtensorMap*>(tv);
     if (dt == PST_BF16) {
-        if (P.d == 128) return dev::launch_cc_t<__nv_bfloat16, 128>(P, k, v, Q, r_tile, n_items, item_off, counter, st);
-        return dev::launch_cc_t<__nv_bfloat16, 64>(P, k, v, Q, r_tile, n_items, item_off, counter, st);
+        if (P.d == 128) return dev::launch_cc_t<__nv_bfloat16, 128>(P, k, v, Q, r_tile, n_items, item_off, counter, st, pdl);
+        return dev::launch_cc_t<__nv_bfloat16, 64>(P, k, v, Q, r_tile, n_items, item_off, counter, st, pdl);
     }
-    if (P.d == 128) return dev::launch_cc_t<float, 128>(P, k, v, Q, r_tile, n_items, item_off, counter, st);
-    return dev::launch_cc_t<float, 64>(P, k, v, Q, r_tile, n_items, item_off, counter, st);
+    if (P.d == 128) return dev::launch_cc_t<float, 128>(P, k, v, Q, r_tile, n_items, item_off, counter, st, pdl);
+    return dev::launch_cc_t<float, 64>(P, k, v, Q, r_tile, n_items, item_off, counter, st, pdl);
 }
 
 }  // namespace pst

@@ -68,6 +68,7 @@ pac_tc_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_co
     constexpr int KSTEPS = D / 16;
 
     extern __shared__ uint8_t smem_raw[];
+    pdl_launch_dependents();   // the next launch group may take the SMs this grid leaves
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t ring = smem_u32(base);
     uint8_t* qs = base + kTcStages * kStage;
@@ -285,7 +286,7 @@ size_t tc_smem_bytes() {
 
 template <int D>
 cudaError_t launch_tc_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q,
-                        int n_items, int item_off, cudaStream_t st) {
+                        int n_items, int item_off, cudaStream_t st, bool pdl) {
     const size_t smem = tc_smem_bytes<D>();
     static DeviceOnce once;   // per device
     cudaError_t e = per_device(once, nullptr, nullptr, [&](int, int* a, int*) {
@@ -293,19 +294,18 @@ cudaError_t launch_tc_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorM
         return cudaFuncSetAttribute(pac_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     });
     if (e != cudaSuccess) return e;
-    pac_tc_kernel<D><<<n_items, (kTcWarps + 1) * 32, smem, st>>>(P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q),
-                                                                  item_off);
-    return cudaGetLastError();
+    return launch_kernel(pac_tc_kernel<D>, dim3(n_items), dim3((kTcWarps + 1) * 32), smem, st, pdl, P, *tk, *tv,
+                         static_cast<const __nv_bfloat16*>(Q), item_off);
 }
 
 }  // namespace dev
 
 cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
-                          int item_off, cudaStream_t st) {
+                          int item_off, cudaStream_t st, bool pdl) {
     const CUtensorMap* k = static_cast<const CUtensorMap*>(tk);
     const CUtensorMap* v = static_cast<const CUtensorMap*>(tv);
-    if (P.d == 128) return dev::launch_tc_t<128>(P, k, v, Q, n_items, item_off, st);
-    return dev::launch_tc_t<64>(P, k, v, Q, n_items, item_off, st);
+    if (P.d == 128) return dev::launch_tc_t<128>(P, k, v, Q, n_items, item_off, st, pdl);
+    return dev::launch_tc_t<64>(P, k, v, Q, n_items, item_off, st, pdl);
 }
 
 }  // namespace pst

@@ -174,6 +174,7 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     constexpr int kSh = R == 4 ? 2 : 1;   // half-warp lane l holds row (l & 15) >> kSh after a reduction
     static_assert(R == 4 || R == 8, "rows per head");
     extern __shared__ uint8_t smem_raw[];
+    pdl_launch_dependents();   // the next launch group may take the SMs this grid leaves
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(base);
     const uint32_t bars = sbase + L::kBars;
@@ -606,7 +607,7 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
 
 template <int R>
 cudaError_t launch_thin_r(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
-                          int item_off, int counter, cudaStream_t st) {
+                          int item_off, int counter, cudaStream_t st, bool pdl) {
     const size_t smem = 1024 + ThinLayout<R>::kBytes;
     static DeviceOnce once;   // per device: the shared-memory limit, the SM count
     int sms = 0;
@@ -617,22 +618,21 @@ cudaError_t launch_thin_r(const DevPlan& P, const CUtensorMap* tk, const CUtenso
     });
     if (e != cudaSuccess) return e;
     const int grid = std::min(n_items, sms);
-    pac_thin_kernel<R><<<grid, kThinThreads, smem, st>>>(P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q), item_off,
-                                                          n_items, counter);
-    return cudaGetLastError();
+    return launch_kernel(pac_thin_kernel<R>, dim3(grid), dim3(kThinThreads), smem, st, pdl, P, *tk, *tv,
+                         static_cast<const __nv_bfloat16*>(Q), item_off, n_items, counter);
 }
 
 }  // namespace dev
 
 // rows_per_head: the items' row block (4 or 8); tk5 / tv5: the pools' 5-D maps
 cudaError_t launch_pac_thin(const DevPlan& P, const void* tk5, const void* tv5, const void* Q, int rows_per_head,
-                            int n_items, int item_off, int counter, cudaStream_t st) {
+                            int n_items, int item_off, int counter, cudaStream_t st, bool pdl) {
     if (P.d != 128 || P.n_kv_heads % kThinHeads) return cudaErrorInvalidValue;
     if (n_items <= 0) return cudaSuccess;
     const CUtensorMap* k = static_cast<const CUtensorMap*>(tk5);
     const CUtensorMap* v = static_cast<const CUtensorMap*>(tv5);
-    return rows_per_head == 4 ? dev::launch_thin_r<4>(P, k, v, Q, n_items, item_off, counter, st)
-                              : dev::launch_thin_r<8>(P, k, v, Q, n_items, item_off, counter, st);
+    return rows_per_head == 4 ? dev::launch_thin_r<4>(P, k, v, Q, n_items, item_off, counter, st, pdl)
+                              : dev::launch_thin_r<8>(P, k, v, Q, n_items, item_off, counter, st, pdl);
 }
 
 }  // namespace pst

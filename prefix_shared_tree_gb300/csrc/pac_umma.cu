@@ -271,6 +271,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     constexpr int NSLAB = L::NSLAB;
     constexpr int KST = L::KST, VST = L::VST;
     extern __shared__ uint8_t smem_raw[];
+    pdl_launch_dependents();   // the next launch group may take the SMs this grid leaves
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(base);
     const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sQ = sbase + L::kQ;
@@ -702,7 +703,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
 
 template <int D, bool EXACT, bool SPLIT>
 cudaError_t launch_umma_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
-                          int item_off, cudaStream_t st) {
+                          int item_off, cudaStream_t st, bool pdl) {
     const size_t smem = 1024 + UmmaLayout<D>::kBytes;
     static DeviceOnce once;   // per device
     cudaError_t e = per_device(once, nullptr, nullptr, [&](int, int* a, int*) {
@@ -718,29 +719,28 @@ cudaError_t launch_umma_t(const DevPlan& P, const CUtensorMap* tk, const CUtenso
         return r;
     });
     if (e != cudaSuccess) return e;
-    pac_umma_kernel<D, EXACT, SPLIT><<<n_items, UWarps<SPLIT>::kThreads, smem, st>>>(P, *tk, *tv,
-                                                                       static_cast<const __nv_bfloat16*>(Q), item_off);
-    return cudaGetLastError();
+    return launch_kernel(pac_umma_kernel<D, EXACT, SPLIT>, dim3(n_items), dim3(UWarps<SPLIT>::kThreads), smem, st, pdl,
+                         P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q), item_off);
 }
 
 template <int D, bool EXACT>
 cudaError_t launch_umma_m(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
-                          int item_off, bool split_rows, cudaStream_t st) {
-    return split_rows ? launch_umma_t<D, EXACT, true>(P, tk, tv, Q, n_items, item_off, st)
-                      : launch_umma_t<D, EXACT, false>(P, tk, tv, Q, n_items, item_off, st);
+                          int item_off, bool split_rows, cudaStream_t st, bool pdl) {
+    return split_rows ? launch_umma_t<D, EXACT, true>(P, tk, tv, Q, n_items, item_off, st, pdl)
+                      : launch_umma_t<D, EXACT, false>(P, tk, tv, Q, n_items, item_off, st, pdl);
 }
 
 }  // namespace dev
 
 cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items, int item_off,
-                            bool exact_p, bool split_rows, cudaStream_t st) {
+                            bool exact_p, bool split_rows, cudaStream_t st, bool pdl) {
     const CUtensorMap* k = static_cast<const CUtensorMap*>(tk);
     const CUtensorMap* v = static_cast<const CUtensorMap*>(tv);
     if (P.d == 128)
-        return exact_p ? dev::launch_umma_m<128, true>(P, k, v, Q, n_items, item_off, split_rows, st)
-                       : dev::launch_umma_m<128, false>(P, k, v, Q, n_items, item_off, split_rows, st);
-    return exact_p ? dev::launch_umma_m<64, true>(P, k, v, Q, n_items, item_off, split_rows, st)
-                   : dev::launch_umma_m<64, false>(P, k, v, Q, n_items, item_off, split_rows, st);
+        return exact_p ? dev::launch_umma_m<128, true>(P, k, v, Q, n_items, item_off, split_rows, st, pdl)
+                       : dev::launch_umma_m<128, false>(P, k, v, Q, n_items, item_off, split_rows, st, pdl);
+    return exact_p ? dev::launch_umma_m<64, true>(P, k, v, Q, n_items, item_off, split_rows, st, pdl)
+                   : dev::launch_umma_m<64, false>(P, k, v, Q, n_items, item_off, split_rows, st, pdl);
 }
 
 }  // namespace pst

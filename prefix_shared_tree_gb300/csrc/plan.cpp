@@ -192,6 +192,7 @@ extern "C" void pst_plan_opts_default(pst_plan_opts* o) {
     o->p_bf16_min_tokens = kPBf16MinTokens;
     o->thin_engine = 0;
     o->debug_stall = 0;
+    o->side_streams = 0;
 }
 
 namespace {

@@ -19,10 +19,10 @@
 namespace pst {
 
 cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
-                            int g, cudaStream_t st);
+                            int g, LaunchSeq& ls);
 cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
-                            cudaStream_t st);
-cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, cudaStream_t st);
+                            LaunchSeq& ls);
+cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, LaunchSeq& ls);
 int encode_pool_map(const pst_plan* p, const void* pool, unsigned char* out);
 DevPlan dev_plan_at(const pst_plan* p, void* ws);
 
@@ -88,12 +88,14 @@ extern "C" int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const v
     rc = encode_pool_map(p, V, tv);
     if (rc) return rc;
     const DevPlan dp = dev_plan_at(p, ws);
-    // the launch groups run one after the other on `stream`
+    // the launch groups on `stream`: chained by programmatic dependencies
+    // (the default), else one after the other
+    LaunchSeq ls(st, p->opts.side_streams == 0);
     for (int g = 0; g < 5; ++g) {
-        e = g < 4 ? launch_tc_group(p, dp, tk, tv, Q, g, st) : launch_cc_group(p, dp, tk, tv, Q, st);
+        e = g < 4 ? launch_tc_group(p, dp, tk, tv, Q, g, ls) : launch_cc_group(p, dp, tk, tv, Q, ls);
         if (e != cudaSuccess) return fail(PST_ECUDA, std::string("decode_attn_noalloc: PAC launch: ") + cudaGetErrorString(e));
     }
-    e = launch_por(dp, O, LSE, st);
+    e = launch_por(dp, O, LSE, ls);
     if (e != cudaSuccess) return fail(PST_ECUDA, std::string("decode_attn_noalloc: POR launch: ") + cudaGetErrorString(e));
     return PST_OK;
 }

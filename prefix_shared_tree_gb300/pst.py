@@ -34,7 +34,7 @@ class PlanOpts(C.Structure):
     _fields_ = [("split_policy", C.c_int32), ("fixed_chunk", C.c_int32), ("tc_min_rows", C.c_int32),
                 ("pack_masks", C.c_int32), ("num_sms", C.c_int32), ("slots_per_sm", C.c_int32),
                 ("tc_engine", C.c_int32), ("tc_block_rows", C.c_int32), ("p_bf16_min_tokens", C.c_int32),
-                ("thin_engine", C.c_int32), ("debug_stall", C.c_int32)]
+                ("thin_engine", C.c_int32), ("debug_stall", C.c_int32), ("side_streams", C.c_int32)]
 
 
 class PlanStats(C.Structure):
@@ -212,7 +212,8 @@ def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int,
                 split_policy: str = "cost_model", fixed_chunk: int | None = None,
                 tc_min_rows: int | None = None, pack_masks: bool | None = None, num_sms: int = 0,
                 slots_per_sm: int = 0, tc_engine: str = "tcgen05", tc_block_rows: int = 256,
-                p_bf16_min_tokens: int = 0, thin_engine: str = "tcgen05", debug_stall: bool = False) -> Plan:
+                p_bf16_min_tokens: int = 0, thin_engine: str = "tcgen05", debug_stall: bool = False,
+                side_streams: bool = False) -> Plan:
     o = plan_opts_default()
     o.split_policy = SPLIT[split_policy]
     if fixed_chunk is not None:
@@ -228,6 +229,7 @@ def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int,
     o.p_bf16_min_tokens = p_bf16_min_tokens
     o.thin_engine = {"tcgen05": 0, "cuda_core": 1}[thin_engine]
     o.debug_stall = int(bool(debug_stall))
+    o.side_streams = int(bool(side_streams))
     qn, qnp = _arr(query_node, np.int32)
     h = C.c_void_p()
     _check(lib().pst_plan_create(tree._h, len(qn), qnp, n_q_heads, n_kv_heads, d, DTYPES[dtype],

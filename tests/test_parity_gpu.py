@@ -206,6 +206,34 @@ def test_cuda_graph_replay_equals_direct_call(lib, name):
     assert_matches(wl, O.cpu().numpy(), L.cpu().numpy(), K, V, Q2, queries=range(0, wl.n_queries, 5))
 
 
+@pytest.mark.parametrize("case", ["few_shot", "random_bf16_all_groups", "random_fp32_cuda_core", "mma_sync"])
+def test_launch_modes_give_identical_outputs(lib, case):
+    """The PAC launch groups chained on one stream (each launch after the
+    first with a programmatic dependency on the one before: the default) and
+    on forked side streams joined before POR give the same outputs bit for
+    bit; the side-stream outputs also match the oracle."""
+    if case == "few_shot":
+        wl, opts = synth.few_shot(), {}
+    elif case == "random_bf16_all_groups":
+        # five PAC launches: tensor-core groups with P rounded once and exact,
+        # above and below 128 rows per block, and the thin PAC
+        wl = synth.random_tree(5189, max_nodes=16, max_len=1500, heads=(32, 8), d=128, dtype="bf16", n_queries=48)
+        opts = {"p_bf16_min_tokens": 256}
+    elif case == "random_fp32_cuda_core":
+        wl = synth.random_tree(5151, max_nodes=12, max_len=200, heads=(8, 2), d=64, dtype="f32", n_queries=24)
+        opts = {}
+    else:
+        wl = synth.random_tree(5152, max_nodes=12, max_len=200, heads=(16, 4), d=128, dtype="bf16", n_queries=24)
+        opts = {"tc_engine": "mma_sync", "tc_min_rows": 1}
+    O1, L1, (K, V, Q), att1 = run_gpu(lib, wl, **opts)
+    O2, L2, _, att2 = run_gpu(lib, wl, pools=(K, V), Q=Q, side_streams=True, **opts)
+    assert att1.plan.stats()["n_launches"] == att2.plan.stats()["n_launches"]
+    assert np.array_equal(O1.view(np.uint32), O2.view(np.uint32))
+    assert np.array_equal(L1.view(np.uint32), L2.view(np.uint32))
+    qs = range(0, wl.n_queries, 7) if case == "few_shot" else None
+    assert_matches(wl, O2, L2, K, V, Q, queries=qs)
+
+
 def test_non_finite_junk_in_unused_page_rows(lib):
     """Rows of a page that no node covers may hold NaN; they never reach O."""
     for seed in range(6):

@@ -6,7 +6,8 @@ depends only on its own item (never on which block ran it or when), so the
 two paths agree bit for bit. Two calls are checked, with a different plan
 (more partial rows) run through the shared array between them, so that the
 second call starts from unrelated contents. The array's status word is read
-with pst_noalloc_check_status. This file sorts last so that a run stopping at
+with pst_noalloc_check_status. Both launch orders are checked (launch groups
+chained on one stream, and one after the other). This file sorts last so that a run stopping at
 its first failure has run everything else."""
 import numpy as np
 import pytest
@@ -37,10 +38,14 @@ def _other_plan():
                                                                               heads=(8, 2), d=128, n_queries=30),
                                   synth.tiny_two_level],
                          ids=["few_shot", "random_bf16", "tiny_fp32"])
-def test_noalloc_matches_workspace_path(lib, make):
+@pytest.mark.parametrize("side_streams", [False, True], ids=["chained", "serial"])
+def test_noalloc_matches_workspace_path(lib, make, side_streams):
+    """side_streams: the workspace path forks its launch groups onto side
+    streams and the no-allocation path runs them one after the other; else
+    both chain them on the caller's stream."""
     import torch
     wl = make()
-    att, Q, K, V = _setup(wl)
+    att, Q, K, V = _setup(wl, side_streams=side_streams)
     assert att.plan.workspace_bytes <= lib.NOALLOC_WORKSPACE_BYTES
     O_ref, L_ref = att(Q, K, V)
     torch.cuda.synchronize()
