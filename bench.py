@@ -381,6 +381,21 @@ def measure(name, args, dev, steps, warmup, timer_steps, plan_opts, e2e=False, w
     gv1.record(stream)
     torch.cuda.synchronize(dev)
     graph_us = gv0.elapsed_time(gv1) * 1e3 / steps
+
+    # ---- one step at a time from an idle GPU: the latency of a single call
+    def _single(fn, n=30):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ts = []
+        for i in range(n):
+            torch.cuda.synchronize(dev)
+            a.record(stream)
+            fn(i)
+            b.record(stream)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) * 1e3)
+        return float(statistics.median(ts))
+    single_us = _single(lambda i: att(Qd[i % copies], Kd[i % copies], Vd[i % copies], O[i % copies], L[i % copies]))
+    single_graph_us = _single(lambda i: graphs[i % copies].replay())
     del graphs
     if att.check_status() != 0:
         raise RuntimeError(f"{name}: device status word set during the graph replays")
@@ -399,6 +414,7 @@ def measure(name, args, dev, steps, warmup, timer_steps, plan_opts, e2e=False, w
     dom_achieved = alg[dom] / (dom_us * 1e-6) / 1e9 if dom_us > 0 else 0.0
     out = {
         "workload": name, "wl": wl, "us": us, "graph_us": graph_us, "U": U, "copies": copies,
+        "single_us": single_us, "single_graph_us": single_graph_us,
         "clocks": clk.summary(),
         "plan": {"plan_us": round(st["plan_us"], 1), "plan_wall_us": round(plan_wall_us, 1),
                  "plan_update_us": round(update_us, 1),
@@ -443,6 +459,7 @@ def _config_entry(m):
     gbs = m["U"] / (m["us"] * 1e-6) / 1e9
     return {
         "us_per_step": round(m["us"], 3), "graph_replay_us_per_step": round(m["graph_us"], 3),
+        "single_step_us": {"call": round(m["single_us"], 3), "graph": round(m["single_graph_us"], 3)},
         "unique_kv_bytes": m["U"], "achieved_unique_kv_gbs": round(gbs, 1),
         "frac_of_8tbs": round(gbs / NOMINAL_HBM_GBS, 4), "frac_of_measured_hbm": round(gbs / peak, 4),
         "dominant_kernel": {"kernel": m["dom"], "algorithmic_bytes": m["alg"][m["dom"]],
@@ -509,11 +526,16 @@ def run_ours(args, rank, world):
         "graph_replay": {"value": round(h["graph_us"], 3), "unit": "us/step",
                          "note": "the same steps replayed from CUDA graphs of pst_decode_attn (one capture per "
                                  "input copy): no host work per step"},
+        "single_step_us": {"call": round(h["single_us"], 3), "graph": round(h["single_graph_us"], 3),
+                           "note": "median of 30 steps each launched on an idle GPU (synchronised before and "
+                                   "after): the latency of one call, host launch work included"},
         "group_end_us": h["group_end_us"],
         "por_us": h["por_us"],
         "timer_note": f"group_end_us: from the call's start to the end of each PAC launch group (the groups run "
                       f"side by side), and POR alone, over a separate loop of {args.timer_steps} calls with the "
-                      f"library's events; the timed loop above records none",
+                      f"library's events; that timed entry point forks the groups onto side streams (events "
+                      f"between chained launches would serialise them), while the timed loop above, the graph "
+                      f"replays and e2e use the default chained launch and record no events",
         "roofline": {"bound": "hbm", "kernel": h["dom"], "achieved": round(h["dom_achieved"], 1), "peak": peak,
                      "peak_source": peak_src, "unit": "GB/s", "frac": round(h["dom_achieved"] / peak, 4),
                      "traffic": traffic, "algorithmic_bytes": h["alg"][h["dom"]]},
