@@ -214,6 +214,11 @@ int pst_plan_upload(pst_plan* p, void* d_workspace, int64_t bytes, void* stream)
  *
  * Page rows not covered by any node may hold any finite or non-finite values;
  * they are never read into the result. Requires a prior pst_plan_upload.
+ * Launches (opts.side_streams = 0): the PAC launch groups and POR on `stream`
+ * only, each after the first with a programmatic dependency on the one
+ * before (programmatic dependent launch); work queued on `stream` after the
+ * call starts when all of it has finished. The call can be captured into a
+ * CUDA graph after one ordinary call (which sets up the kernels).
  * Errors: PST_EWORKSPACE (no upload), PST_EINVAL (null pointer), PST_ECUDA
  * (launch failure). Device-side faults detected by the kernels' own checks
  * are reported by pst_plan_check_status().
@@ -230,7 +235,9 @@ int pst_plan_check_status(const pst_plan* p, void* stream, int32_t* code);
  * Per-kernel device times of pst_decode_attn, for roofline accounting. A timer
  * holds CUDA events for up to `max_calls` calls; pst_decode_attn_timed records
  * an event at the start of the call, after each PAC launch group that has
- * work (on the stream that ran it) and around POR. The events themselves add
+ * work (on the stream that ran it) and around POR. It always runs the groups
+ * on side streams forked from `stream` (opts.side_streams = 1), since events
+ * between chained launches would serialise them. The events themselves add
  * to the call's time: time steps for throughput with pst_decode_attn.
  * Slots (pst_timer_kernel_name):
  *   0 "pac_tc"        tensor-core PAC that rounds P once to bf16 (every

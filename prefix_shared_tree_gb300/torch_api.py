@@ -85,7 +85,8 @@ class TreeDecodeAttention:
     def capture(self, Q, K_pool, V_pool, O, LSE):
         """One decode step captured as a CUDA graph (torch.cuda.CUDAGraph) on
         these tensors: replaying it reruns every launch of pst_decode_attn
-        (the PAC launch groups on their forked streams, the join, POR) with
+        (the chained PAC launch groups and POR, or with side_streams the
+        groups on their forked streams and the join) with
         no host work per step. The plan, its workspace and the tensors must
         stay alive and in place while the graph is used; a new plan needs a
         new capture. One ordinary call first sets up the kernels and the
