@@ -419,6 +419,8 @@ def measure(name, args, dev, steps, warmup, timer_steps, plan_opts, e2e=False, w
         "plan": {"plan_us": round(st["plan_us"], 1), "plan_wall_us": round(plan_wall_us, 1),
                  "plan_update_us": round(update_us, 1),
                  "predicted_makespan_us": round(st["predicted_makespan_us"], 2),
+                 "split_policy": {0: "cost_model", 1: "none", 2: "uniform", 3: "flatten"}[int(st["split_policy"])],
+                 "fixed_chunk": int(st["fixed_chunk"]),
                  "n_chunks": st["n_chunks"], "n_items": st["n_items"], "n_tc_items": st["n_tc_items"],
                  "n_cc_items": st["n_cc_items"], "n_partial_rows": st["n_partial_rows"]},
         "n_launches": int(st["n_launches"]),
@@ -466,7 +468,7 @@ def _config_entry(m):
                             "group_end_us": m["dom_us"], "achieved_gbs": round(m["dom_achieved"], 1),
                             "frac": round(m["dom_achieved"] / peak, 4)},
         "group_end_us": m["group_end_us"], "por_us": m["por_us"], "n_launches": m["n_launches"],
-        "plan_us": m["plan"]["plan_us"], "sm_mhz": m["clocks"].get("sm_mhz"),
+        "plan_us": m["plan"]["plan_us"], "split_policy": m["plan"]["split_policy"], "sm_mhz": m["clocks"].get("sm_mhz"),
     }
 
 

@@ -53,12 +53,21 @@ typedef enum { PST_BF16 = 0, PST_F32 = 1 } pst_dtype;
 typedef enum {
     PST_SPLIT_COST_MODEL = 0, /* binary search on the max-block cost + greedy b_k  */
     PST_SPLIT_NONE       = 1, /* b_k = 1: one chunk per node (DEFT-Node)            */
-    PST_SPLIT_UNIFORM    = 2  /* every node cut into chunks of `fixed_chunk` tokens */
+    PST_SPLIT_UNIFORM    = 2, /* every node cut into chunks of `fixed_chunk` tokens */
+    PST_SPLIT_FLATTEN    = 3  /* DEFT-Flatten (DEFT A.9): the tokens of every node a
+                                 query sees, in depth-first order, cut into chunks
+                                 of at most `fixed_chunk` (1..64, default 64)
+                                 tokens that cross node boundaries; a chunk also
+                                 ends where its tokens stop being consecutive page
+                                 rows. Each chunk is one task with the union of its
+                                 nodes' queries and a 64-bit bit causal mask per
+                                 query (bit j: chunk token j is on its path).    */
 } pst_split_policy;
 
 typedef struct {
     int32_t split_policy;   /* pst_split_policy; default PST_SPLIT_COST_MODEL          */
-    int32_t fixed_chunk;    /* tokens per chunk for PST_SPLIT_UNIFORM (multiple of 64)  */
+    int32_t fixed_chunk;    /* tokens per chunk for PST_SPLIT_UNIFORM (multiple of 64);
+                               at most this many per chunk for PST_SPLIT_FLATTEN    */
     int32_t tc_min_rows;    /* rows (queries x GQA group) from which a node runs on the
                                tensor-core PAC; default 16; fp32 inputs never do      */
     int32_t pack_masks;     /* 1 (default): pack a page-contiguous subtree of <= 64
@@ -99,6 +108,13 @@ typedef struct {
                                pst_decode_attn_timed always uses 1; the
                                no-allocation entry point runs the groups one
                                after the other with 1.                        */
+    int32_t flatten_candidates; /* PST_SPLIT_COST_MODEL only. 0 (default): also
+                               score DEFT-Flatten chunkings (PST_SPLIT_FLATTEN)
+                               of 1024 and 2048 tokens with the same cost model
+                               and keep one whose predicted makespan is at
+                               least 3 % below the node partition's (the plan's
+                               policy then reads PST_SPLIT_FLATTEN); -1: the
+                               node partition only.                           */
 } pst_plan_opts;
 
 /* Fill `o` with the defaults above. */
@@ -313,6 +329,9 @@ typedef struct {
     int64_t workspace_bytes;
     int32_t num_slots;            /* m: concurrent PAC blocks the schedule assumes    */
     int32_t n_launches;           /* kernels per pst_decode_attn                      */
+    int32_t split_policy;         /* the plan's pst_split_policy (after the choice
+                                     between node partition and DEFT-Flatten)      */
+    int32_t fixed_chunk;          /* its fixed_chunk (S_t for PST_SPLIT_FLATTEN)     */
 } pst_plan_stats;
 int pst_plan_stats_get(const pst_plan* p, pst_plan_stats* s);
 

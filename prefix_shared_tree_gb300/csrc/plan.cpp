@@ -193,6 +193,7 @@ extern "C" void pst_plan_opts_default(pst_plan_opts* o) {
     o->thin_engine = 0;
     o->debug_stall = 0;
     o->side_streams = 0;
+    o->flatten_candidates = 0;
 }
 
 namespace {
@@ -559,6 +560,9 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
     if (o.p_bf16_min_tokens == 0) o.p_bf16_min_tokens = kPBf16MinTokens;
     if (o.split_policy == PST_SPLIT_UNIFORM && (o.fixed_chunk <= 0 || o.fixed_chunk % kTileTokens))
         return fail(PST_EINVAL, "plan_create: fixed_chunk must be a positive multiple of 64");
+    if (o.split_policy == PST_SPLIT_FLATTEN && o.fixed_chunk <= 0) o.fixed_chunk = kMaskTokens;
+    if (o.split_policy < PST_SPLIT_COST_MODEL || o.split_policy > PST_SPLIT_FLATTEN)
+        return fail(PST_EINVAL, "plan_create: unknown split policy");
 
     pst_plan* P = new (std::nothrow) pst_plan();
     if (!P) return fail(PST_ENOMEM, "plan_create: out of memory");
@@ -606,9 +610,88 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
     }
     auto nq_of = [&](int32_t n) { return P->nodeq_ptr[n + 1] - P->nodeq_ptr[n]; };
 
+    // A packed chunk's queries (the union of the query lists of `nodes`) and
+    // the bit causal mask of each: bit j set iff chunk token j's node is on
+    // the query's path (DEFT, section 3.3 and A.9).
+    auto set_queries_and_masks = [&](PackedGroup& g, const std::vector<int32_t>& nodes, bool with_masks) {
+        std::vector<int32_t> qs;
+        for (int32_t n : nodes)
+            qs.insert(qs.end(), P->nodeq.begin() + P->nodeq_ptr[n], P->nodeq.begin() + P->nodeq_ptr[n + 1]);
+        std::sort(qs.begin(), qs.end());
+        qs.erase(std::unique(qs.begin(), qs.end()), qs.end());
+        g.queries = qs;
+        g.mask.clear();
+        if (!with_masks) return;
+        g.mask.assign(qs.size(), 0);
+        for (size_t qi = 0; qi < qs.size(); ++qi) {
+            const int32_t q = qs[qi];
+            uint64_t m = 0;
+            for (size_t j = 0; j < g.tok_node.size(); ++j) {
+                bool on = false;
+                for (int32_t k = P->qpath_ptr[q]; k < P->qpath_ptr[q + 1]; ++k)
+                    if (P->qpath_node[k] == g.tok_node[j]) { on = true; break; }
+                if (on) m |= (uint64_t)1 << j;
+            }
+            g.mask[qi] = m;
+        }
+    };
+
     // ---- packing: a page-contiguous set of descendants of <= 64 tokens
     std::vector<int32_t> packed_in(N, -1);
-    if (o.pack_masks) {
+    if (o.split_policy == PST_SPLIT_FLATTEN) {
+        // DEFT-Flatten: walk the nodes some query sees in depth-first order
+        // and cut their tokens into runs of at most fixed_chunk (S_t); a run
+        // that mixes nodes needs a mask bit per token, so it holds at most 64;
+        // a run also ends where the next token is not the next page row (the
+        // kernels read a chunk as consecutive rows of its page list). A run
+        // inside one node needs no mask: all of the node's queries see all of
+        // its tokens.
+        const int32_t ps = T.page_size;
+        PackedGroup cur;
+        int32_t cur_page = -1, cur_row = -1;
+        auto flush = [&]() {
+            if (cur.tok_node.empty()) return;
+            cur.root = -1;
+            cur.nodes.clear();   // the run's nodes, in walk order (each node's tokens are consecutive)
+            for (int32_t n : cur.tok_node)
+                if (cur.nodes.empty() || cur.nodes.back() != n) cur.nodes.push_back(n);
+            // one node: every query sees every token, no mask (and the run may
+            // be longer than the 64 bits of one)
+            set_queries_and_masks(cur, cur.nodes, cur.nodes.size() > 1);
+            const int32_t gid = (int32_t)P->groups.size();
+            for (int32_t n : cur.tok_node) packed_in[n] = gid;   // every flattened node is in some run
+            P->groups.push_back(std::move(cur));
+            cur = PackedGroup();
+        };
+        for (int i = 0; i < N; ++i) {
+            const int32_t n = T.preorder[i];
+            if (T.len[n] == 0 || nq_of(n) == 0) continue;
+            for (int32_t t = 0; t < T.len[n]; ++t) {
+                const int64_t pos = (int64_t)T.first_offset[n] + t;
+                const int32_t page = T.page_ids[T.page_ptr[n] + pos / ps];
+                const int32_t row = (int32_t)(pos % ps);
+                const int32_t held = (int32_t)cur.tok_node.size();
+                const bool next_row = held > 0 &&
+                                      ((page == cur_page && row == cur_row + 1) || (cur_row == ps - 1 && row == 0));
+                // joining this token to the run would make it mix nodes (the
+                // walk visits each node's tokens in one stretch)
+                const bool mixes = held > 0 && cur.tok_node.front() != n;
+                const int32_t limit = mixes ? std::min(o.fixed_chunk, kMaskTokens) : o.fixed_chunk;
+                if (held > 0 && (!next_row || held >= limit)) flush();
+                if (cur.tok_node.empty()) {
+                    cur.page_list.assign(1, page);
+                    cur.pos_begin = row;
+                } else if (page != cur_page) {
+                    cur.page_list.push_back(page);
+                }
+                cur.tok_node.push_back(n);
+                cur.tok_t.push_back(t);
+                cur_page = page;
+                cur_row = row;
+            }
+        }
+        flush();
+    } else if (o.pack_masks) {
         // subtree token totals (excluding the node itself) via reverse preorder
         std::vector<int64_t> sub_tok(N, 0), sub_cnt(N, 0);
         for (int i = N - 1; i >= 0; --i) {
@@ -632,29 +715,8 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
             }
             PackedGroup g;
             if (!build_packed_group(T, p, desc, &g)) continue;
-            // queries: union of the packed nodes' query lists
-            std::vector<int32_t> qs;
-            for (int32_t n : desc)
-                qs.insert(qs.end(), P->nodeq.begin() + P->nodeq_ptr[n], P->nodeq.begin() + P->nodeq_ptr[n + 1]);
-            std::sort(qs.begin(), qs.end());
-            qs.erase(std::unique(qs.begin(), qs.end()), qs.end());
-            if (qs.empty()) continue;
-            std::vector<int32_t> pos_of_node(0);
-            g.queries = qs;
-            g.mask.assign(qs.size(), 0);
-            for (size_t qi = 0; qi < qs.size(); ++qi) {
-                const int32_t q = qs[qi];
-                uint64_t m = 0;
-                for (size_t j = 0; j < g.tok_node.size(); ++j) {
-                    const int32_t n = g.tok_node[j];
-                    // visible iff n is on the query's path
-                    bool on = false;
-                    for (int32_t k = P->qpath_ptr[q]; k < P->qpath_ptr[q + 1]; ++k)
-                        if (P->qpath_node[k] == n) { on = true; break; }
-                    if (on) m |= (uint64_t)1 << j;
-                }
-                g.mask[qi] = m;
-            }
+            set_queries_and_masks(g, desc, true);
+            if (g.queries.empty()) continue;
             const int32_t gid = (int32_t)P->groups.size();
             for (int32_t n : desc) packed_in[n] = gid;
             P->groups.push_back(std::move(g));
@@ -786,7 +848,7 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
             c.dev.n_tok = t.n_tok;
             c.dev.q_base = (int32_t)P->chunk_q.size();
             c.dev.n_q = t.n_q;
-            c.dev.mask_base = (int32_t)P->masks.size();
+            c.dev.mask_base = g.mask.empty() ? -1 : (int32_t)P->masks.size();
             c.dev.r_tile = pl.rows_per_block(t);
             P->chunk_q.insert(P->chunk_q.end(), g.queries.begin(), g.queries.end());
             P->masks.insert(P->masks.end(), g.mask.begin(), g.mask.end());
@@ -897,10 +959,40 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
     return PST_OK;
 }
 
+// CoDec keeps the candidate partition its cost model scores best; the
+// cost-model policy also scores DEFT-Flatten chunkings (DEFT A.9) of these
+// sizes and takes one only when its predicted makespan is lower by the margin:
+// measured on GB300, the model ranks node partitions and flattened plans in
+// the right order, but its error is larger on flattened plans.
+static constexpr int32_t kFlattenCandidates[] = {1024, 2048};
+static constexpr double kFlattenMargin = 0.97;
+
 extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const int32_t* query_node,
                                int32_t n_q_heads, int32_t n_kv_heads, int32_t d, pst_dtype dtype,
                                const pst_plan_opts* opts, pst_plan** out) {
-    return plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, opts, nullptr, nullptr, out);
+    const auto t0 = std::chrono::steady_clock::now();
+    int rc = plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, opts, nullptr, nullptr, out);
+    if (rc != PST_OK) return rc;
+    pst_plan* best = *out;
+    if (best->opts.split_policy != PST_SPLIT_COST_MODEL || best->opts.flatten_candidates < 0) return rc;
+    for (int32_t st : kFlattenCandidates) {
+        pst_plan_opts fo = (*out)->opts;
+        fo.split_policy = PST_SPLIT_FLATTEN;
+        fo.fixed_chunk = st;
+        pst_plan* alt = nullptr;
+        if (plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, &fo, nullptr, nullptr, &alt) !=
+            PST_OK)
+            continue;
+        const double ref = (*out)->makespan_us;   // the node partition's
+        if (alt->makespan_us < kFlattenMargin * ref && alt->makespan_us < best->makespan_us) std::swap(best, alt);
+        if (alt != *out) pst_plan_destroy(alt);
+    }
+    if (best != *out) {
+        pst_plan_destroy(*out);
+        *out = best;
+    }
+    best->plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
+    return PST_OK;
 }
 
 extern "C" int pst_plan_update(const pst_plan* prev, const pst_tree* tree, pst_plan** out) {
@@ -966,6 +1058,8 @@ extern "C" int pst_plan_stats_get(const pst_plan* p, pst_plan_stats* s) {
     s->n_launches = 1;
     for (int g = 0; g < 4; ++g) s->n_launches += p->tc_group_cnt[g] > 0;
     for (int k = 0; k < 4; ++k) s->n_launches += p->cc_class_cnt[k] > 0;
+    s->split_policy = p->opts.split_policy;
+    s->fixed_chunk = p->opts.fixed_chunk;
     return PST_OK;
 }
 

@@ -20,7 +20,7 @@ PST_OK = 0
 ERRORS = {-1: "PST_EINVAL", -2: "PST_ECYCLE", -3: "PST_ERANGE", -4: "PST_EUNSUPPORTED",
           -5: "PST_EWORKSPACE", -6: "PST_ECUDA", -7: "PST_EDEVICE", -8: "PST_ENOMEM"}
 DTYPES = {"bf16": 0, "f32": 1}
-SPLIT = {"cost_model": 0, "none": 1, "uniform": 2}
+SPLIT = {"cost_model": 0, "none": 1, "uniform": 2, "flatten": 3}
 KERNEL_SLOTS = 4
 
 
@@ -34,7 +34,8 @@ class PlanOpts(C.Structure):
     _fields_ = [("split_policy", C.c_int32), ("fixed_chunk", C.c_int32), ("tc_min_rows", C.c_int32),
                 ("pack_masks", C.c_int32), ("num_sms", C.c_int32), ("slots_per_sm", C.c_int32),
                 ("tc_engine", C.c_int32), ("tc_block_rows", C.c_int32), ("p_bf16_min_tokens", C.c_int32),
-                ("thin_engine", C.c_int32), ("debug_stall", C.c_int32), ("side_streams", C.c_int32)]
+                ("thin_engine", C.c_int32), ("debug_stall", C.c_int32), ("side_streams", C.c_int32),
+                ("flatten_candidates", C.c_int32)]
 
 
 class PlanStats(C.Structure):
@@ -42,7 +43,8 @@ class PlanStats(C.Structure):
                 ("cost_lower_bound_us", C.c_double), ("n_chunks", C.c_int64), ("n_items", C.c_int64),
                 ("n_tc_items", C.c_int64), ("n_cc_items", C.c_int64), ("n_partial_rows", C.c_int64),
                 ("unique_kv_tokens", C.c_int64), ("kv_tokens_read", C.c_int64),
-                ("workspace_bytes", C.c_int64), ("num_slots", C.c_int32), ("n_launches", C.c_int32)]
+                ("workspace_bytes", C.c_int64), ("num_slots", C.c_int32), ("n_launches", C.c_int32),
+                ("split_policy", C.c_int32), ("fixed_chunk", C.c_int32)]
 
 
 class ExportSizes(C.Structure):
@@ -213,7 +215,7 @@ def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int,
                 tc_min_rows: int | None = None, pack_masks: bool | None = None, num_sms: int = 0,
                 slots_per_sm: int = 0, tc_engine: str = "tcgen05", tc_block_rows: int = 256,
                 p_bf16_min_tokens: int = 0, thin_engine: str = "tcgen05", debug_stall: bool = False,
-                side_streams: bool = False) -> Plan:
+                side_streams: bool = False, flatten_candidates: bool = True) -> Plan:
     o = plan_opts_default()
     o.split_policy = SPLIT[split_policy]
     if fixed_chunk is not None:
@@ -230,6 +232,7 @@ def plan_create(tree: Tree, query_node, n_q_heads: int, n_kv_heads: int, d: int,
     o.thin_engine = {"tcgen05": 0, "cuda_core": 1}[thin_engine]
     o.debug_stall = int(bool(debug_stall))
     o.side_streams = int(bool(side_streams))
+    o.flatten_candidates = 0 if flatten_candidates else -1
     qn, qnp = _arr(query_node, np.int32)
     h = C.c_void_p()
     _check(lib().pst_plan_create(tree._h, len(qn), qnp, n_q_heads, n_kv_heads, d, DTYPES[dtype],

@@ -129,12 +129,15 @@ def _visible_pairs(wl):
     return np.sort(np.concatenate(codes))
 
 
-@pytest.mark.parametrize("policy", ["cost_model", "none", "uniform"])
+_POLICIES = {"cost_model": {}, "none": {}, "uniform": {"fixed_chunk": 128}, "flatten": {},
+             "flatten16": {"split_policy": "flatten", "fixed_chunk": 16},
+             "flatten300": {"split_policy": "flatten", "fixed_chunk": 300}}
+
+
+@pytest.mark.parametrize("policy", list(_POLICIES))
 @pytest.mark.parametrize("wl", _workloads(), ids=lambda w: w.name)
 def test_plan_covers_each_pair_exactly_once(lib, wl, policy):
-    kw = {"split_policy": policy}
-    if policy == "uniform":
-        kw["fixed_chunk"] = 128
+    kw = {"split_policy": policy, **_POLICIES[policy]}
     e = _plan(lib, wl, **kw).export()
     got = _covered_pairs(wl, e)
     want = _visible_pairs(wl)
@@ -147,6 +150,63 @@ def test_plan_covers_each_pair_exactly_once(lib, wl, policy):
         n_chunks_with_q = sum(q in set(e["chunk_q"][e["chunk_q_ptr"][c]:e["chunk_q_ptr"][c + 1]].tolist())
                               for c in range(len(e["chunk_q_ptr"]) - 1))
         assert len(rows) == n_chunks_with_q
+
+
+def _chunks(e):
+    """Per chunk: (tokens as (node, t) pairs, queries, masks)."""
+    out = []
+    for c in range(len(e["chunk_q_ptr"]) - 1):
+        a, b = e["chunk_tok_ptr"][c], e["chunk_tok_ptr"][c + 1]
+        qa, qb = e["chunk_q_ptr"][c], e["chunk_q_ptr"][c + 1]
+        out.append((list(zip(e["chunk_tok_node"][a:b].tolist(), e["chunk_tok_t"][a:b].tolist())),
+                    e["chunk_q"][qa:qb].tolist(), [int(m) for m in e["chunk_q_mask"][qa:qb]]))
+    return out
+
+
+def test_deft_flatten_chunks_of_a_hand_laid_tree(lib):
+    """DEFT-Flatten (DEFT, A.9) on a tree whose page layout is written out:
+    root 40 tokens in pages 0, 1, 2 (rows 0-7 of page 2); child 1 (20 tokens)
+    continues in page 2 at row 8 and ends in page 3; child 2 (20 tokens)
+    starts a fresh page 4. Query 0 sits on child 1, query 1 on child 2.
+    Depth-first, the root and child 1 are consecutive page rows and child 2
+    is not, so with S_t = 64 the chunks are [root + child 1] (60 tokens,
+    masked: query 1 sees only the root's 40) and [child 2]; with S_t = 32 the
+    root's first 32 tokens form a chunk of their own (one node: no mask),
+    then [root tokens 32-39 + child 1] (28 tokens, query 1 sees 8) and
+    [child 2]."""
+    all_ones = 2**64 - 1
+    tree = lib.tree_build([40, 20, 20], [-1, 0, 0], [0, 3, 5, 7], [0, 1, 2, 2, 3, 4, 5], first_offset=[0, 8, 0],
+                          page_size=16, num_pages=6)
+    def plan(st):
+        return _chunks(lib.plan_create(tree, [1, 2], 8, 2, 128, "bf16", num_sms=152, split_policy="flatten",
+                                       fixed_chunk=st).export())
+    root = [(0, t) for t in range(40)]
+    c1 = [(1, t) for t in range(20)]
+    c2 = [(2, t) for t in range(20)]
+    assert plan(64) == [(root + c1, [0, 1], [(1 << 60) - 1, (1 << 40) - 1]), (c2, [1], [all_ones])]
+    assert plan(32) == [(root[:32], [0, 1], [all_ones, all_ones]),
+                        (root[32:] + c1, [0, 1], [(1 << 28) - 1, (1 << 8) - 1]),
+                        (c2, [1], [all_ones])]
+
+
+def test_cost_model_scores_flatten_candidates(lib):
+    """The cost-model policy also scores DEFT-Flatten chunkings and keeps one
+    only when its predicted makespan is at least 3 % lower: on the
+    tree-of-thought GQA tree (many small nodes) it does; on document QA it
+    keeps the node partition; switched off, the node partition stays."""
+    tot = synth.tree_of_thought("gqa")
+    s_on = _plan(lib, tot).stats()
+    s_off = _plan(lib, tot, flatten_candidates=False).stats()
+    assert s_off["split_policy"] == 0
+    assert s_on["split_policy"] == 3 and s_on["fixed_chunk"] in (1024, 2048)
+    assert s_on["predicted_makespan_us"] < 0.97 * s_off["predicted_makespan_us"]
+    flat = _plan(lib, tot, split_policy="flatten", fixed_chunk=s_on["fixed_chunk"]).stats()
+    assert flat["predicted_makespan_us"] == s_on["predicted_makespan_us"]
+    dqa = synth.document_qa()
+    assert _plan(lib, dqa).stats()["split_policy"] == 0
+    for wl in (synth.few_shot(), synth.speculative(), dqa):
+        on, off = _plan(lib, wl).stats(), _plan(lib, wl, flatten_candidates=False).stats()
+        assert on["predicted_makespan_us"] <= off["predicted_makespan_us"]
 
 
 def test_speculative_drafts_are_packed_with_masks(lib):

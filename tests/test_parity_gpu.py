@@ -88,9 +88,10 @@ def test_random_trees(lib, seed, heads, d, dtype):
 @pytest.mark.parametrize("opts", [dict(tc_min_rows=1), dict(split_policy="uniform", fixed_chunk=64),
                                   dict(split_policy="none"), dict(pack_masks=False),
                                   dict(tc_min_rows=1, tc_engine="mma_sync"), dict(thin_engine="cuda_core"),
-                                  dict(tc_min_rows=17, split_policy="uniform", fixed_chunk=128)],
+                                  dict(tc_min_rows=17, split_policy="uniform", fixed_chunk=128),
+                                  dict(split_policy="flatten"), dict(split_policy="flatten", fixed_chunk=200)],
                          ids=["all_tensor_core", "uniform64", "no_split", "no_masks", "mma_sync", "cuda_core_thin",
-                              "thin_uniform128"])
+                              "thin_uniform128", "flatten64", "flatten200"])
 def test_random_trees_plan_variants(lib, seed, opts):
     wl = synth.random_tree(8000 + seed, max_nodes=12, max_len=300, heads=(8, 2), d=128, dtype="bf16",
                            n_queries=24)
@@ -256,13 +257,22 @@ def test_few_shot_full(lib):
     assert st["n_tc_items"] > 0 and st["n_cc_items"] > 0
 
 
-@pytest.mark.parametrize("name", ["document_qa", "speculative", "tree_of_thought_gqa", "tree_of_thought_mqa",
-                                  "tree_of_thought_mha"])
-def test_full_size_every_query(lib, name):
-    """The full-size workloads with the default plan, every query and head
+_FLATTEN = {"split_policy": "flatten"}
+
+
+@pytest.mark.parametrize("name,opts", [
+    ("document_qa", {}), ("speculative", {}), ("speculative", _FLATTEN),
+    ("speculative", dict(_FLATTEN, fixed_chunk=1024)), ("tree_of_thought_gqa", {}),
+    ("tree_of_thought_gqa", dict(_FLATTEN, fixed_chunk=256)), ("tree_of_thought_mqa", {}),
+    ("tree_of_thought_mha", {})],
+    ids=["document_qa", "speculative", "speculative-flatten64", "speculative-flatten1024", "tree_of_thought_gqa",
+         "tree_of_thought_gqa-flatten256", "tree_of_thought_mqa", "tree_of_thought_mha"])
+def test_full_size_every_query(lib, name, opts):
+    """The full-size workloads with the default plan (and DEFT-Flatten
+    chunking for the trees of many small nodes), every query and head
     compared with the oracle."""
     wl, K, V, Q, ref = full_size(name)
-    O, L, _, att = run_gpu(lib, wl, pools=(K, V), Q=Q)
+    O, L, _, att = run_gpu(lib, wl, pools=(K, V), Q=Q, **opts)
     assert np.all(np.isfinite(O)) and np.all(np.isfinite(L))
     assert_matches(wl, O, L, K, V, Q, ref=ref)
 
