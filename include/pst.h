@@ -314,6 +314,31 @@ int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const void* K_pool
  * *code (nullable) receives the raw word. Allocates nothing. */
 int pst_noalloc_check_status(void* stream, int32_t* code);
 
+/* ---------------------------------------------------------------- MLA
+ * Multi-head latent attention: rebuild the per-head K/V blocks of the tree's
+ * pages from a latent KV cache, after which pst_decode_attn runs the same
+ * prefix-aware pipeline on them (CoDec "supplementary details", the kernel
+ * module paragraph on MLA models). Every token j has a latent c_j of d_c
+ * channels; kv head h has up-projections W_UK[h], W_UV[h] (d x d_c):
+ *   K_pool[page][h][row][:] = bf16( W_UK[h] c_j ),  V likewise with W_UV,
+ * accumulated in fp32 on the tensor cores and rounded once to bf16. Each page
+ * some node of the plan's tree uses is rebuilt once (all its rows), however
+ * many queries share it; other pages of K_pool / V_pool are left as they are.
+ *
+ *   C_pool  device bf16 [num_pages][page_size][d_c], the tree's page ids
+ *   d_c     128, 256, 384 or 512
+ *   W_uk    device bf16 [Hkv][d][d_c] (row e of head h: the weights of output
+ *           channel e), W_uv likewise
+ *   K_pool, V_pool  device bf16 [num_pages][Hkv][page_size][d] (caller-owned
+ *           scratch in the layout pst_decode_attn reads)
+ * All pointers 16-byte aligned. Requires a bf16 plan with page size 16 and a
+ * prior pst_plan_upload (the page list lives in the workspace). Asynchronous
+ * on `stream`; the kernel's bounded waits report through
+ * pst_plan_check_status. Errors: PST_EINVAL, PST_EUNSUPPORTED (dtype, d_c,
+ * page size), PST_EWORKSPACE (no upload), PST_ECUDA. */
+int pst_mla_reconstruct(const pst_plan* p, const void* C_pool, int32_t d_c, const void* W_uk, const void* W_uv,
+                        void* K_pool, void* V_pool, void* stream);
+
 /* ---------------------------------------------------------------- introspection */
 typedef struct {
     double  plan_us;              /* host time of pst_plan_create                    */

@@ -220,6 +220,27 @@ static int make_pool_map(const pst_plan* p, const void* pool, unsigned char* out
 // workspace (same layout, base `ws`).
 int encode_pool_map(const pst_plan* p, const void* pool, unsigned char* out) { return make_pool_map(p, pool, out); }
 
+// A bf16 tensor map with 128-byte swizzle for the library's other launchers:
+// `rank` dims (innermost first), strides in bytes of dims 1.., box extents.
+int encode_bf16_map(void* out, int rank, const void* base, const uint64_t* dims, const uint64_t* strides,
+                    const uint32_t* box) {
+    auto fn = encode_fn();
+    if (!fn) return fail(PST_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], e[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        e[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
+    CUresult r = fn(reinterpret_cast<CUtensorMap*>(out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base),
+                    d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PST_ECUDA, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return PST_OK;
+}
+
 DevPlan dev_plan_at(const pst_plan* p, void* ws) {
     uint8_t* b = static_cast<uint8_t*>(ws);
     DevPlan d;

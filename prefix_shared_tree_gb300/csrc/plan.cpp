@@ -936,6 +936,10 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
     W.masks = off; off = align256(off + (int64_t)P->masks.size() * 8);
     W.merge_ptr = off; off = align256(off + (int64_t)P->merge_ptr.size() * 4);
     W.merge_row = off; off = align256(off + (int64_t)P->merge_row.size() * 4);
+    P->tree_pages.assign(T.page_ids.begin(), T.page_ids.end());
+    std::sort(P->tree_pages.begin(), P->tree_pages.end());
+    P->tree_pages.erase(std::unique(P->tree_pages.begin(), P->tree_pages.end()), P->tree_pages.end());
+    W.tree_pages = off; off = align256(off + (int64_t)P->tree_pages.size() * 4);
     W.meta_end = off;
     W.part_o = off; off = align256(off + part_rows * d * 4);
     W.part_lse = off; off = align256(off + part_rows * 4);
@@ -953,6 +957,7 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
     put(W.masks, P->masks.data(), P->masks.size() * 8);
     put(W.merge_ptr, P->merge_ptr.data(), P->merge_ptr.size() * 4);
     put(W.merge_row, P->merge_row.data(), P->merge_row.size() * 4);
+    put(W.tree_pages, P->tree_pages.data(), P->tree_pages.size() * 4);
 
     P->plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t_start).count();
     *out = guard.release();

@@ -67,6 +67,7 @@ struct WsLayout {
     int64_t masks = 0;
     int64_t merge_ptr = 0;
     int64_t merge_row = 0;
+    int64_t tree_pages = 0;  // int32: every page some node uses, once (the MLA rebuild's work list)
     int64_t meta_end = 0;    // metadata [status, meta_end) is uploaded once
     int64_t part_o = 0;      // fp32 [n_part_rows][d]
     int64_t part_lse = 0;    // fp32 [n_part_rows] (log2 domain)
@@ -175,6 +176,7 @@ struct pst_plan {
     std::vector<int32_t> chunk_q;
     std::vector<uint64_t> masks;
     std::vector<int32_t> merge_ptr, merge_row;
+    std::vector<int32_t> tree_pages;   // ascending ids of the pages the tree's nodes use
     std::vector<pst::DevItem> items;   // tensor-core items first, then CUDA-core
     int64_t n_tc_items = 0, n_cc_items = 0;
     // Tensor-core items come in four launch groups, in this order: P rounded

@@ -92,6 +92,7 @@ def lib() -> C.CDLL:
         "pst_decode_attn": (C.c_int, [vp, vp, vp, vp, vp, vp, vp]),
         "pst_decode_attn_noalloc": (C.c_int, [vp, vp, vp, vp, vp, vp, vp]),
         "pst_noalloc_check_status": (C.c_int, [vp, C.POINTER(i32)]),
+        "pst_mla_reconstruct": (C.c_int, [vp, vp, i32, vp, vp, vp, vp, vp]),
         "pst_plan_check_status": (C.c_int, [vp, vp, C.POINTER(i32)]),
         "pst_timer_create": (C.c_int, [i32, C.POINTER(vp)]),
         "pst_timer_destroy": (None, [vp]),
@@ -333,6 +334,14 @@ def list_schedule(costs, m: int):
     mk = C.c_double(0.0)
     _check(lib().pst_list_schedule(n, cp, int(m), slot.ctypes.data_as(C.c_void_p), C.byref(mk)))
     return slot[:n], float(mk.value)
+
+
+def mla_reconstruct(plan: Plan, c_pool: int, d_c: int, w_uk: int, w_uv: int, k_pool: int, v_pool: int,
+                    stream: int = 0):
+    """Rebuild the per-head K/V pools of the plan's tree pages from a latent
+    pool (multi-head latent attention); device pointers."""
+    _check(lib().pst_mla_reconstruct(plan._h, C.c_void_p(c_pool), int(d_c), C.c_void_p(w_uk), C.c_void_p(w_uv),
+                                     C.c_void_p(k_pool), C.c_void_p(v_pool), C.c_void_p(stream)))
 
 
 def noalloc_check_status(stream: int = 0) -> int:

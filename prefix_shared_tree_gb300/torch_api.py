@@ -127,6 +127,31 @@ class TreeDecodeAttention:
                                   O.data_ptr(), LSE.data_ptr(), st, timer)
         return O, LSE
 
+    def mla_reconstruct(self, C_pool, W_uk, W_uv, K_pool=None, V_pool=None, stream=None):
+        """Multi-head latent attention: rebuild the per-head K/V pools of the
+        tree's pages from the latent pool C_pool [num_pages][page_size][d_c]
+        with up-projections W_uk, W_uv [Hkv][d][d_c] (bf16), into K_pool /
+        V_pool (allocated when not given); then call this object on them."""
+        td = torch.bfloat16
+        for name, t in (("C_pool", C_pool), ("W_uk", W_uk), ("W_uv", W_uv)):
+            if t.dtype != td or t.device != self.device or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous bf16 tensor on {self.device}")
+        d_c = C_pool.shape[-1]
+        if tuple(C_pool.shape) != (self.num_pages, self.page_size, d_c):
+            raise ValueError(f"C_pool shape {tuple(C_pool.shape)}")
+        want_w = (self.n_kv_heads, self.d, d_c)
+        if tuple(W_uk.shape) != want_w or tuple(W_uv.shape) != want_w:
+            raise ValueError(f"W_uk / W_uv shape must be {want_w}")
+        shape = (self.num_pages, self.n_kv_heads, self.page_size, self.d)
+        if K_pool is None:
+            K_pool = torch.empty(shape, dtype=td, device=self.device)
+        if V_pool is None:
+            V_pool = torch.empty(shape, dtype=td, device=self.device)
+        st = (stream or torch.cuda.current_stream(self.device)).cuda_stream
+        pst.mla_reconstruct(self.plan, C_pool.data_ptr(), d_c, W_uk.data_ptr(), W_uv.data_ptr(), K_pool.data_ptr(),
+                            V_pool.data_ptr(), st)
+        return K_pool, V_pool
+
     def check_status(self, stream=None) -> int:
         st = (stream or torch.cuda.current_stream(self.device)).cuda_stream
         return self.plan.check_status(st)

@@ -127,6 +127,34 @@ class Workload:
         rng.parallel_fill(P, fill, workers=workers, min_chunk=16)
         return K, V
 
+    def mla_inputs(self, d_c: int = 512, workers: int | None = None):
+        """Latent KV inputs (multi-head latent attention), bf16 bits:
+        C_pool [P, page, d_c] with N(0, 1) latents per logical token (junk in
+        rows no node covers), and up-projections W_uk, W_uv [Hkv, d, d_c]
+        drawn N(0, 1/d_c), so the rebuilt K and V are about N(0, 1)."""
+        P, S, H, D = self.num_pages, self.page_size, self.n_kv_heads, self.d
+        C = np.empty((P, S, d_c), dtype=np.uint16)
+        lids = self.row_lids().reshape(P, S)
+        kc = rng.stream_key(self.seed, 15, d_c)
+        kj = rng.stream_key(self.seed, 16, d_c)
+        cc = np.arange(d_c, dtype=np.uint64)[None, None, :]
+
+        def fill(p0, p1):
+            lid = lids[p0:p1]
+            used = (lid >= 0)[:, :, None]
+            l64 = np.where(lid >= 0, lid, 0).astype(np.uint64)[:, :, None]
+            pr = np.arange(p0, p1, dtype=np.uint64)[:, None, None]
+            rr = np.arange(S, dtype=np.uint64)[None, :, None]
+            val = rng.normal_at(kc, l64 * np.uint64(d_c) + cc)
+            junk = JUNK_SCALE * rng.normal_at(kj, (pr * np.uint64(S) + rr) * np.uint64(d_c) + cc)
+            C[p0:p1] = rng.round_to_bf16_bits(np.where(used, val, junk))
+
+        rng.parallel_fill(P, fill, workers=workers, min_chunk=16)
+        scale = 1.0 / np.sqrt(d_c)
+        W = [rng.round_to_bf16_bits(scale * rng.normal(rng.stream_key(self.seed, tag, H, D, d_c), 0, H * D * d_c))
+             .reshape(H, D, d_c) for tag in (17, 18)]
+        return C, W[0], W[1]
+
     def q(self) -> np.ndarray:
         B, H, D = self.n_queries, self.n_q_heads, self.d
         x = rng.normal(self.key_q, 0, B * H * D).reshape(B, H, D)
@@ -221,15 +249,16 @@ def tiny_two_level(seed: int | None = None) -> Workload:
 
 
 def document_qa(seed: int | None = None, prefix: int = 32768, n_req: int = 64,
-                suffix_lo: int = 64, suffix_hi: int = 512) -> Workload:
+                suffix_lo: int = 64, suffix_hi: int = 512, heads: tuple = (32, 8)) -> Workload:
     """One shared prefix of 32K tokens and 64 requests with unique suffixes of
-    U{64..512} tokens, one query per request; 32 Q / 8 KV heads, d=128, bf16."""
+    U{64..512} tokens, one query per request; 32 Q / 8 KV heads (`heads`),
+    d=128, bf16."""
     seed = config_seed(2) if seed is None else seed
     key = rng.stream_key(seed, 31)
     suff = [rng.uniform_int(key, i, suffix_lo, suffix_hi) for i in range(n_req)]
     node_len = [prefix] + suff
     parent = [-1] + [0] * n_req
-    return _assemble("document_qa", 32, 8, 128, "bf16", node_len, parent,
+    return _assemble("document_qa", heads[0], heads[1], 128, "bf16", node_len, parent,
                      list(range(1, n_req + 1)), seed, meta={"config": 2})
 
 
