@@ -76,6 +76,7 @@ def parse():
                     help="steps of a separate loop with the library's per-group events (after the timed loop)")
     ap.add_argument("--no-per-config", action="store_true", help="skip the other workloads")
     ap.add_argument("--per-config", default=",".join(PER_CONFIG), help="comma-separated workloads for per_config")
+    ap.add_argument("--no-mla", action="store_true", help="leave the MLA entry out of per_config")
     ap.add_argument("--cpu-sample-s", type=float, default=12.0)
     ap.add_argument("--ref-budget-s", type=float, default=150.0,
                     help="host seconds the reference arm's warm-up and timed steps may take")
@@ -456,6 +457,76 @@ def measure(name, args, dev, steps, warmup, timer_steps, plan_opts, e2e=False, w
     return out
 
 
+MLA_D_C = 512
+MLA_HEADS = (16, 16)
+
+
+def measure_mla(dev, steps: int, warmup: int):
+    """Multi-head latent attention on the document-QA tree (16 heads, d=128,
+    MHA after the rebuild, latent d_c = 512): per step the per-head K/V of
+    every tree page are rebuilt from the latent pool (pst_mla_reconstruct) and
+    the decode pipeline runs on them. Reports the step, the rebuild alone
+    (CUDA events around it, on the launching stream) and the rebuild's
+    tensor-core and HBM rates."""
+    import numpy as np
+    import torch
+    import synth
+    from prefix_shared_tree_gb300.torch_api import TreeDecodeAttention, to_device
+    wl = synth.document_qa(heads=MLA_HEADS)
+    C, Wk, Wv = wl.mla_inputs(MLA_D_C)
+    att = TreeDecodeAttention.from_workload(wl, device=dev)
+    Cd, Wkd, Wvd = (to_device(x, "bf16", dev) for x in (C, Wk, Wv))
+    Qd = to_device(wl.q(), "bf16", dev)
+    shape = (wl.num_pages, wl.n_kv_heads, wl.page_size, wl.d)
+    Kd = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    Vd = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    O = torch.empty((wl.n_queries, wl.n_q_heads, wl.d), dtype=torch.float32, device=dev)
+    L = torch.empty((wl.n_queries, wl.n_q_heads), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        att.mla_reconstruct(Cd, Wkd, Wvd, Kd, Vd)
+        att(Qd, Kd, Vd, O, L)
+
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    ev[0].record(stream)
+    for _ in range(steps):
+        step()
+    ev[1].record(stream)
+    ev[2].record(stream)
+    for _ in range(steps):
+        att.mla_reconstruct(Cd, Wkd, Wvd, Kd, Vd)
+    ev[3].record(stream)
+    torch.cuda.synchronize(dev)
+    if att.check_status() != 0:
+        raise RuntimeError("mla: device status word set")
+    step_us = ev[0].elapsed_time(ev[1]) * 1e3 / steps
+    rebuild_us = ev[2].elapsed_time(ev[3]) * 1e3 / steps
+    n_pages = len(np.unique(wl.page_ids))
+    rows = n_pages * wl.page_size
+    flops = 2.0 * rows * MLA_D_C * 2 * wl.n_kv_heads * wl.d
+    bytes_ = rows * MLA_D_C * 2 + rows * 2 * wl.n_kv_heads * wl.d * 2
+    try:
+        tf_peak = float(json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))["bf16_tflops"])
+    except Exception:
+        tf_peak = 1900.0
+    hbm, _ = measured_peaks()
+    out = {"workload": "document_qa tree, 16 heads (MHA after the rebuild), d=128, latent d_c=512, bf16",
+           "us_per_step": round(step_us, 3), "rebuild_us": round(rebuild_us, 3),
+           "decode_us": round(step_us - rebuild_us, 3), "pages_rebuilt": int(n_pages),
+           "rebuild_tflops": round(flops / (rebuild_us * 1e-6) / 1e12, 1),
+           "rebuild_frac_of_bf16_peak": round(flops / (rebuild_us * 1e-6) / 1e12 / tf_peak, 4),
+           "rebuild_hbm_gbs": round(bytes_ / (rebuild_us * 1e-6) / 1e9, 1),
+           "rebuild_frac_of_hbm": round(bytes_ / (rebuild_us * 1e-6) / 1e9 / hbm, 4),
+           "rebuild_flops": flops, "rebuild_bytes": int(bytes_), "steps": steps}
+    del Cd, Wkd, Wvd, Kd, Vd, att
+    torch.cuda.empty_cache()
+    return out
+
+
 def _config_entry(m):
     peak = m["peak"]
     gbs = m["U"] / (m["us"] * 1e-6) / 1e9
@@ -493,6 +564,8 @@ def run_ours(args, rank, world):
             per_config[name] = _config_entry(m)
             shared_us[name] = m["us"]
             per_config[name]["steps"] = steps_pc
+        if not args.no_mla:
+            per_config["document_qa_mla"] = measure_mla(dev, min(steps_pc, 100), 5)
         for name, e in per_config.items():
             base = name[:-len("_flat")] if name.endswith("_flat") else None
             if base and base in shared_us:

@@ -13,7 +13,7 @@
 // One thread block takes 8 pages (128 latent rows: the M side of a tcgen05
 // MMA) and a range of kv heads. The latent tile stays in shared memory (one
 // TMA box of 16 rows x 64 channels per page and 128-byte slab); the weight
-// rows of each (head, K or V) stream through a two-stage ring, two slabs per
+// rows of each (head, K or V) stream through a three-stage ring, two slabs per
 // stage, as the N x K operand (N = d output channels); the products
 // accumulate in tensor memory, double-buffered so that four epilogue warps
 // convert one head's rows to bf16 and store them while the next head's MMAs
@@ -34,7 +34,7 @@ namespace dev {
 
 constexpr int kMlaRows = 128;                     // latent rows per block (MMA M)
 constexpr int kMlaPages = kMlaRows / kBoxRows;    // 8 pages of 16 rows
-constexpr int kMlaStages = 2;                     // weight ring
+constexpr int kMlaStages = 3;                     // weight ring
 constexpr int kMlaSlabsPerStage = 2;              // 128 latent channels per stage
 constexpr int kMlaMaxSlabs = 8;                   // d_c <= 512
 constexpr int kMlaThreads = 6 * 32;
