@@ -29,16 +29,16 @@ cudaError_t launch_pac_cc(const DevPlan& P, pst_dtype dt, const void* tk, const 
                           int r_tile, int n_items, int item_off, int counter, cudaStream_t st, bool pdl);
 cudaError_t launch_pac_tc(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
                           int item_off, cudaStream_t st, bool pdl);
-cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items,
-                            int item_off, bool exact_p, bool split_rows, cudaStream_t st, bool pdl);
+cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* tq, const void* Q,
+                            int n_items, int item_off, bool exact_p, bool split_rows, cudaStream_t st, bool pdl);
 cudaError_t launch_pac_thin(const DevPlan& P, const void* tk5, const void* tv5, const void* Q, int rows_per_head,
                             int n_items, int item_off, int counter, cudaStream_t st, bool pdl);
 
 // Tensor-core PAC launch group g (pst_plan::tc_group_cnt): P rounded once
 // (g < 2) or exact, more than 128 rows per block (even g) or at most 128.
 // The mma.sync engine has all its items in group 1.
-cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
-                            int g, LaunchSeq& ls) {
+cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* tq,
+                            const void* Q, int g, LaunchSeq& ls) {
     int64_t off = 0;
     for (int k = 0; k < g; ++k) off += p->tc_group_cnt[k];
     const int n = (int)p->tc_group_cnt[g];
@@ -46,7 +46,7 @@ cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk
     if (p->opts.tc_engine == 1) return launch_pac_tc(dp, tk, tv, Q, n, (int)off, ls.st, ls.next_pdl());
     // d = 128: V in 4 KB page boxes (the pool's second 5-D view)
     const void* tv_umma = p->d == 128 ? static_cast<const void*>(static_cast<const unsigned char*>(tv) + 256) : tv;
-    return launch_pac_umma(dp, tk, tv_umma, Q, n, (int)off, g >= 2, (g & 1) == 0, ls.st, ls.next_pdl());
+    return launch_pac_umma(dp, tk, tv_umma, tq, Q, n, (int)off, g >= 2, (g & 1) == 0, ls.st, ls.next_pdl());
 }
 
 // Thin chunks: tcgen05 thin PAC launches for row blocks of 8 and of 4 (work
@@ -220,6 +220,24 @@ static int make_pool_map(const pst_plan* p, const void* pool, unsigned char* out
 // workspace (same layout, base `ws`).
 int encode_pool_map(const pst_plan* p, const void* pool, unsigned char* out) { return make_pool_map(p, pool, out); }
 
+int encode_bf16_map(void* out, int rank, const void* base, const uint64_t* dims, const uint64_t* strides,
+                    const uint32_t* box);
+
+// Q [B][Hq][d] as (channel, q-head, query) with boxes of 64 channels x G
+// heads x 128/G queries: the 128 rows of one tcgen05-PAC row half (query-major,
+// then the G heads of one kv head), 128-byte swizzle. Used for bf16 with G up
+// to 16 and dividing 128: measured on GB300, the TMA copy made document QA
+// (G = 4) 1.6 % and few-shot 6 % faster per step, but tree-of-thought MQA
+// (G = 32) 2 % slower than staging Q row by row.
+bool q_map_fits(const pst_plan* p) { return p->dtype == PST_BF16 && p->group <= 16 && 128 % p->group == 0; }
+
+int encode_q_map(const pst_plan* p, const void* Q, unsigned char* out) {
+    const uint64_t dims[3] = {(uint64_t)p->d, (uint64_t)p->hq, (uint64_t)p->n_queries};
+    const uint64_t str[2] = {(uint64_t)p->d * 2, (uint64_t)p->hq * p->d * 2};
+    const uint32_t box[3] = {64, (uint32_t)p->group, (uint32_t)(128 / p->group)};
+    return encode_bf16_map(out, 3, Q, dims, str, box);
+}
+
 // A bf16 tensor map with 128-byte swizzle for the library's other launchers:
 // `rank` dims (innermost first), strides in bytes of dims 1.., box extents.
 int encode_bf16_map(void* out, int rank, const void* base, const uint64_t* dims, const uint64_t* strides,
@@ -329,6 +347,13 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
         if (rc) return rc;
         p->tmap_v_ptr = V;
     }
+    const bool q_map = q_map_fits(p);
+    if (q_map && p->tmap_q_ptr != Q) {
+        int rc = encode_q_map(p, Q, p->tmap_q);
+        if (rc) return rc;
+        p->tmap_q_ptr = Q;
+    }
+    const void* tq = q_map ? static_cast<const void*>(p->tmap_q) : nullptr;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const DevPlan dp = dev_plan(p);
     cudaEvent_t* ev = nullptr;
@@ -359,7 +384,7 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
         LaunchSeq ls(st, true);
         for (int g = 0; g < kGroups; ++g) {
             if (!has[g]) continue;
-            e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g, ls)
+            e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, tq, Q, g, ls)
                       : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, ls);
             if (e != cudaSuccess) return cuda_fail(g < 4 ? "decode_attn: PAC (tensor core) launch"
                                                          : "decode_attn: PAC (thin chunks) launch", e);
@@ -400,7 +425,7 @@ static int decode_impl(const pst_plan* p, const void* Q, const void* K, const vo
     for (int g = 0; g < kGroups; ++g) {
         if (!has[g]) continue;
         LaunchSeq ls(gst[g], false);
-        e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, Q, g, ls)
+        e = g < 4 ? launch_tc_group(p, dp, p->tmap_k, p->tmap_v, tq, Q, g, ls)
                   : launch_cc_group(p, dp, p->tmap_k, p->tmap_v, Q, ls);
         if (e != cudaSuccess) return cuda_fail(g < 4 ? "decode_attn: PAC (tensor core) launch"
                                                      : "decode_attn: PAC (thin chunks) launch", e);

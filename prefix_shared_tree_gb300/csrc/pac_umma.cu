@@ -103,7 +103,7 @@ struct UmmaLayout {
     static constexpr uint32_t kBars = kLRed + 1024 * 4;
     // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], q_ready, s_full[2], p_full[2], mma_done,
     // xchg[2], lfin
-    static constexpr int kNumBars = 2 * KST + 2 * VST + 9;
+    static constexpr int kNumBars = 2 * KST + 2 * VST + 10;
     static constexpr uint32_t kBytes = kBars + 8 * kNumBars + 16;
     static_assert(kBytes + 1024 <= 232448, "shared memory");
     static constexpr uint32_t kTmemCols = 512;
@@ -266,7 +266,7 @@ __device__ __forceinline__ bool zero_stray_v(const DevPlan& P, uint8_t* base, co
 template <int D, bool EXACT, bool SPLIT>
 __global__ void __launch_bounds__(UWarps<SPLIT>::kThreads, 1)
 pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
-                const __nv_bfloat16* __restrict__ Q, int item_off) {
+                const __nv_bfloat16* __restrict__ Q, int item_off, const __grid_constant__ CUtensorMap tq, int q_tma) {
     using L = UmmaLayout<D>;
     constexpr int NSLAB = L::NSLAB;
     constexpr int KST = L::KST, VST = L::VST;
@@ -284,6 +284,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     const uint32_t mma_done = p_full + 16;
     const uint32_t xchg_bar = mma_done + 8;   // [half]: both groups' row maxima of a half are in
     const uint32_t lfin_bar = xchg_bar + 16;  // both groups' row sums are in
+    const uint32_t q_full = lfin_bar + 8;     // the TMA copy of Q has landed
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kBars + 8 * L::kNumBars);
     float2* xchg = reinterpret_cast<float2*>(base + L::kXchg);
 
@@ -314,6 +315,7 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             mbar_init(v_empty + 8 * s, 1);
         }
         mbar_init(q_ready, 128 * UWarps<SPLIT>::kGroups);
+        mbar_init(q_full, 1);
         for (int w = 0; w < 2; ++w) {
             mbar_init(s_full + 8 * w, 1);
             // above 128 rows every group works on each half
@@ -333,6 +335,18 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     umma::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     const ChunkGeo geo = chunk_geo<kUT>(C);
+    // When the block's queries have consecutive ids (the chunk's query list
+    // is ascending) and it has at least 128 rows, its Q rows (query-major,
+    // then the G heads of this kv head) are one box per 128 rows and
+    // 64-channel slab of the Q tensor map, copied by TMA instead of row by
+    // row (q_tma: the map fits this plan)
+    const int q_first = row0 / G, q_n = (rows_here + G - 1) / G;
+    auto q_run = [&](int* qa) {   // read only by the threads that stage Q
+        // a box holds 128 rows: blocks with fewer copy only their own rows
+        if (!q_tma || rows_here < 128) return false;
+        *qa = P.chunk_q[C.q_base + q_first];
+        return P.chunk_q[C.q_base + q_first + q_n - 1] - *qa == q_n - 1;
+    };
     const int n = geo.n_tiles;
     // steps of softmax group w: tiles it consumes, in order
     auto n_steps = [&](int w) { return split_rows ? n : (n - w + 1) / 2; };
@@ -365,7 +379,24 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         if (lane == 0) {
             constexpr uint32_t idS = umma::idesc_bf16_f32(128, kUT, 0, 0);
             constexpr uint32_t idO = umma::idesc_bf16_f32(128, D, 0, 1);   // V is MN-major
+            // Q by TMA when the block's queries are consecutive (this thread
+            // has nothing else to do before Q is in); the softmax threads
+            // stage it row by row otherwise
+            int qa = 0;
+            const bool q_by_tma = q_run(&qa);
+            if (q_by_tma) {
+                prefetch_tmap(&tq);
+                constexpr int kHalves = SPLIT ? 2 : 1;
+                mbar_arrive_expect_tx(q_full, kHalves * NSLAB * L::kQSlab);
+                for (int h = 0; h < kHalves; ++h)
+                    for (int s = 0; s < NSLAB; ++s)
+                        tma_load_3d(sQ + (h * NSLAB + s) * L::kQSlab, &tq, 64 * s, head * G, qa + h * (128 / G),
+                                    q_full);
+            }
             bool ok = mbar_wait(q_ready, 0, P.status);
+            // (also waited for when the wait above gave up: no copy may still
+            // be writing shared memory when the block leaves)
+            if (q_by_tma) ok = mbar_wait(q_full, 0, P.status) && ok;
             // test only: mma_done gets its first arrival from this thread's
             // final commit below, so this bounded wait (about a millisecond)
             // runs out and the block leaves through its error path
@@ -470,7 +501,8 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             gh = (row0 + rloc) % G;
             if (C.mask_base >= 0) mask = P.masks[C.mask_base + qi];
         }
-        if (split_rows ? w < 2 : w == 0) {
+        int qa_unused;
+        if ((split_rows ? w < 2 : w == 0) && !q_run(&qa_unused)) {
             uint8_t* qdst = base + L::kQ + (split_rows ? w : 0) * NSLAB * L::kQSlab;
             if (row_ok) {
                 const int qid = P.chunk_q[C.q_base + qi];
@@ -702,8 +734,8 @@ pac_umma_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
 }
 
 template <int D, bool EXACT, bool SPLIT>
-cudaError_t launch_umma_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
-                          int item_off, cudaStream_t st, bool pdl) {
+cudaError_t launch_umma_t(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq,
+                          const void* Q, int n_items, int item_off, cudaStream_t st, bool pdl) {
     const size_t smem = 1024 + UmmaLayout<D>::kBytes;
     static DeviceOnce once;   // per device
     cudaError_t e = per_device(once, nullptr, nullptr, [&](int, int* a, int*) {
@@ -720,27 +752,30 @@ cudaError_t launch_umma_t(const DevPlan& P, const CUtensorMap* tk, const CUtenso
     });
     if (e != cudaSuccess) return e;
     return launch_kernel(pac_umma_kernel<D, EXACT, SPLIT>, dim3(n_items), dim3(UWarps<SPLIT>::kThreads), smem, st, pdl,
-                         P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q), item_off);
+                         P, *tk, *tv, static_cast<const __nv_bfloat16*>(Q), item_off, tq ? *tq : *tk, tq ? 1 : 0);
 }
 
 template <int D, bool EXACT>
-cudaError_t launch_umma_m(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const void* Q, int n_items,
-                          int item_off, bool split_rows, cudaStream_t st, bool pdl) {
-    return split_rows ? launch_umma_t<D, EXACT, true>(P, tk, tv, Q, n_items, item_off, st, pdl)
-                      : launch_umma_t<D, EXACT, false>(P, tk, tv, Q, n_items, item_off, st, pdl);
+cudaError_t launch_umma_m(const DevPlan& P, const CUtensorMap* tk, const CUtensorMap* tv, const CUtensorMap* tq,
+                          const void* Q, int n_items, int item_off, bool split_rows, cudaStream_t st, bool pdl) {
+    return split_rows ? launch_umma_t<D, EXACT, true>(P, tk, tv, tq, Q, n_items, item_off, st, pdl)
+                      : launch_umma_t<D, EXACT, false>(P, tk, tv, tq, Q, n_items, item_off, st, pdl);
 }
 
 }  // namespace dev
 
-cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* Q, int n_items, int item_off,
-                            bool exact_p, bool split_rows, cudaStream_t st, bool pdl) {
+// tq: the Q tensor map (boxes of 128 rows x 64 channels), or null to stage Q
+// row by row
+cudaError_t launch_pac_umma(const DevPlan& P, const void* tk, const void* tv, const void* tq, const void* Q,
+                            int n_items, int item_off, bool exact_p, bool split_rows, cudaStream_t st, bool pdl) {
     const CUtensorMap* k = static_cast<const CUtensorMap*>(tk);
     const CUtensorMap* v = static_cast<const CUtensorMap*>(tv);
+    const CUtensorMap* q = static_cast<const CUtensorMap*>(tq);
     if (P.d == 128)
-        return exact_p ? dev::launch_umma_m<128, true>(P, k, v, Q, n_items, item_off, split_rows, st, pdl)
-                       : dev::launch_umma_m<128, false>(P, k, v, Q, n_items, item_off, split_rows, st, pdl);
-    return exact_p ? dev::launch_umma_m<64, true>(P, k, v, Q, n_items, item_off, split_rows, st, pdl)
-                   : dev::launch_umma_m<64, false>(P, k, v, Q, n_items, item_off, split_rows, st, pdl);
+        return exact_p ? dev::launch_umma_m<128, true>(P, k, v, q, Q, n_items, item_off, split_rows, st, pdl)
+                       : dev::launch_umma_m<128, false>(P, k, v, q, Q, n_items, item_off, split_rows, st, pdl);
+    return exact_p ? dev::launch_umma_m<64, true>(P, k, v, q, Q, n_items, item_off, split_rows, st, pdl)
+                   : dev::launch_umma_m<64, false>(P, k, v, q, Q, n_items, item_off, split_rows, st, pdl);
 }
 
 }  // namespace pst

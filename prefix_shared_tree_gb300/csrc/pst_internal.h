@@ -211,4 +211,8 @@ struct pst_plan {
     // PAC's V tiles (4 KB page boxes)
     alignas(64) mutable unsigned char tmap_k[384];
     alignas(64) mutable unsigned char tmap_v[384];
+    // Q for the tcgen05 PAC (boxes of 128 rows x 64 channels), when the plan's
+    // shape allows one (bf16, a GQA group that divides 128)
+    mutable const void* tmap_q_ptr = nullptr;
+    alignas(64) mutable unsigned char tmap_q[128];
 };

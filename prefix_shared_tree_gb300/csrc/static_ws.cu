@@ -18,8 +18,10 @@
 
 namespace pst {
 
-cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
-                            int g, LaunchSeq& ls);
+cudaError_t launch_tc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* tq,
+                            const void* Q, int g, LaunchSeq& ls);
+bool q_map_fits(const pst_plan* p);
+int encode_q_map(const pst_plan* p, const void* Q, unsigned char* out);
 cudaError_t launch_cc_group(const pst_plan* p, const DevPlan& dp, const void* tk, const void* tv, const void* Q,
                             LaunchSeq& ls);
 cudaError_t launch_por(const DevPlan& dp, float* O, float* LSE, LaunchSeq& ls);
@@ -87,12 +89,16 @@ extern "C" int pst_decode_attn_noalloc(const pst_plan* p, const void* Q, const v
     if (rc) return rc;
     rc = encode_pool_map(p, V, tv);
     if (rc) return rc;
+    alignas(64) unsigned char tq[128];
+    const bool q_map = q_map_fits(p);
+    if (q_map && (rc = encode_q_map(p, Q, tq)) != 0) return rc;
     const DevPlan dp = dev_plan_at(p, ws);
     // the launch groups on `stream`: chained by programmatic dependencies
     // (the default), else one after the other
     LaunchSeq ls(st, p->opts.side_streams == 0);
     for (int g = 0; g < 5; ++g) {
-        e = g < 4 ? launch_tc_group(p, dp, tk, tv, Q, g, ls) : launch_cc_group(p, dp, tk, tv, Q, ls);
+        e = g < 4 ? launch_tc_group(p, dp, tk, tv, q_map ? tq : nullptr, Q, g, ls)
+                  : launch_cc_group(p, dp, tk, tv, Q, ls);
         if (e != cudaSuccess) return fail(PST_ECUDA, std::string("decode_attn_noalloc: PAC launch: ") + cudaGetErrorString(e));
     }
     e = launch_por(dp, O, LSE, ls);
