@@ -455,11 +455,17 @@ struct Planner {
         }
         // the plan is never worse (under C_est) than no split or a uniform split
         consider(std::vector<int>(nt, 1));
-        for (int chunk = kTileTokens; chunk <= 8192; chunk *= 2) {
-            std::vector<int> b(nt);
-            for (size_t i = 0; i < nt; ++i)
-                b[i] = tasks[i].node < 0 ? 1 : std::max(1, std::min(tasks[i].max_splits, (tasks[i].n_tok + chunk - 1) / chunk));
-            consider(b);
+        // (64, 128, 192, 256, 384, ... 6144, 8192 tokens: powers of two and
+        // their halfway points, all multiples of the 64-token tile)
+        for (int pow2 = kTileTokens; pow2 <= 8192; pow2 *= 2) {
+            for (int chunk : {pow2, pow2 * 3 / 2}) {
+                if (chunk > 8192 || chunk % kTileTokens) continue;
+                std::vector<int> b(nt);
+                for (size_t i = 0; i < nt; ++i)
+                    b[i] = tasks[i].node < 0 ? 1
+                                             : std::max(1, std::min(tasks[i].max_splits, (tasks[i].n_tok + chunk - 1) / chunk));
+                consider(b);
+            }
         }
         // greedy +-1 refinement of single tasks, largest per-item cost first
         for (int iter = 0; iter < 24; ++iter) {
