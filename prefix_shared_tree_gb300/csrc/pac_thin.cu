@@ -72,16 +72,16 @@ struct ThinLayout {
     static constexpr uint32_t kSlot = kSum + 2 * 2 * 2 * kThinHeads * R * 4;  // ThinSlot x 2 (item parity)
     static constexpr uint32_t kBars = kSlot + 2 * 64;
     // k_full[KST], k_empty[KST], v_full[VST], v_empty[VST], item_full[2], item_empty[2], q_empty[2],
-    // s_full[2], p_full[2], vote_bar[2], o_full, fin, lsum_bar, epi_bar
-    static constexpr int kNumBars = 2 * KST + 2 * VST + 12 + 4;
+    // s_full[2], p_full[2], vote_bar[2], s_free[2], pv_done[2], o_full, fin, fin_pv, lsum_bar, epi_bar
+    static constexpr int kNumBars = 2 * KST + 2 * VST + 16 + 5;
     static constexpr uint32_t kTslot = kBars + 8 * kNumBars;
     static constexpr uint32_t kBytes = kTslot + 16;
     static_assert(kBytes + 1024 <= 232448, "shared memory");
     static_assert(kQ % 1024 == 0 && kP % 1024 == 0 && kQSlab % 1024 == 0, "SW128 operand alignment");
     static constexpr uint32_t kTmemCols = 512;
-    // S^T of group w's tiles; O^T of group w, head h: hi part of row r at
-    // colO(w) + 16 h + r, lo part at colO(w) + 16 h + R + r
-    __device__ static constexpr uint32_t colS(int w) { return NS * w; }
+    // S^T of global tile g in buffer g & 1; O^T of group w, head h: hi part of
+    // row r at colO(w) + 16 h + r, lo part at colO(w) + 16 h + R + r
+    __device__ static constexpr uint32_t colS(int b) { return NS * b; }
     __device__ static constexpr uint32_t colO(int w) { return 2 * NS + 16 * kThinHeads * w; }
     static_assert(2 * NS + 2 * 16 * kThinHeads <= kTmemCols, "tensor memory columns");
 };
@@ -181,10 +181,13 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
     const uint32_t k_full = bars, k_empty = k_full + 8 * KST;
     const uint32_t v_full = k_empty + 8 * KST, v_empty = v_full + 8 * VST;
     const uint32_t item_full = v_empty + 8 * VST, item_empty = item_full + 16, q_empty = item_empty + 16;
-    const uint32_t s_full = q_empty + 16, p_full = s_full + 16;   // [group]
+    const uint32_t s_full = q_empty + 16;     // [S^T buffer]
+    const uint32_t p_full = s_full + 16;      // [group]
     const uint32_t vote_bar = p_full + 16;    // [group]: every head's growth flag is in
-    const uint32_t o_full = vote_bar + 16, fin = o_full + 8;
-    const uint32_t lsum_bar = fin + 8;        // both groups' row sums and maxima are in
+    const uint32_t s_free = vote_bar + 16;    // [S^T buffer]: its softmax has loaded it
+    const uint32_t pv_done = s_free + 16;     // [group]: the group's P V products issued so far have finished
+    const uint32_t o_full = pv_done + 16, fin = o_full + 8, fin_pv = fin + 8;
+    const uint32_t lsum_bar = fin_pv + 8;     // both groups' row sums and maxima are in
     const uint32_t epi_bar = lsum_bar + 8;    // both groups have read both accumulators
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(base + L::kTslot);
     ThinSlot* slots = reinterpret_cast<ThinSlot*>(base + L::kSlot);
@@ -202,12 +205,15 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(item_full + 8 * b, 32);       // every lane of the producer warp (its Q stores)
-            mbar_init(item_empty + 8 * b, 2 + 8);   // the V producer, the MMA thread, the eight softmax warps
+            mbar_init(item_empty + 8 * b, 3 + 8);   // the V producer, the two MMA threads, the eight softmax warps
             mbar_init(q_empty + 8 * b, 1);
             mbar_init(s_full + 8 * b, 1);
             mbar_init(p_full + 8 * b, 128);
             mbar_init(vote_bar + 8 * b, 128);
+            mbar_init(s_free + 8 * b, 128);
+            mbar_init(pv_done + 8 * b, 1);
         }
+        mbar_init(fin_pv, 1);
         mbar_init(o_full, 1);
         mbar_init(fin, 1);
         mbar_init(lsum_bar, 256);
@@ -330,8 +336,15 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             if (gbase >= 0) drain_ring<VST>(v_full, gbase, P.status);
         }
         __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 1 || warp == 3) {
+        // ------------------------------------------------------------ MMA issuers
+        // Two threads issue the tensor-core work side by side: warp 1 the S^T
+        // MMAs of every tile, warp 3 the P V MMAs (issuing a tcgen05 MMA costs
+        // its thread tens of cycles, so one thread for both streams serialises
+        // them). Each orders its own MMAs; the softmax warps get the cross
+        // orderings from barriers: S^T buffer g & 1 is refilled once its
+        // softmax has loaded it (s_free), and a group waits for its previous
+        // P V (pv_done) before it rescales O^T or rewrites its P^T.
         if (lane == 0) {
             constexpr uint32_t idS = umma::idesc_bf16_f32(128, NS, 0, 0);   // K and Q both K-major
             constexpr uint32_t idO = umma::idesc_bf16_f32(128, 16, 1, 0);   // V^T MN-major, P^T K-major
@@ -342,23 +355,9 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             const uint64_t dv0 = umma::smem_desc_sw128(sbase + L::kV, L::kSlab, 1024);
             const uint64_t dq0 = umma::smem_desc_sw128(sbase + L::kQ, 16, 1024);
             const uint64_t dp0 = umma::smem_desc_sw128(sbase + L::kP, 16, 1024);
-            // p_full[w] completes once per tile of group w: its P^T is in (phases so far)
-            int n_p0 = 0, n_p1 = 0;
-            // O^T_h of group w (+)= V_h^T [P_hi; P_lo]_h^T for global tile g, every head h
-            auto issue_pv = [&](int g, int w, bool first) -> bool {
-                if (!mbar_wait(p_full + 8 * w, (w ? n_p1++ : n_p0++) & 1, P.status)) return false;
-                if (!mbar_wait(v_full + 8 * (g % VST), (g / VST) & 1, P.status)) return false;
-                umma::fence_after_sync();
-                const uint64_t dv = dv0 + (uint64_t)(((g % VST) * L::kOp) >> 4);
-                const uint64_t dp = dp0 + (uint64_t)((w * L::kPBuf) >> 4);   // group w's P^T
-#pragma unroll
-                for (int h = 0; h < HB; ++h)
-                    umma::mma_bf16_ss(tmem + L::colO(w) + 16 * h, dv + ((h * 2048) >> 4),
-                                      dp + (((h / 4) * L::kPSlab + (h % 4) * 32) >> 4), idO, first ? 0u : 1u);
-                umma::commit(v_empty + 8 * (g % VST));
-                return true;
-            };
+            const bool s_side = warp == 1;
             int gbase = 0;
+            int n_p[2] = {0, 0};   // P V side: p_full phases consumed per group
             bool ok = true;
             for (int q = 0; ok; ++q) {
                 const int slot = q & 1;
@@ -368,30 +367,53 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 mbar_arrive(item_empty + 8 * slot);
                 if (idx < 0) break;
                 const int n = chunk_geo<kThinTT>(C).n_tiles;
-                const uint64_t dq = dq0 + (uint64_t)((slot * L::kQBuf) >> 4);
-                for (int j = 0; j < n; ++j) {
-                    const int g = gbase + j;
-                    if (!mbar_wait(k_full + 8 * (g % KST), (g / KST) & 1, P.status)) { ok = false; break; }
-                    umma::fence_after_sync();
-                    const uint64_t dk = dk0 + (uint64_t)(((g % KST) * L::kOp) >> 4);
+                if (s_side) {
+                    const uint64_t dq = dq0 + (uint64_t)((slot * L::kQBuf) >> 4);
+                    for (int j = 0; j < n; ++j) {
+                        const int g = gbase + j;
+                        // buffer g & 1 last held S^T of tile g - 2: loaded by its softmax
+                        if (g >= 2 && !mbar_wait(s_free + 8 * (g & 1), ((g >> 1) - 1) & 1, P.status)) {
+                            ok = false;
+                            break;
+                        }
+                        if (!mbar_wait(k_full + 8 * (g % KST), (g / KST) & 1, P.status)) { ok = false; break; }
+                        umma::fence_after_sync();
+                        const uint64_t dk = dk0 + (uint64_t)(((g % KST) * L::kOp) >> 4);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma::mma_bf16_ss(tmem + L::colS(j & 1), dk + (((kk / 4) * L::kSlab + (kk % 4) * 32) >> 4),
-                                          dq + (((kk / 4) * L::kQSlab + (kk % 4) * 32) >> 4), idS,
-                                          kk > 0 ? 1u : 0u);
-                    umma::commit(s_full + 8 * (j & 1));
-                    umma::commit(k_empty + 8 * (g % KST));
-                    if (j == n - 1) umma::commit(q_empty + 8 * slot);
-                    // a group's first tile of the item starts its accumulator
-                    if (j >= 1 && !issue_pv(g - 1, (j - 1) & 1, j - 1 < 2)) { ok = false; break; }
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            umma::mma_bf16_ss(tmem + L::colS(g & 1), dk + (((kk / 4) * L::kSlab + (kk % 4) * 32) >> 4),
+                                              dq + (((kk / 4) * L::kQSlab + (kk % 4) * 32) >> 4), idS,
+                                              kk > 0 ? 1u : 0u);
+                        umma::commit(s_full + 8 * (g & 1));
+                        umma::commit(k_empty + 8 * (g % KST));
+                        if (j == n - 1) umma::commit(q_empty + 8 * slot);
+                    }
+                } else {
+                    // O^T_h of group w (+)= V_h^T [P_hi; P_lo]_h^T for tile g, every
+                    // head h; a group's first tile of the item starts its accumulator
+                    for (int j = 0; j < n; ++j) {
+                        const int g = gbase + j, w = j & 1;
+                        if (!mbar_wait(p_full + 8 * w, n_p[w]++ & 1, P.status)) { ok = false; break; }
+                        if (!mbar_wait(v_full + 8 * (g % VST), (g / VST) & 1, P.status)) { ok = false; break; }
+                        umma::fence_after_sync();
+                        const uint64_t dv = dv0 + (uint64_t)(((g % VST) * L::kOp) >> 4);
+                        const uint64_t dp = dp0 + (uint64_t)((w * L::kPBuf) >> 4);   // group w's P^T
+#pragma unroll
+                        for (int h = 0; h < HB; ++h)
+                            umma::mma_bf16_ss(tmem + L::colO(w) + 16 * h, dv + ((h * 2048) >> 4),
+                                              dp + (((h / 4) * L::kPSlab + (h % 4) * 32) >> 4), idO,
+                                              j < 2 ? 0u : 1u);
+                        umma::commit(v_empty + 8 * (g % VST));
+                        umma::commit(pv_done + 8 * w);
+                    }
+                    if (ok) umma::commit(o_full);
                 }
-                if (!ok || !issue_pv(gbase + n - 1, (n - 1) & 1, n - 1 < 2)) break;
-                umma::commit(o_full);
                 gbase += n;
             }
-            // every MMA issued above has finished before tensor memory is released
-            umma::commit(fin);
-            mbar_wait(fin, 0, P.status);
+            // every MMA this thread issued has finished before tensor memory is released
+            const uint32_t done = s_side ? fin : fin_pv;
+            umma::commit(done);
+            mbar_wait(done, 0, P.status);
         }
         __syncwarp();
     } else if (warp >= 4) {
@@ -403,7 +425,7 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
         const uint32_t lane_addr = tmem + ((uint32_t)(32 * wq) << 16);
         float* vote = reinterpret_cast<float*>(base + L::kVote) + w * 2 * HB * (R + 1);   // [vote parity][head][1 + R]
         const float sl = P.scale_log2;
-        int gbase = 0, n_done = 0, n_vote = 0, n_tiles_w = 0;   // n_tiles_w: this group's tiles so far
+        int gbase = 0, n_done = 0, n_vote = 0, n_tiles_w = 0;   // n_tiles_w: this group's tiles so far (all items)
         bool ok = true;
         for (int q = 0; ok; ++q) {
             const int slot = q & 1;
@@ -433,11 +455,29 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
             }
             for (int j = w; j < n; j += 2) {
                 const int g = gbase + j;
-                if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * w, n_tiles_w++ & 1, P.status))) { ok = false; break; }
+                const int k_w = n_tiles_w++;   // this group's tiles before this one (all items)
+                if (!__all_sync(0xffffffffu, mbar_wait(s_full + 8 * (g & 1), (g >> 1) & 1, P.status))) {
+                    ok = false;
+                    break;
+                }
                 umma::fence_after_sync();
                 uint32_t sr[2 * R];   // this warp's two heads
-                ld_2r<R>(lane_addr + L::colS(w) + 2 * wq * R, sr);
+                ld_2r<R>(lane_addr + L::colS(g & 1) + 2 * wq * R, sr);
                 umma::wait_ld();
+                umma::fence_before_sync();
+                mbar_arrive(s_free + 8 * (g & 1));   // the S^T MMA thread may refill the buffer
+                // The group's previous P V (tile j - 2, issued by the other MMA
+                // thread) has finished before its O^T is rescaled or its P^T
+                // rewritten; for tiles j < 2 the previous item's P V products
+                // finished before its epilogue.
+                bool pv_waited = j < 2;
+                auto wait_prev_pv = [&]() -> bool {
+                    if (pv_waited) return true;
+                    pv_waited = true;
+                    if (!__all_sync(0xffffffffu, mbar_wait(pv_done + 8 * w, (k_w - 1) & 1, P.status))) return false;
+                    umma::fence_after_sync();   // order later tensor-memory accesses after those MMAs
+                    return true;
+                };
                 const int tpos = geo.tile0 + j * kThinTT;
                 const int pos = tpos + t;
                 const bool in = pos >= geo.pos_begin && pos < geo.pos_end;
@@ -453,6 +493,11 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                 // zero them before P V multiplies them by P = 0
                 if (tpos < geo.pos_begin || tpos + kThinTT > geo.pos_end) {
                     const int vs = g % VST;
+                    // V of tile g - 2 has landed (its P V finished) before the stage's
+                    // full barrier is waited on for tile g: with two V stages that
+                    // barrier could otherwise still be two phases back, where its
+                    // parity reads the same as tile g's
+                    if (!wait_prev_pv()) { ok = false; break; }
                     if (!__all_sync(0xffffffffu, mbar_wait(v_full + 8 * vs, (g / VST) & 1, P.status))) { ok = false; break; }
                     if (!in) {
 #pragma unroll
@@ -490,10 +535,10 @@ pac_thin_kernel(DevPlan P, const __grid_constant__ CUtensorMap tk, const __grid_
                     }
                 }
                 if (j >= 2) {
+                    if (!wait_prev_pv()) { ok = false; break; }
                     // a rescale of O^T touches every lane (channel): the group's heads
-                    // vote. The group's previous P V (tile j - 2) was issued before
-                    // S^T of tile j, so it has finished. The vote area alternates, so
-                    // the vote after next reuses it when every thread has read it.
+                    // vote. The vote area alternates, so the vote after next reuses it
+                    // when every thread has read it.
                     float* vb = vote + (n_vote & 1) * HB * (R + 1);
                     if (t == 0) {
                         vb[h * (R + 1)] = resc ? 1.f : 0.f;
