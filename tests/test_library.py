@@ -189,24 +189,28 @@ def test_deft_flatten_chunks_of_a_hand_laid_tree(lib):
                         (c2, [1], [all_ones])]
 
 
-def test_cost_model_scores_flatten_candidates(lib):
-    """The cost-model policy also scores DEFT-Flatten chunkings and keeps one
-    only when its predicted makespan is at least 3 % lower: on the
-    tree-of-thought GQA tree (many small nodes) it does; on document QA it
-    keeps the node partition; switched off, the node partition stays."""
-    tot = synth.tree_of_thought("gqa")
-    s_on = _plan(lib, tot).stats()
-    s_off = _plan(lib, tot, flatten_candidates=False).stats()
-    assert s_off["split_policy"] == 0
-    assert s_on["split_policy"] == 3 and s_on["fixed_chunk"] in (1024, 2048)
-    assert s_on["predicted_makespan_us"] < 0.97 * s_off["predicted_makespan_us"]
-    flat = _plan(lib, tot, split_policy="flatten", fixed_chunk=s_on["fixed_chunk"]).stats()
-    assert flat["predicted_makespan_us"] == s_on["predicted_makespan_us"]
-    dqa = synth.document_qa()
-    assert _plan(lib, dqa).stats()["split_policy"] == 0
-    for wl in (synth.few_shot(), synth.speculative(), dqa):
-        on, off = _plan(lib, wl).stats(), _plan(lib, wl, flatten_candidates=False).stats()
-        assert on["predicted_makespan_us"] <= off["predicted_makespan_us"]
+@pytest.mark.parametrize("make", [lambda: synth.tree_of_thought("gqa"), synth.document_qa, synth.few_shot,
+                                  synth.speculative, lambda: synth.random_tree(1007)],
+                         ids=["tot_gqa", "document_qa", "few_shot", "speculative", "random"])
+def test_cost_model_scores_flatten_candidates(lib, make):
+    """The cost-model policy also scores DEFT-Flatten chunkings of 1024 and
+    2048 tokens and keeps one only when its predicted makespan is at least
+    3 % below the node partition's; switched off, the node partition stays.
+    The rule is checked against plans built separately (whichever way the
+    measured cost tables decide it for this workload)."""
+    wl = make()
+    node = _plan(lib, wl, flatten_candidates=False).stats()
+    assert node["split_policy"] == 0
+    flat = {st: _plan(lib, wl, split_policy="flatten", fixed_chunk=st).stats()["predicted_makespan_us"]
+            for st in (1024, 2048)}
+    chosen = _plan(lib, wl).stats()
+    best_st = min(flat, key=lambda st: (flat[st], st))
+    if flat[best_st] < 0.97 * node["predicted_makespan_us"]:
+        assert chosen["split_policy"] == 3 and chosen["fixed_chunk"] == best_st
+        assert chosen["predicted_makespan_us"] == flat[best_st]
+    else:
+        assert chosen["split_policy"] == 0
+        assert chosen["predicted_makespan_us"] == node["predicted_makespan_us"]
 
 
 def test_speculative_drafts_are_packed_with_masks(lib):
