@@ -26,17 +26,17 @@
 // both parts in separate O^T columns (summed at the end): P V is as accurate
 // as an fp32 product. Two softmax warpgroups take alternate tiles of an item
 // (even and odd tile index, so the result does not depend on which block ran
-// the item) into their own S^T buffer and O^T accumulator (split-KV inside
-// the block) and merge at the end of the item. A group's running max only moves (and its O^T is
-// rescaled in tensor memory, after a vote of its four warps) when it grows by
-// more than 2^8.
+// the item), each into its own O^T accumulator (split-KV inside the block),
+// and merge at the end of the item; S^T of global tile g goes to buffer g & 1.
+// A group's running max only moves (and its O^T is rescaled in tensor memory,
+// after a vote of its four warps) when it grows by more than 2^8.
 //
 // Persistent blocks, one per SM, take items (largest first) from a work queue:
 //   warp 0      claims an item, stages its Q rows in shared memory, then
 //               streams the chunk's K tiles with TMA; warp 2 streams its V
 //               tiles into a second ring at its own pace;
-//   warp 1      allocates tensor memory and issues every MMA (one thread):
-//               S^T of tile g, then the P V products of tile g - 1;
+//   warp 1      allocates tensor memory and issues the S^T MMAs (one
+//               thread); warp 3 issues the P V MMAs (one thread);
 //   warps 4-7, 8-11  two softmax warpgroups (even and odd tiles of an item),
 //               one thread per tensor-memory lane, and the epilogue.
 #include <algorithm>
@@ -115,7 +115,7 @@ struct HRed {
     }
 };
 
-// An item as the producer hands it to the MMA thread and the softmax warps
+// An item as the producer hands it to the MMA threads and the softmax warps
 // (index -1: no more items).
 struct alignas(16) ThinSlot {
     DevChunk C;
