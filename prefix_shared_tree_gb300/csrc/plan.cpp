@@ -22,6 +22,7 @@
 #include <new>
 #include <numeric>
 #include <queue>
+#include <unordered_map>
 #include <string>
 
 #include "pst_internal.h"
@@ -273,20 +274,27 @@ double list_schedule(std::vector<ItemCost>& v, int m, std::vector<int>* slot = n
     return mk;
 }
 
+// `n` items of one launch class and one cost (a chunk's row block over the
+// kv heads). Which of several equal-cost items goes first does not change
+// any SM's load, so the dispatcher's view below depends only on the
+// multiset of (class, cost) and takes the items as such runs.
+struct CostRun {
+    double cost;
+    int32_t n;
+    int8_t klass;   // as ItemCost::klass
+};
+
 // The block dispatcher's view of one decode call, used to score a partition:
 // the tensor-core launches come first and hold an SM per block (largest
 // first, the exact-P launch after the other); the CUDA-core launches run one
 // after the other on their own stream with `cc_per_sm[k]` blocks per SM, a
 // block taking cc_per_sm[k] x C_est of wall time (C_est is per-SM-slot
 // throughput), on the SMs the tensor-core blocks leave and, once those
-// retire, on theirs. Returns the time the last block ends.
-double simulate_call(std::vector<ItemCost> v, int num_sms, const int (&cc_per_sm)[4]) {
-    std::sort(v.begin(), v.end(), [](const ItemCost& a, const ItemCost& b) {
+// retire, on theirs. Sorts v; returns the time the last block ends.
+double simulate_call(std::vector<CostRun>& v, int num_sms, const int (&cc_per_sm)[4]) {
+    std::sort(v.begin(), v.end(), [](const CostRun& a, const CostRun& b) {
         if (a.klass != b.klass) return a.klass < b.klass;
-        if (a.cost != b.cost) return a.cost > b.cost;
-        if (a.chunk != b.chunk) return a.chunk < b.chunk;
-        if (a.head != b.head) return a.head < b.head;
-        return a.rb < b.rb;
+        return a.cost > b.cost;
     });
     using Slot = std::pair<double, int>;
     std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> sm;
@@ -295,12 +303,14 @@ double simulate_call(std::vector<ItemCost> v, int num_sms, const int (&cc_per_sm
     size_t i = 0;
     double end = 0;
     for (; i < v.size() && v[i].klass < 2; ++i) {
-        Slot x = sm.top();
-        sm.pop();
-        x.first += v[i].cost;
-        sm_free[x.second] = x.first;
-        end = std::max(end, x.first);
-        sm.push(x);
+        for (int32_t r = 0; r < v[i].n; ++r) {
+            Slot x = sm.top();
+            sm.pop();
+            x.first += v[i].cost;
+            sm_free[x.second] = x.first;
+            end = std::max(end, x.first);
+            sm.push(x);
+        }
     }
     double start = 0;   // a CUDA-core launch starts when the previous one has ended
     while (i < v.size()) {
@@ -311,11 +321,13 @@ double simulate_call(std::vector<ItemCost> v, int num_sms, const int (&cc_per_sm
             for (int b = 0; b < per; ++b) slots.push(std::max(start, sm_free[s2]));
         double cls_end = start;
         for (; i < v.size() && v[i].klass - 2 == k; ++i) {
-            double t = slots.top();
-            slots.pop();
-            t += per * v[i].cost;
-            cls_end = std::max(cls_end, t);
-            slots.push(t);
+            for (int32_t r = 0; r < v[i].n; ++r) {
+                double t = slots.top();
+                slots.pop();
+                t += per * v[i].cost;
+                cls_end = std::max(cls_end, t);
+                slots.push(t);
+            }
         }
         start = cls_end;
         end = std::max(end, cls_end);
@@ -361,37 +373,46 @@ struct Planner {
     // kv heads one item covers (the thin PAC takes kThinHeads at once)
     int heads_per_item(const Task& t) const { return (t.kind == 0 && P.thin) ? kThinHeads : 1; }
 
-    // per-item cost and item count of task t split b ways
-    void task_items(const Task& t, int b, std::vector<ItemCost>* out, double* total,
-                    int chunk_id_base) const {
+    // C_est of each item of task i split b ways (one per chunk and row
+    // block, chunk-major; every kv head's item costs the same). Memoised: the
+    // search below scores many partitions that share a task's split count.
+    mutable std::vector<std::unordered_map<int, std::vector<double>>> memo;
+    const std::vector<double>& task_costs(size_t i, int b) const {
+        if (memo.size() != P.tasks.size()) memo.assign(P.tasks.size(), {});
+        auto hit = memo[i].find(b);
+        if (hit != memo[i].end()) return hit->second;
+        const Task& t = P.tasks[i];
         const int rpb = rows_per_block(t);
         const int n_rb = (t.rows + rpb - 1) / rpb;
         Span s = t.node >= 0 ? node_span(T.first_offset[t.node], t.n_tok, tile_tokens(t.kind, P.opts, P.thin))
                               : Span{0, t.n_tok, 0, 1, kTileTokens};
+        std::vector<double> c;
+        c.reserve((size_t)b * n_rb);
         for (int k = 0; k < b; ++k) {
             int32_t tb = 0, te = t.n_tok;
             if (t.node >= 0) chunk_range(s, b, k, &tb, &te);
-            for (int rb = 0; rb < n_rb; ++rb) {
-                const int rows_blk = std::min(rpb, t.rows - rb * rpb);
-                const double c = item_cost(t, rows_blk, te - tb);
-                const int hpi = heads_per_item(t);
-                if (total) *total += c * (P.hkv / hpi);
-                if (out)
-                    for (int h = 0; h < P.hkv; h += hpi)
-                        out->push_back({c, chunk_id_base + k, (int16_t)h, (int16_t)rb, item_class(t)});
-            }
+            for (int rb = 0; rb < n_rb; ++rb) c.push_back(item_cost(t, std::min(rpb, t.rows - rb * rpb), te - tb));
         }
+        return memo[i].emplace(b, std::move(c)).first->second;
+    }
+
+    // sum of the item costs of task i split b ways, over the kv heads
+    void add_task_total(size_t i, int b, double* total) const {
+        const int per = P.hkv / heads_per_item(P.tasks[i]);
+        for (double c : task_costs(i, b)) *total += c * per;
     }
 
     double makespan(const std::vector<int>& b, int m) const {
         (void)m;
-        std::vector<ItemCost> v;
-        int cid = 0;
+        std::vector<CostRun> v;
         for (size_t i = 0; i < P.tasks.size(); ++i) {
-            task_items(P.tasks[i], b[i], &v, nullptr, cid);
-            cid += b[i];
+            const Task& t = P.tasks[i];
+            const int hpi = heads_per_item(t);
+            const int32_t n = (P.hkv + hpi - 1) / hpi;
+            const int8_t klass = item_class(t);
+            for (double c : task_costs(i, b[i])) v.push_back({c, n, klass});
         }
-        return simulate_call(std::move(v), num_sms, cc_per_sm);
+        return simulate_call(v, num_sms, cc_per_sm);
     }
 
     // launch class of a task's items (see ItemCost::klass)
@@ -416,8 +437,7 @@ struct Planner {
         };
         auto avg_at = [&](double Tc) {
             double total = 0;
-            for (size_t i = 0; i < nt; ++i)
-                task_items(tasks[i], b_of(i, Tc, tasks[i].max_splits), nullptr, &total, 0);
+            for (size_t i = 0; i < nt; ++i) add_task_total(i, b_of(i, Tc, tasks[i].max_splits), &total);
             return total / m;
         };
         double hi = 0, lo = 1e30;
@@ -942,9 +962,7 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
     W.masks = off; off = align256(off + (int64_t)P->masks.size() * 8);
     W.merge_ptr = off; off = align256(off + (int64_t)P->merge_ptr.size() * 4);
     W.merge_row = off; off = align256(off + (int64_t)P->merge_row.size() * 4);
-    P->tree_pages.assign(T.page_ids.begin(), T.page_ids.end());
-    std::sort(P->tree_pages.begin(), P->tree_pages.end());
-    P->tree_pages.erase(std::unique(P->tree_pages.begin(), P->tree_pages.end()), P->tree_pages.end());
+    P->tree_pages = T.unique_pages;
     W.tree_pages = off; off = align256(off + (int64_t)P->tree_pages.size() * 4);
     W.meta_end = off;
     W.part_o = off; off = align256(off + part_rows * d * 4);

@@ -113,6 +113,7 @@ struct Tree {
     std::vector<int64_t> page_ptr;
     std::vector<int32_t> page_ids;
     std::vector<std::vector<int32_t>> children;
+    std::vector<int32_t> unique_pages;   // every page some node uses, once, ascending
 };
 
 struct HostChunk {

@@ -4,6 +4,7 @@
 // virtual root; an edge p -> c says that p is a prefix of c. Node tokens live in
 // fixed-size pages listed per node (PagedAttention block tables, as in the
 // shared-prefix techniques blog, section 4.3).
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -107,6 +108,9 @@ extern "C" int pst_tree_build(int32_t n_nodes, const int32_t* node_len, const in
     }
     if ((int32_t)T.preorder.size() != n_nodes)
         return bad(PST_ECYCLE, "tree_build: parent array has a cycle (nodes unreachable from the virtual root)");
+    T.unique_pages.assign(T.page_ids.begin(), T.page_ids.end());
+    std::sort(T.unique_pages.begin(), T.unique_pages.end());
+    T.unique_pages.erase(std::unique(T.unique_pages.begin(), T.unique_pages.end()), T.unique_pages.end());
     *out = t;
     return PST_OK;
 }
