@@ -689,31 +689,52 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
             P->groups.push_back(std::move(cur));
             cur = PackedGroup();
         };
-        for (int i = 0; i < N; ++i) {
-            const int32_t n = T.preorder[i];
-            if (T.len[n] == 0 || nq_of(n) == 0) continue;
-            for (int32_t t = 0; t < T.len[n]; ++t) {
+        // tokens [t0, t0 + k) of node n join the run, a page row-range at a time
+        auto append = [&](int32_t n, int32_t t0, int32_t k) {
+            for (int32_t t = t0; t < t0 + k;) {
                 const int64_t pos = (int64_t)T.first_offset[n] + t;
                 const int32_t page = T.page_ids[T.page_ptr[n] + pos / ps];
                 const int32_t row = (int32_t)(pos % ps);
-                const int32_t held = (int32_t)cur.tok_node.size();
-                const bool next_row = held > 0 &&
-                                      ((page == cur_page && row == cur_row + 1) || (cur_row == ps - 1 && row == 0));
-                // joining this token to the run would make it mix nodes (the
-                // walk visits each node's tokens in one stretch)
-                const bool mixes = held > 0 && cur.tok_node.front() != n;
-                const int32_t limit = mixes ? std::min(o.fixed_chunk, kMaskTokens) : o.fixed_chunk;
-                if (held > 0 && (!next_row || held >= limit)) flush();
+                const int32_t m = std::min(t0 + k - t, ps - row);
                 if (cur.tok_node.empty()) {
                     cur.page_list.assign(1, page);
                     cur.pos_begin = row;
                 } else if (page != cur_page) {
                     cur.page_list.push_back(page);
                 }
-                cur.tok_node.push_back(n);
-                cur.tok_t.push_back(t);
+                cur.tok_node.insert(cur.tok_node.end(), m, n);
+                for (int32_t j = 0; j < m; ++j) cur.tok_t.push_back(t + j);
                 cur_page = page;
-                cur_row = row;
+                cur_row = row + m - 1;
+                t += m;
+            }
+        };
+        for (int i = 0; i < N; ++i) {
+            const int32_t n = T.preorder[i];
+            if (T.len[n] == 0 || nq_of(n) == 0) continue;
+            // A node's tokens follow one another on its pages (the next row, or
+            // row 0 after the last row), so within the node a run ends only at
+            // its length limit; the first token may also end it for want of
+            // page continuity with the run so far.
+            for (int32_t t = 0; t < T.len[n];) {
+                const int64_t pos = (int64_t)T.first_offset[n] + t;
+                const int32_t page = T.page_ids[T.page_ptr[n] + pos / ps];
+                const int32_t row = (int32_t)(pos % ps);
+                int32_t held = (int32_t)cur.tok_node.size();
+                const bool next_row = held > 0 &&
+                                      ((page == cur_page && row == cur_row + 1) || (cur_row == ps - 1 && row == 0));
+                // joining this token to the run would make it mix nodes (the
+                // walk visits each node's tokens in one stretch)
+                const bool mixes = held > 0 && cur.tok_node.front() != n;
+                int32_t limit = mixes ? std::min(o.fixed_chunk, kMaskTokens) : o.fixed_chunk;
+                if (held > 0 && (!next_row || held >= limit)) {
+                    flush();
+                    held = 0;
+                    limit = o.fixed_chunk;
+                }
+                const int32_t k = std::min(T.len[n] - t, limit - held);
+                append(n, t, k);
+                t += k;
             }
         }
         flush();
