@@ -100,16 +100,35 @@ def measured_peaks():
 
 
 def kernel_sources_sha():
+    """Digest of the sources that build the kernels (.cu, .cuh and .h under
+    csrc). The host planner's sources are left out: what it produces enters a
+    traffic record through the plan digest."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "prefix_shared_tree_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(kernel, workload):
-    """DRAM bytes per launch of `kernel` from a committed ncu summary, if its
-    kernel sources are the ones built now."""
+def plan_digest(plan):
+    """Digest of a plan: its exported index, chunks and merge lists, and its
+    stats without the host time. A launch's DRAM traffic depends on the
+    kernels and on the items the plan gives them."""
+    import numpy as np
+    h = hashlib.sha256()
+    ex = plan.export()
+    for k in sorted(ex):
+        h.update(k.encode())
+        h.update(np.ascontiguousarray(ex[k]).tobytes())
+    st = {k: v for k, v in plan.stats().items() if k != "plan_us"}
+    h.update(json.dumps(st, sort_keys=True, default=float).encode())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload, digest):
+    """DRAM bytes per launch of `kernel` from a committed ncu summary, if it
+    was taken with the kernels built now and with the same plan."""
     p = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.json")
     if not os.path.exists(p):
         return None
@@ -117,7 +136,7 @@ def recorded_traffic(kernel, workload):
         d = json.load(open(p))
     except Exception:
         return None
-    if d.get("sources_sha") != kernel_sources_sha():
+    if d.get("sources_sha") != kernel_sources_sha() or d.get("plan_digest") != digest:
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -423,7 +442,8 @@ def measure(name, args, dev, steps, warmup, timer_steps, plan_opts, e2e=False, w
                  "split_policy": {0: "cost_model", 1: "none", 2: "uniform", 3: "flatten"}[int(st["split_policy"])],
                  "fixed_chunk": int(st["fixed_chunk"]),
                  "n_chunks": st["n_chunks"], "n_items": st["n_items"], "n_tc_items": st["n_tc_items"],
-                 "n_cc_items": st["n_cc_items"], "n_partial_rows": st["n_partial_rows"]},
+                 "n_cc_items": st["n_cc_items"], "n_partial_rows": st["n_partial_rows"],
+                 "digest": plan_digest(att.plan)},
         "n_launches": int(st["n_launches"]),
         "group_end_us": {k: v for k, v in group_us.items() if k != "por"},
         "por_us": group_us["por"],
@@ -580,7 +600,7 @@ def run_ours(args, rank, world):
     U = h["U"]
     wl = h["wl"]
     achieved_gbs = U / (us * 1e-6) / 1e9
-    traffic = recorded_traffic(h["dom"], args.workload)
+    traffic = recorded_traffic(h["dom"], args.workload, h["plan"]["digest"])
     line = {
         "metric": METRIC,
         "value": round(us, 3),

@@ -402,7 +402,25 @@ struct Planner {
         for (double c : task_costs(i, b)) *total += c * per;
     }
 
+    // makespan of split vector b: memoised, since the candidate partitions
+    // the search scores often coincide (the factors and the uniform sizes
+    // map most tasks to the same split counts)
+    struct VecHash {
+        size_t operator()(const std::vector<int>& b) const {
+            uint64_t h = 1469598103934665603ull;
+            for (int x : b) h = (h ^ (uint32_t)x) * 1099511628211ull;
+            return (size_t)h;
+        }
+    };
+    mutable std::unordered_map<std::vector<int>, double, VecHash> mk_memo;
     double makespan(const std::vector<int>& b, int m) const {
+        auto hit = mk_memo.find(b);
+        if (hit != mk_memo.end()) return hit->second;
+        const double mk = simulate(b, m);
+        mk_memo.emplace(b, mk);
+        return mk;
+    }
+    double simulate(const std::vector<int>& b, int m) const {
         (void)m;
         std::vector<CostRun> v;
         for (size_t i = 0; i < P.tasks.size(); ++i) {
