@@ -580,10 +580,13 @@ static bool build_packed_group(const Tree& T, int32_t root, const std::vector<in
 }
 
 // Plan creation; with `prev` the KV-axis splits are taken from it instead of
-// being searched (pst_plan_update).
+// being searched (pst_plan_update). With `score_only` the build stops once
+// the predicted makespan is known: a DEFT-Flatten run then keeps its token
+// count, nodes and queries, not its per-token records or masks, and no
+// chunks, items or metadata are made (the plan is good for its makespan only).
 static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* query_node, int32_t n_q_heads,
                       int32_t n_kv_heads, int32_t d, pst_dtype dtype, const pst_plan_opts* opts,
-                      const pst_plan* prev, const int32_t* prev_node, pst_plan** out) {
+                      const pst_plan* prev, const int32_t* prev_node, pst_plan** out, bool score_only = false) {
     const auto t_start = std::chrono::steady_clock::now();
     if (!out) return fail(PST_EINVAL, "plan_create: out is null");
     *out = nullptr;
@@ -682,6 +685,7 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
 
     // ---- packing: a page-contiguous set of descendants of <= 64 tokens
     std::vector<int32_t> packed_in(N, -1);
+    std::vector<int32_t> run_tokens;   // tokens of each DEFT-Flatten run (groups made below)
     if (o.split_policy == PST_SPLIT_FLATTEN) {
         // DEFT-Flatten: walk the nodes some query sees in depth-first order
         // and cut their tokens into runs of at most fixed_chunk (S_t); a run
@@ -693,22 +697,36 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
         const int32_t ps = T.page_size;
         PackedGroup cur;
         int32_t cur_page = -1, cur_row = -1;
+        int32_t held_tok = 0;   // tokens in the run so far
         auto flush = [&]() {
-            if (cur.tok_node.empty()) return;
+            if (held_tok == 0) return;
             cur.root = -1;
-            cur.nodes.clear();   // the run's nodes, in walk order (each node's tokens are consecutive)
-            for (int32_t n : cur.tok_node)
-                if (cur.nodes.empty() || cur.nodes.back() != n) cur.nodes.push_back(n);
+            if (!score_only) {
+                cur.nodes.clear();   // the run's nodes, in walk order (each node's tokens are consecutive)
+                for (int32_t n : cur.tok_node)
+                    if (cur.nodes.empty() || cur.nodes.back() != n) cur.nodes.push_back(n);
+            }
             // one node: every query sees every token, no mask (and the run may
             // be longer than the 64 bits of one)
-            set_queries_and_masks(cur, cur.nodes, cur.nodes.size() > 1);
+            set_queries_and_masks(cur, cur.nodes, !score_only && cur.nodes.size() > 1);
             const int32_t gid = (int32_t)P->groups.size();
-            for (int32_t n : cur.tok_node) packed_in[n] = gid;   // every flattened node is in some run
+            for (int32_t n : cur.nodes) packed_in[n] = gid;   // every flattened node is in some run
+            run_tokens.push_back(held_tok);
             P->groups.push_back(std::move(cur));
             cur = PackedGroup();
+            held_tok = 0;
         };
         // tokens [t0, t0 + k) of node n join the run, a page row-range at a time
         auto append = [&](int32_t n, int32_t t0, int32_t k) {
+            if (score_only) {   // the count, the nodes and where the run ends
+                if (cur.nodes.empty() || cur.nodes.back() != n) cur.nodes.push_back(n);
+                const int64_t last = (int64_t)T.first_offset[n] + t0 + k - 1;
+                cur_page = T.page_ids[T.page_ptr[n] + last / ps];
+                cur_row = (int32_t)(last % ps);
+                held_tok += k;
+                return;
+            }
+            held_tok += k;
             for (int32_t t = t0; t < t0 + k;) {
                 const int64_t pos = (int64_t)T.first_offset[n] + t;
                 const int32_t page = T.page_ids[T.page_ptr[n] + pos / ps];
@@ -738,12 +756,12 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
                 const int64_t pos = (int64_t)T.first_offset[n] + t;
                 const int32_t page = T.page_ids[T.page_ptr[n] + pos / ps];
                 const int32_t row = (int32_t)(pos % ps);
-                int32_t held = (int32_t)cur.tok_node.size();
+                int32_t held = held_tok;
                 const bool next_row = held > 0 &&
                                       ((page == cur_page && row == cur_row + 1) || (cur_row == ps - 1 && row == 0));
                 // joining this token to the run would make it mix nodes (the
                 // walk visits each node's tokens in one stretch)
-                const bool mixes = held > 0 && cur.tok_node.front() != n;
+                const bool mixes = held > 0 && (score_only ? cur.nodes.front() : cur.tok_node.front()) != n;
                 int32_t limit = mixes ? std::min(o.fixed_chunk, kMaskTokens) : o.fixed_chunk;
                 if (held > 0 && (!next_row || held >= limit)) {
                     flush();
@@ -810,7 +828,7 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
         t.group = (int32_t)gi;
         t.n_q = (int32_t)g.queries.size();
         t.rows = t.n_q * G;
-        t.n_tok = (int32_t)g.tok_node.size();
+        t.n_tok = gi < run_tokens.size() ? run_tokens[gi] : (int32_t)g.tok_node.size();
         t.kind = (tc_ok && t.rows >= o.tc_min_rows) ? 1 : 0;
         t.max_splits = 1;
         P->tasks.push_back(t);
@@ -869,6 +887,10 @@ static int plan_build(const pst_tree* tree, int32_t n_queries, const int32_t* qu
         std::vector<int> b(P->tasks.size());
         for (size_t i = 0; i < b.size(); ++i) b[i] = P->tasks[i].b_k;
         P->makespan_us = pl.makespan(b, m);
+    }
+    if (score_only) {
+        *out = guard.release();
+        return PST_OK;
     }
 
     // ---- chunks, pages, chunk queries, masks, partial rows
@@ -1041,25 +1063,37 @@ extern "C" int pst_plan_create(const pst_tree* tree, int32_t n_queries, const in
     const auto t0 = std::chrono::steady_clock::now();
     int rc = plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, opts, nullptr, nullptr, out);
     if (rc != PST_OK) return rc;
-    pst_plan* best = *out;
-    if (best->opts.split_policy != PST_SPLIT_COST_MODEL || best->opts.flatten_candidates < 0) return rc;
+    if ((*out)->opts.split_policy != PST_SPLIT_COST_MODEL || (*out)->opts.flatten_candidates < 0) return rc;
+    // score each candidate without building it; build the winner, if any
+    const double ref = (*out)->makespan_us;   // the node partition's
+    double best_mk = ref;
+    int32_t best_st = 0;
     for (int32_t st : kFlattenCandidates) {
         pst_plan_opts fo = (*out)->opts;
         fo.split_policy = PST_SPLIT_FLATTEN;
         fo.fixed_chunk = st;
         pst_plan* alt = nullptr;
-        if (plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, &fo, nullptr, nullptr, &alt) !=
-            PST_OK)
+        if (plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, &fo, nullptr, nullptr, &alt,
+                       true) != PST_OK)
             continue;
-        const double ref = (*out)->makespan_us;   // the node partition's
-        if (alt->makespan_us < kFlattenMargin * ref && alt->makespan_us < best->makespan_us) std::swap(best, alt);
-        if (alt != *out) pst_plan_destroy(alt);
+        if (alt->makespan_us < kFlattenMargin * ref && alt->makespan_us < best_mk) {
+            best_mk = alt->makespan_us;
+            best_st = st;
+        }
+        pst_plan_destroy(alt);
     }
-    if (best != *out) {
-        pst_plan_destroy(*out);
-        *out = best;
+    if (best_st > 0) {
+        pst_plan_opts fo = (*out)->opts;
+        fo.split_policy = PST_SPLIT_FLATTEN;
+        fo.fixed_chunk = best_st;
+        pst_plan* alt = nullptr;
+        if (plan_build(tree, n_queries, query_node, n_q_heads, n_kv_heads, d, dtype, &fo, nullptr, nullptr, &alt) ==
+            PST_OK) {
+            pst_plan_destroy(*out);
+            *out = alt;
+        }
     }
-    best->plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
+    (*out)->plan_us = std::chrono::duration<double, std::micro>(std::chrono::steady_clock::now() - t0).count();
     return PST_OK;
 }
 
