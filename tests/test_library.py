@@ -189,28 +189,53 @@ def test_deft_flatten_chunks_of_a_hand_laid_tree(lib):
                         (c2, [1], [all_ones])]
 
 
-@pytest.mark.parametrize("make", [lambda: synth.tree_of_thought("gqa"), synth.document_qa, synth.few_shot,
-                                  synth.speculative, lambda: synth.random_tree(1007)],
-                         ids=["tot_gqa", "document_qa", "few_shot", "speculative", "random"])
-def test_cost_model_scores_flatten_candidates(lib, make):
+def _same_export(a, b):
+    return a.keys() == b.keys() and all(np.array_equal(a[k], b[k]) for k in a)
+
+
+# (the flattened control of document QA on 148 SMs is a case the flattened
+# chunking wins under the measured tables)
+@pytest.mark.parametrize("make,sms", [(lambda: synth.tree_of_thought("gqa"), 152), (synth.document_qa, 152),
+                                      (synth.few_shot, 152), (synth.speculative, 152),
+                                      (lambda: synth.random_tree(1007), 152),
+                                      (lambda: synth.flat_control(synth.document_qa()), 148)],
+                         ids=["tot_gqa", "document_qa", "few_shot", "speculative", "random", "document_qa_flat"])
+def test_cost_model_scores_flatten_candidates(lib, make, sms):
     """The cost-model policy also scores DEFT-Flatten chunkings of 1024 and
     2048 tokens and keeps one only when its predicted makespan is at least
     3 % below the node partition's; switched off, the node partition stays.
     The rule is checked against plans built separately (whichever way the
-    measured cost tables decide it for this workload)."""
+    measured cost tables decide it for this workload), and the plan kept is
+    the separately built one, array for array."""
     wl = make()
-    node = _plan(lib, wl, flatten_candidates=False).stats()
+    node_plan = _plan(lib, wl, flatten_candidates=False, num_sms=sms)
+    node = node_plan.stats()
     assert node["split_policy"] == 0
-    flat = {st: _plan(lib, wl, split_policy="flatten", fixed_chunk=st).stats()["predicted_makespan_us"]
-            for st in (1024, 2048)}
-    chosen = _plan(lib, wl).stats()
+    flat_plans = {st: _plan(lib, wl, split_policy="flatten", fixed_chunk=st, num_sms=sms) for st in (1024, 2048)}
+    flat = {st: p.stats()["predicted_makespan_us"] for st, p in flat_plans.items()}
+    chosen_plan = _plan(lib, wl, num_sms=sms)
+    chosen = chosen_plan.stats()
     best_st = min(flat, key=lambda st: (flat[st], st))
     if flat[best_st] < 0.97 * node["predicted_makespan_us"]:
         assert chosen["split_policy"] == 3 and chosen["fixed_chunk"] == best_st
         assert chosen["predicted_makespan_us"] == flat[best_st]
+        assert _same_export(chosen_plan.export(), flat_plans[best_st].export())
     else:
         assert chosen["split_policy"] == 0
         assert chosen["predicted_makespan_us"] == node["predicted_makespan_us"]
+        assert _same_export(chosen_plan.export(), node_plan.export())
+
+
+def test_flatten_wins_somewhere(lib):
+    """The flattened winner is reachable (so the test above can check it):
+    under the measured tables some no-sharing control flattens on some SM
+    count (the 148-SM document-QA control is the case the test above uses)."""
+    wins = []
+    for make in (lambda: synth.flat_control(synth.document_qa()), lambda: synth.flat_control(synth.speculative())):
+        wl = make()
+        for sms in (148, 64, 8):
+            wins.append(_plan(lib, wl, num_sms=sms).stats()["split_policy"] == 3)
+    assert any(wins)
 
 
 def test_speculative_drafts_are_packed_with_masks(lib):
