@@ -81,3 +81,24 @@ def test_list_schedule_rejects_bad_input(lib):
         lib.list_schedule([1.0], 0)
     slot, mk = lib.list_schedule([], 3)
     assert slot.size == 0 and mk == 0.0
+
+
+@pytest.mark.parametrize("n_tok,chunk,sms", [(8192, 1024, 20), (8192, 1536, 20), (8192, 1536, 7),
+                                             (9000, 4096, 3), (20000, 2560, 152)])
+def test_predicted_makespan_is_the_list_schedule_of_one_launch(lib, n_tok, chunk, sms):
+    """A plan whose items all belong to one tensor-core launch is dispatched
+    largest first onto the SMs, one block each: its predicted makespan is the
+    list schedule (above) of its items' C_est. One node of n_tok tokens seen
+    by 64 queries x 4 q-heads per kv head (256 rows: tensor cores, P rounded
+    once), 8 kv heads, uniform chunks; the chunk lengths come from the plan,
+    the costs from the cost model's own estimate."""
+    n_pages = (n_tok + 15) // 16
+    t = lib.tree_build([n_tok], [-1], [0, n_pages], list(range(n_pages)), None, 16, n_pages)
+    p = lib.plan_create(t, [0] * 64, 32, 8, 128, "bf16", split_policy="uniform", fixed_chunk=chunk, num_sms=sms)
+    st, ex = p.stats(), p.export()
+    assert st["n_cc_items"] == 0
+    lens = np.diff(ex["chunk_tok_ptr"])
+    costs = [lib.cost_estimate(1, 256, int(n)) for n in lens for _ in range(8)]
+    assert st["n_tc_items"] == len(costs)
+    _, mk = lib.list_schedule(costs, sms)
+    assert st["predicted_makespan_us"] == pytest.approx(mk, rel=1e-12)
